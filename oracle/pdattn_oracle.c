@@ -1,0 +1,279 @@
+/*
+ * Plain CPU oracle for one decode step of grouped-query attention over a
+ * paged KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may load this file's library.  It shares no
+ * code with the CUDA path (no headers, helpers or tables) and is deliberately
+ * slow: serial loops, fp64 wherever the pages leave the precision open.
+ *
+ * What each function follows (page title, section):
+ *   oracle_rope_tables   Llama example page, "src/rope.linnet" (`tables`):
+ *                        inv_freq from theta and iota in f32, angles = s *
+ *                        inv_freq, full = concat(angles, angles), cos and sin
+ *                        cast to T.
+ *   oracle_rope_write_kv Llama example page, "src/attention.linnet"
+ *                        (`decode`): rope on q and the new k at pos, then
+ *                        write_at of k and v; the paged slot comes from the
+ *                        llama-3.1-8b-instruct architecture page, entry table
+ *                        (`decode_paged`, `table: Tensor[Rows, Pages; i32]`)
+ *                        and the `PageSize: Dim = 64` generic of
+ *                        GroupedQueryAttention.
+ *   oracle_decode        Llama example page, "src/attention.linnet"
+ *                        (`decode`): mask seen[s] = s <= pos, scale
+ *                        rsqrt(f32(head dim)), grouped attention where query
+ *                        head h reads kv head h / (Heads / KvHeads) ("Key
+ *                        ideas", grouped-query attention); sliding window from
+ *                        the gpt-oss-20b architecture page (`window: i32`).
+ *
+ * Readings where the pages leave a step open:
+ *   - rope(x, cos, sin) = x * cos + rotate_half(x) * sin with
+ *     rotate_half(x) = concat(-x[D/2:], x[:D/2]); the halves share frequency i
+ *     because the table is concat(angles, angles).  Each product is an f32
+ *     product, the sum one f32 add, the result rounded once to T.  The
+ *     rotation direction is a convention the pages do not print: parity for
+ *     the direction alone is unpinned.
+ *   - cos, sin, exp and log are the correctly rounded f32 results, computed
+ *     in double and rounded to f32 (then to T for the tables).
+ *   - Attention scores, softmax and the weighted sum are computed in double
+ *     and the output rounded once to T.
+ *   - window W > 0 attends positions in (pos - W, pos]; W <= 0 attends [0, pos].
+ *
+ * Element types: dtype 0 = bf16 (stored as uint16 bit patterns), 1 = f32.
+ * Build with -ffp-contract=off so that no product and sum fuse.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+    int32_t rows, heads, kv_heads, head_dim;
+    int32_t page_size, pages_per_row, num_pages;
+    int32_t dtype;      /* 0 = bf16, 1 = f32 */
+    int32_t window;     /* <= 0: every cached position up to pos */
+    float rope_theta;   /* <= 0: no rotation (GPT-2: learned positions upstream) */
+} oracle_shape;
+
+enum { ORACLE_OK = 0, ORACLE_EINVAL = 1, ORACLE_EBADPAGE = 4 };
+
+/* ---- element access ---------------------------------------------------- */
+
+static float bf16_bits_to_float(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round an f32 to bf16, to nearest with ties to even. */
+static uint16_t float_to_bf16_bits(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u) /* NaN stays NaN */
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t keep = u >> 16;
+    uint32_t rest = u & 0xffffu;
+    if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u)))
+        keep += 1u;
+    return (uint16_t)keep;
+}
+
+static float load_t(const void* base, size_t i, int dtype) {
+    if (dtype == 0) return bf16_bits_to_float(((const uint16_t*)base)[i]);
+    return ((const float*)base)[i];
+}
+
+/* Round an f32 value to T and store it. */
+static void store_t(void* base, size_t i, float v, int dtype) {
+    if (dtype == 0) ((uint16_t*)base)[i] = float_to_bf16_bits(v);
+    else ((float*)base)[i] = v;
+}
+
+/* Round an f32 value to T and return it as f32. */
+static float round_t(float v, int dtype) {
+    return dtype == 0 ? bf16_bits_to_float(float_to_bf16_bits(v)) : v;
+}
+
+static void copy_t(void* dst, size_t di, const void* src, size_t si, int dtype) {
+    if (dtype == 0) ((uint16_t*)dst)[di] = ((const uint16_t*)src)[si];
+    else ((float*)dst)[di] = ((const float*)src)[si];
+}
+
+/* ---- rotary tables ----------------------------------------------------- */
+
+/* inv_freq[i] = exp(-(f32(i) * 2.0 / f32(D)) * log(theta)), all in f32. */
+static float inv_freq_f32(int i, int D, float theta) {
+    float two_i = (float)i * 2.0f;
+    float ratio = two_i / (float)D;
+    float log_theta = (float)log((double)theta);
+    float arg = (-ratio) * log_theta;
+    return (float)exp((double)arg);
+}
+
+/* cos and sin (f32, not yet rounded to T) of f32(s) * inv_freq[i]. */
+static void angle_cos_sin(int s, int i, int D, float theta, float* c, float* sn) {
+    float angle = (float)s * inv_freq_f32(i, D, theta);
+    *c = (float)cos((double)angle);
+    *sn = (float)sin((double)angle);
+}
+
+/* Tables [S, D] of T: column i and i + D/2 hold the same frequency. */
+int oracle_rope_tables(float theta, int D, int S, int dtype, void* cos_out, void* sin_out) {
+    if (D <= 0 || D % 2 != 0 || S < 0 || theta <= 0.0f || (dtype != 0 && dtype != 1))
+        return ORACLE_EINVAL;
+    int half = D / 2;
+    for (int s = 0; s < S; ++s) {
+        for (int j = 0; j < D; ++j) {
+            float c, sn;
+            angle_cos_sin(s, j % half, D, theta, &c, &sn);
+            store_t(cos_out, (size_t)s * D + j, c, dtype);
+            store_t(sin_out, (size_t)s * D + j, sn, dtype);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* rope of one head vector x[D] (T) at position pos into y[D] (T). */
+static void rope_vector(const void* x, size_t xo, void* y, size_t yo, int D, int pos,
+                        float theta, int dtype) {
+    int half = D / 2;
+    for (int j = 0; j < D; ++j) {
+        float c, sn;
+        angle_cos_sin(pos, j % half, D, theta, &c, &sn);
+        c = round_t(c, dtype);   /* cos(full) and sin(full) are cast to T */
+        sn = round_t(sn, dtype);
+        float xj = load_t(x, xo + j, dtype);
+        /* rotate_half(x)[j] = -x[j + D/2] for j < D/2, x[j - D/2] otherwise */
+        float rh = j < half ? -load_t(x, xo + j + half, dtype) : load_t(x, xo + j - half, dtype);
+        float a = xj * c;
+        float b = rh * sn;
+        store_t(y, yo + j, a + b, dtype);
+    }
+}
+
+static int shape_ok(const oracle_shape* p) {
+    if (!p) return 0;
+    if (p->rows < 0 || p->heads <= 0 || p->kv_heads <= 0 || p->heads % p->kv_heads != 0) return 0;
+    if (p->head_dim <= 0 || p->head_dim % 2 != 0) return 0;
+    if (p->page_size <= 0 || p->pages_per_row <= 0 || p->num_pages <= 0) return 0;
+    if (p->dtype != 0 && p->dtype != 1) return 0;
+    return 1;
+}
+
+/* Pool element index of (page, kv head, offset, d) in [NumPages, KvHeads, PageSize, D]. */
+static size_t pool_index(const oracle_shape* p, int page, int kvh, int off, int d) {
+    return (((size_t)page * p->kv_heads + kvh) * p->page_size + off) * p->head_dim + d;
+}
+
+/*
+ * RoPE on q [R, Hq, D] and k_new [R, Hk, D] at positions[r]; q_out receives
+ * the rotated q, and the rotated k and the unrotated v_new go into the pool
+ * slot table[r, pos / PageSize], offset pos % PageSize.
+ */
+int oracle_rope_write_kv(const oracle_shape* p, const void* q, const void* k_new,
+                         const void* v_new, const int32_t* positions, const int32_t* table,
+                         void* q_out, void* k_pool, void* v_pool) {
+    if (!shape_ok(p)) return ORACLE_EINVAL;
+    const int D = p->head_dim, Hq = p->heads, Hk = p->kv_heads, PS = p->page_size;
+    int status = ORACLE_OK;
+    for (int r = 0; r < p->rows; ++r) {
+        int pos = positions[r];
+        if (pos < 0 || pos >= p->pages_per_row * PS) { status = ORACLE_EINVAL; continue; }
+        int page = table[(size_t)r * p->pages_per_row + pos / PS];
+        int off = pos % PS;
+        for (int h = 0; h < Hq; ++h) {
+            size_t o = ((size_t)r * Hq + h) * D;
+            if (p->rope_theta > 0.0f) rope_vector(q, o, q_out, o, D, pos, p->rope_theta, p->dtype);
+            else for (int d = 0; d < D; ++d) copy_t(q_out, o + d, q, o + d, p->dtype);
+        }
+        if (page < 0 || page >= p->num_pages) { status = ORACLE_EBADPAGE; continue; }
+        for (int h = 0; h < Hk; ++h) {
+            size_t o = ((size_t)r * Hk + h) * D;
+            size_t slot = pool_index(p, page, h, off, 0);
+            if (p->rope_theta > 0.0f) rope_vector(k_new, o, k_pool, slot, D, pos, p->rope_theta, p->dtype);
+            else for (int d = 0; d < D; ++d) copy_t(k_pool, slot + d, k_new, o + d, p->dtype);
+            for (int d = 0; d < D; ++d) copy_t(v_pool, slot + d, v_new, o + d, p->dtype);
+        }
+    }
+    return status;
+}
+
+/*
+ * Attention of the rotated queries q_rot [R, Hq, D] over the cached positions
+ * of each row.  out [R, Hq, D] is rounded to T; out64 (may be NULL) receives
+ * the unrounded double result.
+ */
+int oracle_decode(const oracle_shape* p, const void* q_rot, const int32_t* positions,
+                  const int32_t* table, const void* k_pool, const void* v_pool, void* out,
+                  double* out64) {
+    if (!shape_ok(p)) return ORACLE_EINVAL;
+    const int D = p->head_dim, Hq = p->heads, Hk = p->kv_heads, PS = p->page_size;
+    const int group = Hq / Hk;
+    const double scale = (double)(float)(1.0 / sqrt((double)D)); /* rsqrt(f32(D)) */
+    int max_ctx = p->pages_per_row * PS;
+    double* scores = (double*)malloc(sizeof(double) * (size_t)max_ctx);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)D);
+    if (!scores || !acc) { free(scores); free(acc); return ORACLE_EINVAL; }
+    int status = ORACLE_OK;
+    for (int r = 0; r < p->rows; ++r) {
+        int pos = positions[r];
+        if (pos < 0 || pos >= max_ctx) { status = ORACLE_EINVAL; continue; }
+        int lo = 0;
+        if (p->window > 0 && pos - p->window + 1 > 0) lo = pos - p->window + 1;
+        int bad = 0;
+        for (int t = lo; t <= pos; ++t) {
+            int page = table[(size_t)r * p->pages_per_row + t / PS];
+            if (page < 0 || page >= p->num_pages) bad = 1;
+        }
+        if (bad) { status = ORACLE_EBADPAGE; continue; }
+        for (int h = 0; h < Hq; ++h) {
+            int kvh = h / group;
+            size_t qo = ((size_t)r * Hq + h) * D;
+            double m = -INFINITY;
+            for (int t = lo; t <= pos; ++t) {
+                int page = table[(size_t)r * p->pages_per_row + t / PS];
+                size_t ko = pool_index(p, page, kvh, t % PS, 0);
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d)
+                    dot += (double)load_t(q_rot, qo + d, p->dtype) * (double)load_t(k_pool, ko + d, p->dtype);
+                scores[t - lo] = scale * dot;
+                if (scores[t - lo] > m) m = scores[t - lo];
+            }
+            double l = 0.0;
+            for (int t = lo; t <= pos; ++t) {
+                scores[t - lo] = exp(scores[t - lo] - m);
+                l += scores[t - lo];
+            }
+            for (int d = 0; d < D; ++d) acc[d] = 0.0;
+            for (int t = lo; t <= pos; ++t) {
+                int page = table[(size_t)r * p->pages_per_row + t / PS];
+                size_t vo = pool_index(p, page, kvh, t % PS, 0);
+                double w = scores[t - lo] / l;
+                for (int d = 0; d < D; ++d) acc[d] += w * (double)load_t(v_pool, vo + d, p->dtype);
+            }
+            for (int d = 0; d < D; ++d) {
+                if (out64) out64[qo + d] = acc[d];
+                store_t(out, qo + d, (float)acc[d], p->dtype);
+            }
+        }
+    }
+    free(scores);
+    free(acc);
+    return status;
+}
+
+/*
+ * One whole step: rope + cache write, then attention of the rotated queries.
+ * q_rot is caller scratch of the size of q.
+ */
+int oracle_step(const oracle_shape* p, const void* q, const void* k_new, const void* v_new,
+                const int32_t* positions, const int32_t* table, void* k_pool, void* v_pool,
+                void* q_rot, void* out, double* out64) {
+    int s1 = oracle_rope_write_kv(p, q, k_new, v_new, positions, table, q_rot, k_pool, v_pool);
+    int s2 = oracle_decode(p, q_rot, positions, table, k_pool, v_pool, out, out64);
+    return s1 != ORACLE_OK ? s1 : s2;
+}
+
+/* Exposed for pins on the rounding helper itself. */
+uint16_t oracle_f32_to_bf16(float f) { return float_to_bf16_bits(f); }

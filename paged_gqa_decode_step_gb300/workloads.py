@@ -1,0 +1,187 @@
+"""Seeded synthetic inputs for the paged decode step.
+
+This module only draws random numbers and lays out page tables; it holds none
+of the method's arithmetic, so that the CPU oracle and the CUDA path can both
+be fed from it without sharing any computation.
+
+The shapes follow the model pages:
+  * llama-3.1-8b-instruct architecture page, "Generics" (H 4096, Heads 32,
+    KvHeads 8, MaxSeq 8192) and GroupedQueryAttention (PageSize 64);
+  * gpt-oss-20b architecture page, "Generics" (Heads 64, KvHeads 8, HeadDim 64,
+    Window 128, MaxSeq 4096);
+  * gpt2 architecture page, "Generics" (H 768, Heads 12, MaxSeq 1024, T f32).
+
+Recipe (every workload): draws come from one ``torch.Generator`` seeded with
+the workload's seed, in the order positions -> page permutation -> q -> k_new
+-> v_new -> k_pool -> v_pool.  Values are N(0, 1) drawn in f32 and rounded to
+the element type.  The pool holds sum_r ceil((pos_r + 1) / 64) pages plus 10%
+spare (or an explicit count); page ids are a seeded permutation of the pool,
+handed to rows in row order, and table entries past a row's last page are -1.
+The prefilled pool stands for keys that were rotated when they were written.
+"""
+from dataclasses import dataclass, field, replace
+import math
+from typing import Optional, Sequence
+
+import torch
+
+PAGE_SIZE = 64
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    rows: int
+    heads: int
+    kv_heads: int
+    head_dim: int
+    pages_per_row: int
+    dtype: str                      # "bf16" or "f32"
+    rope_theta: float               # <= 0: no rotation
+    window: int = 0                 # <= 0: attend every position up to pos
+    positions: str = "uniform"      # "fixed" | "uniform" | "loguniform_ctx"
+    pos_lo: int = 0
+    pos_hi: int = 0
+    fixed_positions: Sequence[int] = field(default_factory=tuple)
+    num_pages: int = 0              # 0: needed pages + 10% spare
+    seed: int = 0
+
+    @property
+    def group(self) -> int:
+        return self.heads // self.kv_heads
+
+    @property
+    def max_seq(self) -> int:
+        return self.pages_per_row * PAGE_SIZE
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    @property
+    def elem_bytes(self) -> int:
+        return 2 if self.dtype == "bf16" else 4
+
+
+# The five workloads, in the order they are listed for this step.
+TINY = Workload("tiny", rows=2, heads=8, kv_heads=8, head_dim=64, pages_per_row=8, dtype="bf16",
+                rope_theta=10000.0, positions="fixed", fixed_positions=(37, 100), num_pages=16,
+                seed=1000)
+LLAMA_LAYER = Workload("llama8b_layer", rows=32, heads=32, kv_heads=8, head_dim=128,
+                       pages_per_row=128, dtype="bf16", rope_theta=500000.0, positions="uniform",
+                       pos_lo=1024, pos_hi=8191, seed=1001)
+LLAMA_SERVING = Workload("llama8b_serving", rows=256, heads=32, kv_heads=8, head_dim=128,
+                         pages_per_row=128, dtype="bf16", rope_theta=500000.0,
+                         positions="loguniform_ctx", pos_lo=16, pos_hi=8192, seed=1002)
+GPTOSS_FULL = Workload("gptoss20b_full", rows=64, heads=64, kv_heads=8, head_dim=64,
+                       pages_per_row=64, dtype="bf16", rope_theta=150000.0, window=0,
+                       positions="uniform", pos_lo=256, pos_hi=4095, seed=1003)
+GPTOSS_SLIDING = replace(GPTOSS_FULL, name="gptoss20b_sliding", window=128)
+GPT2 = Workload("gpt2_f32", rows=128, heads=12, kv_heads=12, head_dim=64, pages_per_row=16,
+                dtype="f32", rope_theta=0.0, positions="uniform", pos_lo=1, pos_hi=1023,
+                seed=1004)
+
+WORKLOADS = {w.name: w for w in (TINY, LLAMA_LAYER, LLAMA_SERVING, GPTOSS_FULL, GPTOSS_SLIDING, GPT2)}
+
+
+def draw_positions(w: Workload, gen: torch.Generator) -> torch.Tensor:
+    """Positions [rows] int32 on the generator's device."""
+    dev = gen.device
+    if w.positions == "fixed":
+        assert len(w.fixed_positions) == w.rows
+        return torch.tensor(list(w.fixed_positions), dtype=torch.int32, device=dev)
+    if w.positions == "uniform":
+        return torch.randint(w.pos_lo, w.pos_hi + 1, (w.rows,), generator=gen, device=dev,
+                             dtype=torch.int64).to(torch.int32)
+    if w.positions == "loguniform_ctx":
+        u = torch.rand((w.rows,), generator=gen, device=dev, dtype=torch.float64)
+        lo, hi = math.log(w.pos_lo), math.log(w.pos_hi)
+        ctx = torch.floor(torch.exp(lo + (hi - lo) * u)).clamp(w.pos_lo, w.pos_hi)
+        return (ctx - 1).to(torch.int32)
+    raise ValueError(w.positions)
+
+
+def pages_needed(positions: torch.Tensor) -> torch.Tensor:
+    """Pages each row owns: ceil((pos + 1) / 64)."""
+    return (positions.to(torch.int64) + PAGE_SIZE) // PAGE_SIZE
+
+
+def generate(w: Workload, device="cpu", seed: Optional[int] = None, poison: bool = False):
+    """Draw one step's inputs.
+
+    Returns a dict of tensors on ``device``: q [R, Hq, D], k_new / v_new
+    [R, Hk, D], positions [R] i32, table [R, Pages] i32, k_pool / v_pool
+    [NumPages, Hk, 64, D].  With ``poison``, pool slots that no row may read
+    (spare pages, slots past a row's position in its last page and slots
+    before its window) hold NaN, so that any read of them shows in the output.
+    """
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed if seed is None else seed)
+    positions = draw_positions(w, gen)
+    assert int(positions.max()) < w.max_seq and int(positions.min()) >= 0
+    need = pages_needed(positions)
+    total = int(need.sum())
+    num_pages = w.num_pages if w.num_pages > 0 else total + math.ceil(total * 0.1)
+    assert num_pages >= total
+    perm = torch.randperm(num_pages, generator=gen, device=device).to(torch.int32)
+    table = torch.full((w.rows, w.pages_per_row), -1, dtype=torch.int32, device=device)
+    need_cpu = need.cpu().tolist()
+    off = 0
+    for r, n in enumerate(need_cpu):
+        table[r, :n] = perm[off:off + n]
+        off += n
+
+    def normal(*shape):
+        return torch.randn(*shape, generator=gen, device=device, dtype=torch.float32).to(w.torch_dtype)
+
+    R, Hq, Hk, D = w.rows, w.heads, w.kv_heads, w.head_dim
+    q = normal(R, Hq, D)
+    k_new = normal(R, Hk, D)
+    v_new = normal(R, Hk, D)
+    k_pool = normal(num_pages, Hk, PAGE_SIZE, D)
+    v_pool = normal(num_pages, Hk, PAGE_SIZE, D)
+    if poison:
+        _poison(w, positions, table, k_pool, v_pool)
+    return dict(q=q, k_new=k_new, v_new=v_new, positions=positions, table=table,
+                k_pool=k_pool, v_pool=v_pool)
+
+
+def _poison(w, positions, table, k_pool, v_pool):
+    nan = float("nan")
+    used = torch.zeros(k_pool.shape[0], dtype=torch.bool, device=k_pool.device)
+    pos_cpu = positions.cpu().tolist()
+    tab_cpu = table.cpu()
+    for r, pos in enumerate(pos_cpu):
+        lo = max(0, pos - w.window + 1) if w.window > 0 else 0
+        n = pos // PAGE_SIZE + 1
+        pages = tab_cpu[r, :n].tolist()
+        used[torch.tensor(pages, dtype=torch.int64, device=k_pool.device)] = True
+        last = pages[-1]
+        k_pool[last, :, pos % PAGE_SIZE + 1:, :] = nan
+        v_pool[last, :, pos % PAGE_SIZE + 1:, :] = nan
+        for t_page in range(lo // PAGE_SIZE):
+            k_pool[pages[t_page]] = nan
+            v_pool[pages[t_page]] = nan
+        if lo % PAGE_SIZE:
+            first = pages[lo // PAGE_SIZE]
+            k_pool[first, :, :lo % PAGE_SIZE, :] = nan
+            v_pool[first, :, :lo % PAGE_SIZE, :] = nan
+    k_pool[~used] = nan
+    v_pool[~used] = nan
+
+
+def to_numpy(t: torch.Tensor):
+    """Host numpy view for the oracle: bf16 as uint16 bit patterns."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view("uint16")
+    return t.numpy()
+
+
+def from_numpy(a, dtype) -> torch.Tensor:
+    """Inverse of to_numpy."""
+    t = torch.from_numpy(a.copy())
+    if dtype == torch.bfloat16:
+        return t.view(torch.int16).view(torch.bfloat16)
+    return t
