@@ -1,0 +1,468 @@
+#!/usr/bin/env python
+"""Benchmark of one paged GQA decode step (RoPE + cache write + attention).
+
+Default workload: the Llama-3.1-8B serving batch (256 rows, 32 query heads,
+8 kv heads, head dim 128, 64-token pages, context lengths log-uniform in
+[16, 8192], bf16).  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+* value: KV GB/s of the whole step over all ranks (algorithmic K/V bytes the
+  step must read, divided by the device time of K steps; max over ranks).
+* roofline: the attention kernel timed alone with CUDA events around each
+  launch; achieved = its algorithmic bytes per launch / mean launch time,
+  against the measured HBM copy bandwidth.
+* e2e: the same metric through the public call with pinned host buffers:
+  each step copies that step's inputs host->device and the output back.
+* cpu_baseline: the CPU oracle on the host (single thread), timed on whole
+  steps of the same workload.
+* --impl reference: the CPU oracle alone, each step a bounded sample of rows.
+"""
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from paged_gqa_decode_step_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak) and row-steps/s per layer"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ helpers --
+def visible(w, pos):
+    lo = max(0, pos - w.window + 1) if w.window > 0 else 0
+    return lo, pos - lo + 1
+
+
+def kv_bytes(w, positions):
+    """K and V bytes the step must read: sum_r 2 * ctx_r * Hk * D * E."""
+    return sum(2 * visible(w, int(p))[1] * w.kv_heads * w.head_dim * w.elem_bytes for p in positions)
+
+
+def attend_bytes(w, positions):
+    """Algorithmic bytes of the attention kernel: K/V, q in, out, table entries."""
+    E = w.elem_bytes
+    total = kv_bytes(w, positions)
+    for p in positions:
+        lo, _ = visible(w, int(p))
+        total += 2 * w.heads * w.head_dim * E + 4 * (int(p) // 64 - lo // 64 + 1)
+    return total
+
+
+def step_bytes(w, positions):
+    """Whole step: attention plus q read / rotated q write, k and v in, slot writes."""
+    E = w.elem_bytes
+    R = len(positions)
+    return attend_bytes(w, positions) + R * (2 * w.heads * w.head_dim * E + 4 * w.kv_heads * w.head_dim * E + 8)
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "paged_gqa_decode_step_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per attention launch from the committed ncu summary, if it
+    was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"attend_{workload}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the GPU works."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        sel = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"] + sel
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        self.out.flush()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) != 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        sm = sorted(r[0] for r in rows)
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# -------------------------------------------------------------- distributed --
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_seed(w, rank):
+    """Each rank draws its own batch of rows (weak scaling, no data exchange)."""
+    return w.seed + 7919 * rank
+
+
+# --------------------------------------------------------------------- CPU --
+def cpu_oracle_rate(w, host, budget_s, rows_per_step=None, max_steps=None):
+    """Run the oracle on whole steps (or row samples) for about budget_s.
+    Returns (KV GB/s, seconds, description, steps)."""
+    import numpy as np
+    import oracle
+    pos = host["positions"]
+    R = len(pos)
+    num_pages = host["k_pool"].shape[0]
+    od = oracle.BF16 if w.dtype == "bf16" else oracle.F32
+    done_bytes, spent, steps, start_row = 0, 0.0, 0, 0
+    rows_per_step = rows_per_step or R
+    while True:
+        sub = (np.arange(rows_per_step) + start_row) % R
+        start_row = (start_row + rows_per_step) % R
+        shape = oracle.make_shape(len(sub), w.heads, w.kv_heads, w.head_dim, w.pages_per_row, num_pages, od,
+                                  window=w.window, rope_theta=w.rope_theta)
+        args = [np.ascontiguousarray(host[k][sub]) for k in ("q", "k_new", "v_new", "positions", "table")]
+        t0 = time.perf_counter()
+        _, _, _, rc = oracle.step(shape, *args, host["k_pool"], host["v_pool"])
+        spent += time.perf_counter() - t0
+        assert rc == 0
+        done_bytes += kv_bytes(w, pos[sub])
+        steps += 1
+        if (max_steps and steps >= max_steps) or (not max_steps and spent >= budget_s):
+            break
+    desc = (f"{steps} oracle step(s) of {rows_per_step} of the {R} rows "
+            f"({'whole workload' if rows_per_step == R else 'rows taken round-robin'}), single thread")
+    return done_bytes / spent / 1e9, spent, desc, steps
+
+
+# ---------------------------------------------------------------- our arm --
+def run_ours(args, w, world, rank, local):
+    from paged_gqa_decode_step_gb300 import build
+    build.build()
+    from paged_gqa_decode_step_gb300 import binding as b
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    t = wl.generate(w, dev, seed=rank_seed(w, rank))
+    pos_list = t["positions"].cpu().tolist()
+    num_pages = t["k_pool"].shape[0]
+    tables = b.rope_tables(w.rope_theta, w.head_dim, w.max_seq, w.torch_dtype) if w.rope_theta > 0 else (None, None)
+    p = b.make_params(w.rows, w.heads, w.kv_heads, w.head_dim, w.pages_per_row, num_pages, w.torch_dtype,
+                      window=w.window, rope_cos=tables[0], rope_sin=tables[1])
+    ws = b.new_workspace(p)
+    out = torch.empty_like(t["q"])
+    kvb = kv_bytes(w, pos_list)
+    pool_bytes = 2 * t["k_pool"].numel() * t["k_pool"].element_size()
+    large = kvb > 2 * L2_BYTES
+    flush = None if large else torch.empty(4 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def step():
+        b.decode_fused(p, t["q"], t["k_new"], t["v_new"], t["positions"], t["table"], t["k_pool"], t["v_pool"], out, ws)
+
+    for _ in range(args.warmup):
+        step()
+    b.check_status(ws)
+    launches_per_step = b.last_launch_count()
+
+    # ---- timed region: K whole steps
+    with ClockSampler(dev) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        if large:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.steps):
+                step()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / args.steps
+        else:
+            total = 0.0
+            for _ in range(args.steps):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                step()
+                e1.record()
+                e1.synchronize()
+                total += e0.elapsed_time(e1)
+            ms = total / args.steps
+        torch.cuda.synchronize()
+        barrier(world)
+    clk = clocks.summary()
+    b.check_status(ws)
+    ms = max_over_ranks(ms, world)
+    all_kv = sum_over_ranks(kvb, world)
+    rows_all = w.rows * world
+    value = all_kv / (ms * 1e-3) / 1e9
+
+    # ---- roofline: the attention kernel alone, events around every launch
+    q_rot = torch.empty_like(t["q"])
+    b.rope_write_kv(p, t["q"], t["k_new"], t["v_new"], t["positions"], t["table"], q_rot, t["k_pool"], t["v_pool"], ws)
+    b.plan(p, t["positions"], ws)
+    for _ in range(3):
+        b.attend(p, q_rot, t["positions"], t["table"], t["k_pool"], t["v_pool"], out, ws)
+    n_att = max(20, min(args.steps, 400))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_att)]
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        if flush is not None:
+            flush.fill_(1)
+        e0.record()
+        b.attend(p, q_rot, t["positions"], t["table"], t["k_pool"], t["v_pool"], out, ws)
+        e1.record()
+    torch.cuda.synchronize()
+    b.check_status(ws)
+    att_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / n_att
+    att_bytes = attend_bytes(w, pos_list)
+    peak, peak_kind = measured_hbm_peak()
+    achieved = att_bytes / (att_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(w.name)
+
+    # ---- end to end: pinned host inputs in, output back, every step
+    host_in = {k: t[k].cpu().pin_memory() for k in ("q", "k_new", "v_new", "positions", "table")}
+    dev_in = {k: torch.empty_like(t[k]) for k in host_in}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    n_e2e = max(10, min(args.steps, 500))
+    stream = torch.cuda.current_stream()
+
+    def e2e_step():
+        for k in host_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        b.decode_fused(p, dev_in["q"], dev_in["k_new"], dev_in["v_new"], dev_in["positions"], dev_in["table"],
+                       t["k_pool"], t["v_pool"], out, ws)
+        host_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / n_e2e
+    e2e_s = max_over_ranks(e2e_s, world)
+    b.check_status(ws)
+    e2e_value = all_kv / e2e_s / 1e9
+
+    # ---- CPU baseline: the oracle on this host, rank 0 at N = 1 only
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = {k: wl.to_numpy(v) for k, v in t.items()}
+        rate, spent, desc, _ = cpu_oracle_rate(w, host, args.cpu_baseline_seconds)
+        cpu = {"value": rate, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc,
+               "seconds": round(spent, 2), "cpu": cpu_model()}
+
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) q/k/v and prefilled pool, shuffled page table)",
+        "config": {
+            "workload": w.name, "rows_per_gpu": w.rows, "heads": w.heads, "kv_heads": w.kv_heads,
+            "head_dim": w.head_dim, "page_size": 64, "pages_per_row": w.pages_per_row,
+            "positions": f"{w.positions} [{w.pos_lo}, {w.pos_hi}]", "window": w.window,
+            "rope_theta": w.rope_theta, "kv_bytes_per_step_per_gpu": kvb,
+            "l2": (f"inputs larger than L2: each step streams {kvb / 1e9:.2f} GB of K/V from a "
+                   f"{pool_bytes / 1e9:.2f} GB pool (L2 129 MB)") if large else
+                  "L2 flushed (512 MB write) between timed steps, outside the events",
+            "parallelism": f"replicas x{world} (rows sharded across ranks, no exchange)",
+        },
+        "row_steps_per_s": rows_all / (ms * 1e-3),
+        "frac_of_hbm_peak": value / world / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "kernel": f"attend_kernel<{w.dtype},{w.head_dim}>",
+                     "bytes_per_launch": att_bytes, "launch_us": att_ms * 1e3, "peak_kind": peak_kind},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    return line
+
+
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return os.uname().machine
+
+
+# ----------------------------------------------------------- reference arm --
+def run_reference(args, w, world, rank):
+    """The oracle on the host cores, each step a bounded sample of rows."""
+    if rank != 0:
+        return None
+    t = wl.generate(w, "cpu", seed=rank_seed(w, 0)) if w.rows * w.pages_per_row <= 4096 else None
+    if t is None:
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = wl.generate(w, dev, seed=rank_seed(w, 0))
+    host = {k: wl.to_numpy(v) for k, v in t.items()}
+    del t
+    pos = host["positions"]
+    mean_ctx = float(sum(visible(w, int(p))[1] for p in pos)) / len(pos)
+    # ~11 us per visible token-row on one core; size each step to fit ~90 s total
+    per_step_budget = min(5.0, 90.0 / max(1, args.steps + args.warmup))
+    per_row = mean_ctx * w.heads / 32 * 11e-6 * (w.head_dim / 128)
+    rows = int(max(1, min(w.rows, per_step_budget / max(per_row, 1e-9))))
+    if args.warmup:
+        cpu_oracle_rate(w, host, 0, rows_per_step=rows, max_steps=args.warmup)
+    rate, spent, desc, steps = cpu_oracle_rate(w, host, 0, rows_per_step=rows, max_steps=max(1, args.steps))
+    ms = spent / steps * 1e3
+    return {
+        "metric": METRIC, "value": rate, "unit": "GB/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name, "rows_per_step": rows, "rows": w.rows},
+        "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": desc, "value": rate, "unit": "GB/s",
+                         "cpu": cpu_model()},
+        "e2e": {"value": rate, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama8b_serving", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = wl.WORKLOADS[args.workload]
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, w, world, rank)
+    else:
+        line = run_ours(args, w, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,170 @@
+/*
+ * pdattn — one decode step of grouped-query attention over a paged KV cache,
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the `decode` body of GroupedQueryAttention on the Llama
+ * example page ("src/attention.linnet": rope on q and k at pos, write_at of k
+ * and v, attention over positions <= pos with scale rsqrt(f32(head dim)),
+ * each kv head shared by Heads / KvHeads query heads), addressed through a
+ * page table as the paged entries on the llama-3.1-8b-instruct architecture
+ * page state it (`decode_paged(…, positions: Tensor[Rows; i32],
+ * table: Tensor[Rows, Pages; i32])`, `PageSize: Dim = 64`), with the optional
+ * sliding window of the gpt-oss-20b architecture page (`window: i32`).
+ *
+ * Layouts (all row-major, contiguous, DEVICE pointers unless stated):
+ *   q, q_out, out     [rows, heads, head_dim]        element type T
+ *   k_new, v_new      [rows, kv_heads, head_dim]     T
+ *   positions         [rows]                         int32, pos of each row's new token
+ *   table             [rows, pages_per_row]          int32 page ids into the pools
+ *   k_pool, v_pool    [num_pages, kv_heads, 64, head_dim]  T
+ *   rope cos / sin    [rope_len, head_dim]           T (from pdattn_rope_tables)
+ * Row r's position t lives in pool page table[r, t / 64] at offset t % 64.
+ * T is bf16 or f32 (pdattn_dtype).  head_dim is 64 or 128, page_size 64,
+ * heads / kv_heads <= 8.  Pointers to T data must be 16-byte aligned.
+ *
+ * Ownership: the caller allocates and owns every buffer, including the
+ * workspace; the library allocates no device memory, keeps no per-call state
+ * and frees nothing.  It caches only per-device properties.
+ *
+ * Errors: every call validates its arguments on the host and returns
+ * PDATTN_EINVAL / PDATTN_EUNSUPPORTED before launching anything; launch
+ * failures return PDATTN_ECUDA.  Calls are asynchronous on `stream`.  Bad
+ * data found on the device (a position outside the table or the rope table,
+ * a page id outside the pool, a wait that ran past its time limit) is
+ * recorded in the workspace's status word; the affected rows are skipped and
+ * their outputs are left unspecified.  pdattn_check_status() reports and
+ * clears it.  pdattn_last_error() gives a message for the calling thread's
+ * last failure.
+ */
+#ifndef PDATTN_H
+#define PDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st* pdattn_stream;
+
+typedef enum {
+    PDATTN_OK = 0,
+    PDATTN_EINVAL = 1,        /* bad argument (host check) */
+    PDATTN_EUNSUPPORTED = 2,  /* shape or type this build does not handle */
+    PDATTN_ECUDA = 3,         /* a CUDA call failed */
+    PDATTN_EBADPAGE = 4,      /* device: page id outside [0, num_pages) */
+    PDATTN_ETIMEOUT = 5,      /* device: a bounded wait ran out */
+    PDATTN_EBADPOS = 6        /* device: position outside the table or the rope table */
+} pdattn_status;
+
+typedef enum { PDATTN_BF16 = 0, PDATTN_F32 = 1 } pdattn_dtype;
+
+typedef struct {
+    int32_t rows;           /* Rows; 0 makes every call a no-op */
+    int32_t heads;          /* Heads (query heads) */
+    int32_t kv_heads;       /* KvHeads; heads % kv_heads == 0 */
+    int32_t head_dim;       /* D = H / Heads: 64 or 128 */
+    int32_t page_size;      /* PageSize: must be 64 */
+    int32_t pages_per_row;  /* Pages: row stride of the table */
+    int32_t num_pages;      /* pages in each pool */
+    int32_t dtype;          /* pdattn_dtype of q, k, v, pools, tables and out */
+    int32_t window;         /* <= 0: attend [0, pos]; W > 0: attend (pos - W, pos] */
+    float scale;            /* score scale; 0 selects rsqrt(f32(head_dim)) */
+    const void* rope_cos;   /* NULL: no rotation (positions were added upstream) */
+    const void* rope_sin;   /* both NULL or both set */
+    int32_t rope_len;       /* rows of the rope tables; positions must be below it */
+    int32_t chunk_pages;    /* 0: the planner picks pages per split; else fixed */
+} pdattn_params;
+
+/*
+ * Bytes of workspace the calls below need for these parameters on the
+ * current device.  The workspace must be zero-filled once before first use;
+ * the calls leave it reusable.  Calls that share a workspace must be
+ * ordered (same stream or synchronised).
+ */
+size_t pdattn_workspace_size(const pdattn_params* p);
+
+/*
+ * Rotary tables (Llama example page, "src/rope.linnet", `tables`):
+ * inv_freq[i] = exp(-(f32(i) * 2 / f32(D)) * log(theta)) in f32,
+ * angle[s, i] = f32(s) * inv_freq[i], full = concat(angle, angle),
+ * cos_out = cast<T>(cos(full)), sin_out = cast<T>(sin(full)), each
+ * [length, head_dim].  cos, sin, exp and log are the correctly rounded f32
+ * values (computed in double and rounded).  Build once per model.
+ */
+pdattn_status pdattn_rope_tables(float theta, int32_t head_dim, int32_t length, int32_t dtype,
+                                 void* cos_out, void* sin_out, pdattn_stream stream);
+
+/*
+ * RoPE and cache write (Llama example page, "src/attention.linnet",
+ * `decode`: rope on q and k, `write_at(cache, k, pos)`), paged: for each
+ * row, q_out[r] = rope(q[r]) and the pool slot (table[r, pos / 64],
+ * pos % 64) of every kv head receives rope(k_new[r]) and v_new[r].
+ * rope(x) = x * cos[pos] + rotate_half(x) * sin[pos] with rotate_half(x) =
+ * concat(-x[D/2:], x[:D/2]): f32 products, one f32 add, one rounding to T.
+ * Without rope tables q_out is a copy of q and k_new is written as is.
+ * q_out may alias q.  Writes are bit-exact copies of these values.
+ */
+pdattn_status pdattn_rope_write_kv(const pdattn_params* p, const void* q, const void* k_new,
+                                   const void* v_new, const int32_t* positions,
+                                   const int32_t* table, void* q_out, void* k_pool, void* v_pool,
+                                   void* workspace, size_t workspace_bytes, pdattn_stream stream);
+
+/*
+ * Split plan for these positions: divides every row's visible pages into
+ * chunks (pages per chunk from the total work and the SM count, or
+ * p->chunk_pages) and orders the (row, kv head, chunk) work items
+ * largest first, in the workspace.  pdattn_attend uses it.
+ */
+pdattn_status pdattn_plan(const pdattn_params* p, const int32_t* positions, void* workspace,
+                          size_t workspace_bytes, pdattn_stream stream);
+
+/*
+ * Attention of already-rotated queries over the pools, which must already
+ * hold position pos of every row (Llama example page, `decode`: mask
+ * seen[s] = s <= pos, `grouped_attention(q, cache_k, cache_v,
+ * rsqrt(f32(D)), seen)`), following the plan last made in this workspace
+ * for the same positions: out[r, h] = sum_t softmax_t(scale * q[r, h] .
+ * K[t, h / g]) V[t, h / g] over t in [lo, pos], fp32 online softmax,
+ * split chunks merged on the device, result rounded to T.
+ */
+pdattn_status pdattn_attend(const pdattn_params* p, const void* q_rot, const int32_t* positions,
+                            const int32_t* table, const void* k_pool, const void* v_pool,
+                            void* out, void* workspace, size_t workspace_bytes,
+                            pdattn_stream stream);
+
+/* pdattn_plan followed by pdattn_attend. */
+pdattn_status pdattn_decode(const pdattn_params* p, const void* q_rot, const int32_t* positions,
+                            const int32_t* table, const void* k_pool, const void* v_pool,
+                            void* out, void* workspace, size_t workspace_bytes,
+                            pdattn_stream stream);
+
+/*
+ * The whole step: RoPE and cache write (rotated q kept in the workspace)
+ * with the plan in the same launch, then attention.  Equivalent to
+ * pdattn_rope_write_kv + pdattn_decode.
+ */
+pdattn_status pdattn_decode_fused(const pdattn_params* p, const void* q, const void* k_new,
+                                  const void* v_new, const int32_t* positions,
+                                  const int32_t* table, void* k_pool, void* v_pool, void* out,
+                                  void* workspace, size_t workspace_bytes, pdattn_stream stream);
+
+/*
+ * Synchronises `stream`, reads the workspace's device status word, clears
+ * it and returns the first error it recorded (PDATTN_OK if none).
+ */
+pdattn_status pdattn_check_status(void* workspace, pdattn_stream stream);
+
+/* Message for the calling thread's last failed call ("" if none). */
+const char* pdattn_last_error(void);
+
+/* Number of kernel launches the last successful call on this thread made. */
+int32_t pdattn_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PDATTN_H */

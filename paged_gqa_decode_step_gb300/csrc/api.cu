@@ -1,0 +1,368 @@
+// extern "C" entry points of libpdattn: host-side validation, TMA
+// descriptors and launches.  See include/pdattn.h for the contract.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/pdattn.h"
+#include "internal.h"
+
+using namespace pdattn;
+
+namespace {
+
+thread_local std::string g_error;
+thread_local int g_launches = 0;
+
+pdattn_status fail(pdattn_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_error = buf;
+    return s;
+}
+
+pdattn_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(PDATTN_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// SM count per device, read once.
+int sm_count() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 0 || dev >= 64) return 0;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev].store(v, std::memory_order_relaxed);
+    return v;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Pool [num_pages, kv_heads, 64, D] viewed as a 2-D tensor of
+// num_pages * kv_heads * 64 rows by D columns; boxes of 64 rows x 128 bytes,
+// 128-byte swizzled.
+pdattn_status make_pool_map(CUtensorMap* map, const void* pool, const pdattn_params* p) {
+    auto fn = encode_fn();
+    if (!fn) return fail(PDATTN_ECUDA, "cuTensorMapEncodeTiled is not available");
+    const int elem = p->dtype == PDATTN_BF16 ? 2 : 4;
+    cuuint64_t dims[2] = {(cuuint64_t)p->head_dim, (cuuint64_t)p->num_pages * p->kv_heads * kPageSize};
+    cuuint64_t strides[1] = {(cuuint64_t)p->head_dim * elem};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)kPageSize};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, p->dtype == PDATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                    2, const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PDATTN_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return PDATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+pdattn_status check_params(const pdattn_params* p) {
+    if (!p) return fail(PDATTN_EINVAL, "params is NULL");
+    if (p->rows < 0) return fail(PDATTN_EINVAL, "rows < 0");
+    if (p->heads <= 0 || p->kv_heads <= 0 || p->heads % p->kv_heads != 0)
+        return fail(PDATTN_EINVAL, "heads (%d) must be a positive multiple of kv_heads (%d)", p->heads, p->kv_heads);
+    if (p->head_dim <= 0 || p->head_dim % 2 != 0) return fail(PDATTN_EINVAL, "head_dim must be even and positive");
+    if (p->dtype != PDATTN_BF16 && p->dtype != PDATTN_F32) return fail(PDATTN_EINVAL, "unknown dtype %d", p->dtype);
+    if (p->pages_per_row <= 0 || p->num_pages <= 0) return fail(PDATTN_EINVAL, "pages_per_row and num_pages must be > 0");
+    if ((p->rope_cos == nullptr) != (p->rope_sin == nullptr))
+        return fail(PDATTN_EINVAL, "rope_cos and rope_sin must be both set or both NULL");
+    if (p->rope_cos && p->rope_len <= 0) return fail(PDATTN_EINVAL, "rope_len must be > 0 with rope tables");
+    if (p->rope_cos && (!aligned16(p->rope_cos) || !aligned16(p->rope_sin)))
+        return fail(PDATTN_EINVAL, "rope tables must be 16-byte aligned");
+    if (p->chunk_pages < 0 || p->chunk_pages > kChunkMax)
+        return fail(PDATTN_EINVAL, "chunk_pages must be in [0, %d]", kChunkMax);
+    if (!(p->scale >= 0.f)) return fail(PDATTN_EINVAL, "scale must be >= 0 (0 selects rsqrt(head_dim))");
+    if (p->page_size != kPageSize) return fail(PDATTN_EUNSUPPORTED, "page_size must be 64");
+    if (p->head_dim != 64 && p->head_dim != 128) return fail(PDATTN_EUNSUPPORTED, "head_dim must be 64 or 128");
+    if (p->heads / p->kv_heads > kMaxGroup) return fail(PDATTN_EUNSUPPORTED, "heads / kv_heads must be <= 8");
+    if (p->kv_heads > 32767) return fail(PDATTN_EUNSUPPORTED, "kv_heads must be < 32768");
+    if ((long long)p->num_pages * p->kv_heads * kPageSize >= (1ll << 31))
+        return fail(PDATTN_EUNSUPPORTED, "pool too large for 32-bit TMA row coordinates");
+    if ((long long)p->pages_per_row * kPageSize >= (1ll << 30)) return fail(PDATTN_EUNSUPPORTED, "pages_per_row too large");
+    return PDATTN_OK;
+}
+
+int elem_bytes(const pdattn_params* p) { return p->dtype == PDATTN_BF16 ? 2 : 4; }
+
+WsLayout layout_for(const pdattn_params* p, int grid) {
+    return ws_layout(p->rows, p->heads, p->kv_heads, p->head_dim, p->pages_per_row, elem_bytes(p),
+                     p->chunk_pages, grid);
+}
+
+pdattn_status check_ws(const pdattn_params* p, void* ws, size_t bytes, int grid, WsLayout* L) {
+    if (!ws) return fail(PDATTN_EINVAL, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return fail(PDATTN_EINVAL, "workspace must be 256-byte aligned");
+    *L = layout_for(p, grid);
+    if (bytes < L->total)
+        return fail(PDATTN_EINVAL, "workspace too small: %zu bytes given, %zu needed", bytes, L->total);
+    return PDATTN_OK;
+}
+
+PrepArgs prep_args(const pdattn_params* p, const int32_t* positions, const int32_t* table, char* ws,
+                   const WsLayout& L, int grid) {
+    PrepArgs a = {};
+    a.rows = p->rows;
+    a.heads = p->heads;
+    a.kv_heads = p->kv_heads;
+    a.head_dim = p->head_dim;
+    a.pages_per_row = p->pages_per_row;
+    a.num_pages = p->num_pages;
+    a.window = p->window;
+    a.rope_len = p->rope_len;
+    a.positions = positions;
+    a.table = table;
+    a.rope_cos = p->rope_cos;
+    a.rope_sin = p->rope_sin;
+    a.grid_attend = grid;
+    a.chunk_pages = p->chunk_pages;
+    a.ws = ws;
+    a.L = L;
+    return a;
+}
+
+float scale_log2(const pdattn_params* p) {
+    const double s = p->scale > 0.f ? (double)p->scale : (double)(float)(1.0 / std::sqrt((double)p->head_dim));
+    return (float)(s * 1.4426950408889634);
+}
+
+pdattn_status attend_impl(const pdattn_params* p, const void* q_rot, const int32_t* table,
+                          const void* k_pool, const void* v_pool, void* out, char* ws,
+                          const WsLayout& L, int grid, bool programmatic, cudaStream_t stream) {
+    CUtensorMap km, vm;
+    pdattn_status s = make_pool_map(&km, k_pool, p);
+    if (s != PDATTN_OK) return s;
+    s = make_pool_map(&vm, v_pool, p);
+    if (s != PDATTN_OK) return s;
+    AttendArgs a = {};
+    a.rows = p->rows;
+    a.heads = p->heads;
+    a.kv_heads = p->kv_heads;
+    a.group = p->heads / p->kv_heads;
+    a.head_dim = p->head_dim;
+    a.pages_per_row = p->pages_per_row;
+    a.num_pages = p->num_pages;
+    a.scale_log2 = scale_log2(p);
+    a.q = q_rot;
+    a.table = table;
+    a.out = out;
+    a.ws = ws;
+    a.L = L;
+    cudaError_t e = launch_attend(a, km, vm, p->dtype, grid, programmatic, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+    ++g_launches;
+    return PDATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pdattn_workspace_size(const pdattn_params* p) {
+    if (check_params(p) != PDATTN_OK) return 0;
+    const int grid = sm_count();
+    if (grid <= 0) return 0;
+    return layout_for(p, grid).total;
+}
+
+pdattn_status pdattn_rope_tables(float theta, int32_t head_dim, int32_t length, int32_t dtype, void* cos_out,
+                                 void* sin_out, pdattn_stream stream) {
+    g_launches = 0;
+    if (!(theta > 0.f)) return fail(PDATTN_EINVAL, "theta must be > 0");
+    if (head_dim <= 0 || head_dim % 2 != 0) return fail(PDATTN_EINVAL, "head_dim must be even and positive");
+    if (length < 0) return fail(PDATTN_EINVAL, "length must be >= 0");
+    if (dtype != PDATTN_BF16 && dtype != PDATTN_F32) return fail(PDATTN_EINVAL, "unknown dtype");
+    if (length > 0 && (!cos_out || !sin_out)) return fail(PDATTN_EINVAL, "NULL table pointer");
+    cudaError_t e = launch_rope_tables(theta, head_dim, length, dtype, cos_out, sin_out, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
+    g_launches = length > 0 ? 1 : 0;
+    return PDATTN_OK;
+}
+
+pdattn_status pdattn_rope_write_kv(const pdattn_params* p, const void* q, const void* k_new, const void* v_new,
+                                   const int32_t* positions, const int32_t* table, void* q_out, void* k_pool,
+                                   void* v_pool, void* workspace, size_t workspace_bytes, pdattn_stream stream) {
+    g_launches = 0;
+    pdattn_status s = check_params(p);
+    if (s != PDATTN_OK) return s;
+    if (p->rows == 0) return PDATTN_OK;
+    if (!q || !k_new || !v_new || !positions || !table || !q_out || !k_pool || !v_pool)
+        return fail(PDATTN_EINVAL, "NULL data pointer");
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(q_out) || !aligned16(k_pool) ||
+        !aligned16(v_pool))
+        return fail(PDATTN_EINVAL, "q, k_new, v_new, q_out and the pools must be 16-byte aligned");
+    const int grid = sm_count();
+    if (grid <= 0) return fail(PDATTN_ECUDA, "no CUDA device");
+    WsLayout L;
+    s = check_ws(p, workspace, workspace_bytes, grid, &L);
+    if (s != PDATTN_OK) return s;
+    PrepArgs a = prep_args(p, positions, table, static_cast<char*>(workspace), L, grid);
+    a.q = q;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.q_out = q_out;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.rope_blocks = p->rows;
+    a.do_plan = 0;
+    cudaError_t e = launch_prep(a, p->dtype, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "rope/write launch");
+    g_launches = 1;
+    return PDATTN_OK;
+}
+
+pdattn_status pdattn_plan(const pdattn_params* p, const int32_t* positions, void* workspace,
+                          size_t workspace_bytes, pdattn_stream stream) {
+    g_launches = 0;
+    pdattn_status s = check_params(p);
+    if (s != PDATTN_OK) return s;
+    if (p->rows == 0) return PDATTN_OK;
+    if (!positions) return fail(PDATTN_EINVAL, "NULL positions");
+    const int grid = sm_count();
+    if (grid <= 0) return fail(PDATTN_ECUDA, "no CUDA device");
+    WsLayout L;
+    s = check_ws(p, workspace, workspace_bytes, grid, &L);
+    if (s != PDATTN_OK) return s;
+    PrepArgs a = prep_args(p, positions, nullptr, static_cast<char*>(workspace), L, grid);
+    a.rope_blocks = 0;
+    a.do_plan = 1;
+    cudaError_t e = launch_prep(a, p->dtype, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "plan launch");
+    g_launches = 1;
+    return PDATTN_OK;
+}
+
+static pdattn_status check_attend_ptrs(const void* q, const int32_t* positions, const int32_t* table,
+                                       const void* k_pool, const void* v_pool, const void* out) {
+    if (!q || !positions || !table || !k_pool || !v_pool || !out) return fail(PDATTN_EINVAL, "NULL data pointer");
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+        return fail(PDATTN_EINVAL, "q, the pools and out must be 16-byte aligned");
+    return PDATTN_OK;
+}
+
+pdattn_status pdattn_attend(const pdattn_params* p, const void* q_rot, const int32_t* positions, const int32_t* table,
+                            const void* k_pool, const void* v_pool, void* out, void* workspace,
+                            size_t workspace_bytes, pdattn_stream stream) {
+    g_launches = 0;
+    pdattn_status s = check_params(p);
+    if (s != PDATTN_OK) return s;
+    if (p->rows == 0) return PDATTN_OK;
+    s = check_attend_ptrs(q_rot, positions, table, k_pool, v_pool, out);
+    if (s != PDATTN_OK) return s;
+    const int grid = sm_count();
+    if (grid <= 0) return fail(PDATTN_ECUDA, "no CUDA device");
+    WsLayout L;
+    s = check_ws(p, workspace, workspace_bytes, grid, &L);
+    if (s != PDATTN_OK) return s;
+    return attend_impl(p, q_rot, table, k_pool, v_pool, out, static_cast<char*>(workspace), L, grid, false,
+                       (cudaStream_t)stream);
+}
+
+pdattn_status pdattn_decode(const pdattn_params* p, const void* q_rot, const int32_t* positions, const int32_t* table,
+                            const void* k_pool, const void* v_pool, void* out, void* workspace,
+                            size_t workspace_bytes, pdattn_stream stream) {
+    g_launches = 0;
+    pdattn_status s = check_params(p);
+    if (s != PDATTN_OK) return s;
+    if (p->rows == 0) return PDATTN_OK;
+    s = check_attend_ptrs(q_rot, positions, table, k_pool, v_pool, out);
+    if (s != PDATTN_OK) return s;
+    const int grid = sm_count();
+    if (grid <= 0) return fail(PDATTN_ECUDA, "no CUDA device");
+    WsLayout L;
+    s = check_ws(p, workspace, workspace_bytes, grid, &L);
+    if (s != PDATTN_OK) return s;
+    PrepArgs a = prep_args(p, positions, table, static_cast<char*>(workspace), L, grid);
+    a.rope_blocks = 0;
+    a.do_plan = 1;
+    cudaError_t e = launch_prep(a, p->dtype, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "plan launch");
+    s = attend_impl(p, q_rot, table, k_pool, v_pool, out, static_cast<char*>(workspace), L, grid, true,
+                    (cudaStream_t)stream);
+    if (s == PDATTN_OK) g_launches = 2;
+    return s;
+}
+
+pdattn_status pdattn_decode_fused(const pdattn_params* p, const void* q, const void* k_new, const void* v_new,
+                                  const int32_t* positions, const int32_t* table, void* k_pool, void* v_pool,
+                                  void* out, void* workspace, size_t workspace_bytes, pdattn_stream stream) {
+    g_launches = 0;
+    pdattn_status s = check_params(p);
+    if (s != PDATTN_OK) return s;
+    if (p->rows == 0) return PDATTN_OK;
+    if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
+        return fail(PDATTN_EINVAL, "k_new and v_new must be non-NULL and 16-byte aligned");
+    s = check_attend_ptrs(q, positions, table, k_pool, v_pool, out);
+    if (s != PDATTN_OK) return s;
+    const int grid = sm_count();
+    if (grid <= 0) return fail(PDATTN_ECUDA, "no CUDA device");
+    WsLayout L;
+    s = check_ws(p, workspace, workspace_bytes, grid, &L);
+    if (s != PDATTN_OK) return s;
+    char* ws = static_cast<char*>(workspace);
+    void* q_rot = ws + L.q_rot;
+    PrepArgs a = prep_args(p, positions, table, ws, L, grid);
+    a.q = q;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.q_out = q_rot;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.rope_blocks = p->rows;
+    a.do_plan = 1;
+    cudaError_t e = launch_prep(a, p->dtype, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "rope/write/plan launch");
+    s = attend_impl(p, q_rot, table, k_pool, v_pool, out, ws, L, grid, true, (cudaStream_t)stream);
+    if (s == PDATTN_OK) g_launches = 2;
+    return s;
+}
+
+pdattn_status pdattn_check_status(void* workspace, pdattn_stream stream) {
+    if (!workspace) return fail(PDATTN_EINVAL, "workspace is NULL");
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    int status = 0;
+    e = cudaMemcpy(&status, workspace, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (status != 0) {
+        const int zero = 0;
+        e = cudaMemcpy(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "status clear");
+    }
+    if (status & kErrTimeout) return fail(PDATTN_ETIMEOUT, "a device wait ran past its limit (status 0x%x)", status);
+    if (status & kErrBadPage) return fail(PDATTN_EBADPAGE, "a page id outside the pool (status 0x%x)", status);
+    if (status & kErrBadPos) return fail(PDATTN_EBADPOS, "a position outside the table or rope table (status 0x%x)", status);
+    if (status & kErrBadPlan) return fail(PDATTN_EINVAL, "attention ran without a matching plan (status 0x%x)", status);
+    return PDATTN_OK;
+}
+
+const char* pdattn_last_error(void) { return g_error.c_str(); }
+
+int32_t pdattn_last_launch_count(void) { return g_launches; }
+
+}  // extern "C"

@@ -1,0 +1,228 @@
+// Device helpers shared by the pdattn kernels: inline PTX for mbarriers,
+// TMA / bulk copies, warp-level MMA, and the workspace layout.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace pdattn {
+
+constexpr int kPageSize = 64;
+constexpr int kMaxGroup = 8;          // query heads per kv head (the MMA's N)
+constexpr int kChunkMax = 64;         // largest pages-per-split the planner picks
+constexpr int kItemsPerCta = 8;       // planner's target work items per persistent CTA
+constexpr uint32_t kPlanMagic = 0x70646174u;
+
+// Status bits in the workspace's status word.
+constexpr int kErrBadPage = 1;
+constexpr int kErrBadPos = 2;
+constexpr int kErrTimeout = 4;
+constexpr int kErrBadPlan = 8;
+
+// Control block at the start of the workspace (256 bytes).
+struct Ctrl {
+    int status;        // OR of kErr* bits; cleared by pdattn_check_status
+    int next_item;     // persistent-scheduler cursor
+    int done_ctas;     // CTAs that finished fetching work
+    int n_items;       // work items in the plan
+    int chunk_pages;   // pages per split chosen by the plan
+    uint32_t magic;    // kPlanMagic once a plan is written
+    int rows, kv_heads, pages_per_row, max_items, group, head_dim;
+    int pad[52];
+};
+static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
+
+// Byte offsets of the workspace regions (all 256-byte aligned).
+struct WsLayout {
+    size_t ctrl, row_info, items, merge_cnt, part_ml, part_o, q_rot, total;
+    int max_items;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// max work items: min over split choices of the planner, see the planner.
+__host__ __device__ inline int plan_max_items(int rows, int kv_heads, int pages_per_row,
+                                              int chunk_pages, int grid) {
+    long long rh = (long long)rows * kv_heads;
+    long long n;
+    if (chunk_pages > 0) {
+        n = rh * ((pages_per_row + chunk_pages - 1) / chunk_pages);
+    } else {
+        long long a = (long long)kItemsPerCta * grid + rh;
+        long long b = rh * ((pages_per_row + kChunkMax - 1) / kChunkMax);
+        n = a > b ? a : b;
+    }
+    return (int)n;
+}
+
+__host__ __device__ inline WsLayout ws_layout(int rows, int heads, int kv_heads, int head_dim,
+                                              int pages_per_row, int elem_bytes, int chunk_pages,
+                                              int grid) {
+    WsLayout L;
+    int g = heads / kv_heads;
+    L.max_items = plan_max_items(rows, kv_heads, pages_per_row, chunk_pages, grid);
+    size_t off = 0;
+    L.ctrl = off; off += 256;
+    L.row_info = off; off = align256(off + sizeof(int4) * (size_t)rows);
+    L.items = off; off = align256(off + sizeof(int2) * (size_t)L.max_items);
+    L.merge_cnt = off; off = align256(off + sizeof(int) * (size_t)rows * kv_heads);
+    L.part_ml = off; off = align256(off + sizeof(float2) * (size_t)L.max_items * g);
+    L.part_o = off; off = align256(off + sizeof(float) * (size_t)L.max_items * g * head_dim);
+    L.q_rot = off; off = align256(off + (size_t)elem_bytes * rows * heads * head_dim);
+    L.total = off;
+    return L;
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; gives up after
+// `timeout_ns` and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t timeout_ns = 2000000000ull) {
+    #pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = globaltimer_ns();
+    #pragma unroll 1
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+// 2-D tiled TMA load of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Contiguous bulk copy global -> shared (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// D = A(16x16 bf16, row) * B(16x8 bf16, col) + D, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 2^x on the SFU.
+__device__ __forceinline__ float exp2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Address of 16-byte chunk `chunk` (0..7) of row `row` in a 64-row x 128-byte
+// box written by TMA with 128-byte swizzling (box base 1024-byte aligned).
+__device__ __forceinline__ uint32_t swz128(uint32_t box, int row, int chunk) {
+    return box + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ void set_error(Ctrl* ctrl, int bits) { atomicOr(&ctrl->status, bits); }
+
+}  // namespace pdattn

@@ -1,0 +1,311 @@
+// RoPE tables, RoPE + paged cache write, and the split planner.
+//
+// Follows the Llama example page: "src/rope.linnet" (`tables`) for the
+// tables and "src/attention.linnet" (`decode`: rope on q and k at pos, then
+// `write_at` of k and v) for the write, with the paged slot of the
+// llama-3.1-8b-instruct architecture page (`decode_paged`, PageSize = 64).
+#include "internal.h"
+
+namespace pdattn {
+
+// ---------------------------------------------------------------------------
+// Tables: inv_freq[i] = exp(-(f32(i) * 2 / f32(D)) * log(theta)) in f32,
+// angle = f32(s) * inv_freq[i], full = concat(angle, angle), cast<T>(cos),
+// cast<T>(sin).  Every f32 step is one correctly rounded operation; cos, sin,
+// exp and log are evaluated in double and rounded to f32.
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+
+template <typename T>
+__global__ void rope_tables_kernel(float theta, int D, int S, T* __restrict__ cos_out,
+                                   T* __restrict__ sin_out) {
+    const int half = D / 2;
+    const float log_theta = static_cast<float>(log(static_cast<double>(theta)));
+    const long long n = static_cast<long long>(S) * half;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int s = static_cast<int>(idx / half);
+        const int i = static_cast<int>(idx % half);
+        const float two_i = __fmul_rn(static_cast<float>(i), 2.0f);
+        const float ratio = __fdiv_rn(two_i, static_cast<float>(D));
+        const float arg = __fmul_rn(-ratio, log_theta);
+        const float inv_freq = static_cast<float>(exp(static_cast<double>(arg)));
+        const float angle = __fmul_rn(static_cast<float>(s), inv_freq);
+        const float c = static_cast<float>(cos(static_cast<double>(angle)));
+        const float sn = static_cast<float>(sin(static_cast<double>(angle)));
+        const size_t o = static_cast<size_t>(s) * D + i;
+        cos_out[o] = from_f32<T>(c);
+        cos_out[o + half] = from_f32<T>(c);
+        sin_out[o] = from_f32<T>(sn);
+        sin_out[o + half] = from_f32<T>(sn);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 16-byte vectors of T and the rotation of one pair of them.
+// ---------------------------------------------------------------------------
+template <typename T>
+struct Vec16;
+template <>
+struct Vec16<__nv_bfloat16> {
+    static constexpr int N = 8;
+    __device__ static void to_f32(const uint4& v, float (&f)[8]) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+        #pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float2 t = __bfloat1622float2(h[k]);
+            f[2 * k] = t.x;
+            f[2 * k + 1] = t.y;
+        }
+    }
+    __device__ static uint4 from_f32(const float (&f)[8]) {
+        uint4 v;
+        uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+        #pragma unroll
+        for (int k = 0; k < 4; ++k) w[k] = pack_bf16x2(f[2 * k], f[2 * k + 1]);
+        return v;
+    }
+};
+template <>
+struct Vec16<float> {
+    static constexpr int N = 4;
+    __device__ static void to_f32(const uint4& v, float (&f)[4]) {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    }
+    __device__ static uint4 from_f32(const float (&f)[4]) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                          __float_as_uint(f[3]));
+    }
+};
+
+// y_lo = x_lo * c_lo - x_hi * s_lo, y_hi = x_hi * c_hi + x_lo * s_hi: the
+// pages' x * cos + rotate_half(x) * sin with rotate_half(x) = [-x_hi, x_lo].
+// Separate f32 products and one f32 add (no fused multiply-add), then one
+// rounding to T.
+template <typename T>
+__device__ __forceinline__ void rope_pair(const T* x, T* y, const T* cos_row, const T* sin_row,
+                                          int half, int e0) {
+    using V = Vec16<T>;
+    constexpr int N = V::N;
+    float xl[N], xh[N], cl[N], ch[N], sl[N], sh[N], yl[N], yh[N];
+    V::to_f32(*reinterpret_cast<const uint4*>(x + e0), xl);
+    V::to_f32(*reinterpret_cast<const uint4*>(x + half + e0), xh);
+    V::to_f32(__ldg(reinterpret_cast<const uint4*>(cos_row + e0)), cl);
+    V::to_f32(__ldg(reinterpret_cast<const uint4*>(cos_row + half + e0)), ch);
+    V::to_f32(__ldg(reinterpret_cast<const uint4*>(sin_row + e0)), sl);
+    V::to_f32(__ldg(reinterpret_cast<const uint4*>(sin_row + half + e0)), sh);
+    #pragma unroll
+    for (int k = 0; k < N; ++k) {
+        yl[k] = __fsub_rn(__fmul_rn(xl[k], cl[k]), __fmul_rn(xh[k], sl[k]));
+        yh[k] = __fadd_rn(__fmul_rn(xh[k], ch[k]), __fmul_rn(xl[k], sh[k]));
+    }
+    *reinterpret_cast<uint4*>(y + e0) = V::from_f32(yl);
+    *reinterpret_cast<uint4*>(y + half + e0) = V::from_f32(yh);
+}
+
+// ---------------------------------------------------------------------------
+// Prep kernel: blocks [0, rope_blocks) rotate and write one row each; the
+// last block (if plan) builds the split plan.
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ void rope_write_row(const PrepArgs& a, int row) {
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(a.ws + a.L.ctrl);
+    const int D = a.head_dim, half = D / 2, Hq = a.heads, Hk = a.kv_heads;
+    const int pos = __ldg(a.positions + row);
+    const bool rope = a.rope_cos != nullptr;
+    if (pos < 0 || pos >= a.pages_per_row * kPageSize || (rope && pos >= a.rope_len)) {
+        if (threadIdx.x == 0) set_error(ctrl, kErrBadPos);
+        return;
+    }
+    const int page = __ldg(a.table + (size_t)row * a.pages_per_row + pos / kPageSize);
+    const bool page_ok = page >= 0 && page < a.num_pages;
+    if (!page_ok && threadIdx.x == 0) set_error(ctrl, kErrBadPage);
+    const int off = pos % kPageSize;
+
+    constexpr int N = Vec16<T>::N;
+    const T* q = static_cast<const T*>(a.q) + (size_t)row * Hq * D;
+    T* q_out = static_cast<T*>(a.q_out) + (size_t)row * Hq * D;
+    const T* kn = static_cast<const T*>(a.k_new) + (size_t)row * Hk * D;
+    const T* vn = static_cast<const T*>(a.v_new) + (size_t)row * Hk * D;
+    T* kp = static_cast<T*>(a.k_pool);
+    T* vp = static_cast<T*>(a.v_pool);
+    const T* cos_row = rope ? static_cast<const T*>(a.rope_cos) + (size_t)pos * D : nullptr;
+    const T* sin_row = rope ? static_cast<const T*>(a.rope_sin) + (size_t)pos * D : nullptr;
+
+    const int per_head = rope ? half / N : D / N;  // work units per head vector
+    const int uq = Hq * per_head, uk = Hk * per_head, uv = Hk * (D / N);
+    for (int u = threadIdx.x; u < uq + uk + uv; u += blockDim.x) {
+        if (u < uq) {
+            const int h = u / per_head, e0 = (u % per_head) * N;
+            if (rope) {
+                rope_pair<T>(q + (size_t)h * D, q_out + (size_t)h * D, cos_row, sin_row, half, e0);
+            } else {
+                *reinterpret_cast<uint4*>(q_out + (size_t)h * D + e0) =
+                    *reinterpret_cast<const uint4*>(q + (size_t)h * D + e0);
+            }
+        } else if (!page_ok) {
+            break;
+        } else if (u < uq + uk) {
+            const int v = u - uq, h = v / per_head, e0 = (v % per_head) * N;
+            T* slot = kp + (((size_t)page * Hk + h) * kPageSize + off) * D;
+            if (rope) {
+                rope_pair<T>(kn + (size_t)h * D, slot, cos_row, sin_row, half, e0);
+            } else {
+                *reinterpret_cast<uint4*>(slot + e0) =
+                    __ldg(reinterpret_cast<const uint4*>(kn + (size_t)h * D + e0));
+            }
+        } else {
+            const int v = u - uq - uk, h = v / (D / N), e0 = (v % (D / N)) * N;
+            T* slot = vp + (((size_t)page * Hk + h) * kPageSize + off) * D;
+            *reinterpret_cast<uint4*>(slot + e0) =
+                __ldg(reinterpret_cast<const uint4*>(vn + (size_t)h * D + e0));
+        }
+    }
+}
+
+// Visible positions of a row: [lo, pos] with lo = 0 or pos - window + 1.
+__device__ __forceinline__ int row_lo(int pos, int window) {
+    return (window > 0 && pos - window + 1 > 0) ? pos - window + 1 : 0;
+}
+
+// One block.  Splits every row's visible pages [lo / 64, pos / 64] into
+// chunks of C pages and lists the (row, kv head, chunk) items sorted by size,
+// largest first (a counting sort over the C sizes), so that the persistent
+// attention kernel hands out long items before short ones.
+__device__ void build_plan(const PrepArgs& a) {
+    __shared__ int s_cnt[kChunkMax + 1];
+    __shared__ int s_cur[kChunkMax + 1];
+    __shared__ unsigned long long s_work;
+    __shared__ int s_slots;
+    __shared__ int s_chunk;
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(a.ws + a.L.ctrl);
+    int4* row_info = reinterpret_cast<int4*>(a.ws + a.L.row_info);
+    int2* items = reinterpret_cast<int2*>(a.ws + a.L.items);
+    int* merge_cnt = reinterpret_cast<int*>(a.ws + a.L.merge_cnt);
+    const int tid = threadIdx.x, R = a.rows, Hk = a.kv_heads, max_pos = a.pages_per_row * kPageSize;
+
+    if (tid == 0) { s_work = 0; s_slots = 0; }
+    for (int i = tid; i <= kChunkMax; i += blockDim.x) s_cnt[i] = 0;
+    __syncthreads();
+
+    unsigned long long w = 0;
+    for (int r = tid; r < R; r += blockDim.x) {
+        const int pos = __ldg(a.positions + r);
+        if (pos >= 0 && pos < max_pos) w += pos / kPageSize - row_lo(pos, a.window) / kPageSize + 1;
+    }
+    if (w) atomicAdd(&s_work, w);
+    __syncthreads();
+    if (tid == 0) {
+        int c = a.chunk_pages;
+        if (c <= 0) {
+            const unsigned long long total = s_work * Hk;
+            const unsigned long long per = (unsigned long long)kItemsPerCta * a.grid_attend;
+            unsigned long long cc = (total + per - 1) / per;
+            c = (int)(cc < 1 ? 1 : (cc > kChunkMax ? kChunkMax : cc));
+        }
+        s_chunk = c;
+    }
+    __syncthreads();
+    const int C = s_chunk;
+
+    for (int r = tid; r < R; r += blockDim.x) {
+        const int pos = __ldg(a.positions + r);
+        const bool ok = pos >= 0 && pos < max_pos;
+        if (!ok) set_error(ctrl, kErrBadPos);
+        const int lo = ok ? row_lo(pos, a.window) : 0;
+        const int n = ok ? pos / kPageSize - lo / kPageSize + 1 : 0;
+        const int nch = (n + C - 1) / C;
+        if (n / C) atomicAdd(&s_cnt[C], (n / C) * Hk);
+        if (n % C) atomicAdd(&s_cnt[n % C], Hk);
+        const int base = nch ? atomicAdd(&s_slots, nch * Hk) : 0;
+        row_info[r] = make_int4(ok ? pos : -1, lo, nch, base);
+        for (int h = 0; h < Hk; ++h) merge_cnt[(size_t)r * Hk + h] = 0;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int off = 0;
+        for (int s = C; s >= 1; --s) { s_cur[s] = off; off += s_cnt[s]; }
+        s_cnt[0] = off;  // total items
+    }
+    __syncthreads();
+    const int n_items = s_cnt[0];
+    const bool fits = n_items <= a.L.max_items;
+    if (fits) {
+        for (long long pr = tid; pr < (long long)R * Hk; pr += blockDim.x) {
+            const int r = (int)(pr / Hk), h = (int)(pr % Hk);
+            const int pos = __ldg(a.positions + r);
+            if (pos < 0 || pos >= max_pos) continue;
+            const int n = pos / kPageSize - row_lo(pos, a.window) / kPageSize + 1;
+            const int full = n / C, tail = n % C;
+            for (int c = 0; c < full; ++c) items[atomicAdd(&s_cur[C], 1)] = make_int2(r, (h << 16) | c);
+            if (tail) items[atomicAdd(&s_cur[tail], 1)] = make_int2(r, (h << 16) | full);
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        if (!fits) set_error(ctrl, kErrBadPlan);
+        ctrl->n_items = fits ? n_items : 0;
+        ctrl->chunk_pages = C;
+        ctrl->next_item = 0;
+        ctrl->done_ctas = 0;
+        ctrl->rows = R;
+        ctrl->kv_heads = Hk;
+        ctrl->pages_per_row = a.pages_per_row;
+        ctrl->max_items = a.L.max_items;
+        ctrl->group = a.heads / Hk;
+        ctrl->head_dim = a.head_dim;
+        ctrl->magic = kPlanMagic;
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepArgs a) {
+    // Let the attention kernel that follows start its prologue now; it waits
+    // for this grid's completion before it reads anything written here.
+    griddep_launch_dependents();
+    if (a.do_plan && blockIdx.x == gridDim.x - 1) {
+        build_plan(a);
+        return;
+    }
+    rope_write_row<T>(a, blockIdx.x);
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers
+// ---------------------------------------------------------------------------
+cudaError_t launch_rope_tables(float theta, int D, int S, int dtype, void* cos_out, void* sin_out,
+                               cudaStream_t stream) {
+    const long long n = (long long)S * (D / 2);
+    if (n == 0) return cudaSuccess;
+    const int block = 256;
+    const int grid = (int)((n + block - 1) / block < 4096 ? (n + block - 1) / block : 4096);
+    if (dtype == 0)
+        rope_tables_kernel<__nv_bfloat16><<<grid, block, 0, stream>>>(
+            theta, D, S, static_cast<__nv_bfloat16*>(cos_out), static_cast<__nv_bfloat16*>(sin_out));
+    else
+        rope_tables_kernel<float><<<grid, block, 0, stream>>>(
+            theta, D, S, static_cast<float*>(cos_out), static_cast<float*>(sin_out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prep(const PrepArgs& a, int dtype, cudaStream_t stream) {
+    const int blocks = a.rope_blocks + (a.do_plan ? 1 : 0);
+    if (blocks == 0) return cudaSuccess;
+    if (dtype == 0)
+        prep_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(a);
+    else
+        prep_kernel<float><<<blocks, 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace pdattn
