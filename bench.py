@@ -293,6 +293,12 @@ def run_ours(args, w, world, rank, local):
         barrier(world)
     clk = clocks.summary()
     b.check_status(ws)
+    if args.quick:
+        # profiling mode: warm-up and timed steps only
+        if rank == 0:
+            print(json.dumps({"quick": True, "workload": w.name, "ms_per_step": ms,
+                              "kv_gbs": kvb / (ms * 1e-3) / 1e9}), flush=True)
+        return None
     ms = max_over_ranks(ms, world)
     all_kv = sum_over_ranks(kvb, world)
     rows_all = w.rows * world
@@ -448,6 +454,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama8b_serving", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="warm-up and timed steps only, no JSON line (for profiler captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

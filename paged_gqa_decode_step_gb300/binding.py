@@ -85,6 +85,8 @@ def make_params(rows, heads, kv_heads, head_dim, pages_per_row, num_pages, dtype
         for name, t in (("rope_cos", rope_cos), ("rope_sin", rope_sin)):
             _expect(name, t, (rope_cos.shape[0], head_dim), dtype)
         p.rope_cos, p.rope_sin, p.rope_len = rope_cos.data_ptr(), rope_sin.data_ptr(), rope_cos.shape[0]
+        # the block holds raw pointers: keep the tables alive as long as it lives
+        p._tables = (rope_cos, rope_sin)
     return p
 
 
