@@ -152,6 +152,28 @@ pdattn_status pdattn_decode_fused(const pdattn_params* p, const void* q, const v
                                   void* workspace, size_t workspace_bytes, pdattn_stream stream);
 
 /*
+ * pdattn_decode_fused without a workspace, for callers that cannot allocate
+ * device memory (an allocator that is frozen once serving starts, a plugin
+ * inside a program that owns all device memory, a C caller with no CUDA
+ * allocator).  The paper has no counterpart: this is a packaging of the same
+ * step.  Its scratch is one fixed 16 MiB array compiled into the library,
+ * which every GPU that loads the library keeps until the process exits.
+ * Parameters whose workspace (pdattn_workspace_size) exceeds 16 MiB are
+ * rejected with PDATTN_EINVAL before any launch; the Llama-3.1-8B shape at
+ * 256 rows needs about 10 MiB.  The first call on each device (with that
+ * device current) looks up the array's device address and clears its control
+ * block; make that first call before capturing any stream.  All calls on a
+ * device share the one array: calls whose work overlaps on the GPU (other
+ * streams, other threads) race and must be serialised by the caller.  Bad
+ * positions or page ids found on the device are skipped but not reported;
+ * check the inputs beforehand or use pdattn_decode_fused for reports.
+ */
+pdattn_status pdattn_decode_fused_noalloc(const pdattn_params* p, const void* q, const void* k_new,
+                                          const void* v_new, const int32_t* positions,
+                                          const int32_t* table, void* k_pool, void* v_pool,
+                                          void* out, pdattn_stream stream);
+
+/*
  * Synchronises `stream`, reads the workspace's device status word, clears
  * it and returns the first error it recorded (PDATTN_OK if none).
  */

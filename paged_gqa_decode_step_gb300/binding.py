@@ -49,6 +49,7 @@ def _load():
         "pdattn_attend": (i32, [P, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "pdattn_decode": (i32, [P, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "pdattn_decode_fused": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "pdattn_decode_fused_noalloc": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         "pdattn_check_status": (i32, [vp, vp]),
         "pdattn_last_error": (ctypes.c_char_p, []),
         "pdattn_last_launch_count": (i32, []),
@@ -181,6 +182,14 @@ def decode_fused(p, q, k_new, v_new, positions, table, k_pool, v_pool, out, ws, 
     w, n = _ws(ws)
     _check(lib.pdattn_decode_fused(ctypes.byref(p), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions),
                                    _ptr(table), _ptr(k_pool), _ptr(v_pool), _ptr(out), w, n, _stream(stream)))
+
+
+def decode_fused_noalloc(p, q, k_new, v_new, positions, table, k_pool, v_pool, out, stream=None):
+    """decode_fused with the library's fixed scratch array instead of a workspace."""
+    _check_common(p, positions, table, k_pool, v_pool)
+    _check_q(p, q=q, k_new=k_new, v_new=v_new, out=out)
+    _check(lib.pdattn_decode_fused_noalloc(ctypes.byref(p), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions),
+                                           _ptr(table), _ptr(k_pool), _ptr(v_pool), _ptr(out), _stream(stream)))
 
 
 def check_status(ws, stream=None):

@@ -366,3 +366,76 @@ const char* pdattn_last_error(void) { return g_error.c_str(); }
 int32_t pdattn_last_launch_count(void) { return g_launches; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Entry point for callers that cannot allocate device memory.
+//
+// Some callers have no way to hand the library a workspace: code running
+// under an allocator that forbids new device allocations once serving has
+// started, plugins loaded into a host program that owns all device memory,
+// or C callers without a CUDA allocator of their own.  For them the whole
+// fused step runs with its scratch (split plan, partial results, counters
+// and rotated queries) in one fixed array compiled into this library.
+//
+// The array is a file-scope __device__ variable, so every GPU that loads the
+// library holds kStaticScratchBytes of device memory until the process exits.
+// Host code cannot use the variable's name as a device address; the first
+// call on each device (with that device current) looks the address up with
+// cudaGetSymbolAddress and keeps it.  Make that first call before capturing
+// any stream.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;   // 16 MiB
+
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mutex;
+void* g_static_ptr[64] = {};
+
+// Device address of the array on the current device; set up once per device.
+pdattn_status static_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(PDATTN_EUNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (!g_static_ptr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+        if (e != cudaSuccess || ptr == nullptr) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        // The status word lives in the array; start it clean.
+        e = cudaMemset(ptr, 0, 256);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch control block");
+        g_static_ptr[dev] = ptr;
+    }
+    *out = g_static_ptr[dev];
+    return PDATTN_OK;
+}
+
+}  // namespace
+
+extern "C" pdattn_status pdattn_decode_fused_noalloc(const pdattn_params* p, const void* q, const void* k_new,
+                                                     const void* v_new, const int32_t* positions,
+                                                     const int32_t* table, void* k_pool, void* v_pool, void* out,
+                                                     pdattn_stream stream) {
+    g_launches = 0;
+    pdattn_status s = check_params(p);
+    if (s != PDATTN_OK) return s;
+    if (p->rows == 0) return PDATTN_OK;
+    const int grid = sm_count();
+    if (grid <= 0) return fail(PDATTN_ECUDA, "no CUDA device");
+    const size_t need = layout_for(p, grid).total;
+    if (need > kStaticScratchBytes)
+        return fail(PDATTN_EINVAL,
+                    "these parameters need %zu bytes of scratch, more than the %zu-byte static array of "
+                    "pdattn_decode_fused_noalloc; use pdattn_decode_fused with a workspace",
+                    need, kStaticScratchBytes);
+    void* scratch = nullptr;
+    s = static_scratch(&scratch);
+    if (s != PDATTN_OK) return s;
+    // The planner that runs first in this call resets every counter the
+    // attention kernel relies on, so nothing else in the array needs clearing.
+    return pdattn_decode_fused(p, q, k_new, v_new, positions, table, k_pool, v_pool, out, scratch,
+                               kStaticScratchBytes, stream);
+}
