@@ -250,7 +250,7 @@ def run_ours(args, w, world, rank, local):
     num_pages = t["k_pool"].shape[0]
     tables = b.rope_tables(w.rope_theta, w.head_dim, w.max_seq, w.torch_dtype) if w.rope_theta > 0 else (None, None)
     p = b.make_params(w.rows, w.heads, w.kv_heads, w.head_dim, w.pages_per_row, num_pages, w.torch_dtype,
-                      window=w.window, rope_cos=tables[0], rope_sin=tables[1])
+                      window=w.window, rope_cos=tables[0], rope_sin=tables[1], chunk_pages=args.chunk_pages)
     ws = b.new_workspace(p)
     out = torch.empty_like(t["q"])
     kvb = kv_bytes(w, pos_list)
@@ -296,8 +296,8 @@ def run_ours(args, w, world, rank, local):
     if args.quick:
         # profiling mode: warm-up and timed steps only
         if rank == 0:
-            print(json.dumps({"quick": True, "workload": w.name, "ms_per_step": ms,
-                              "kv_gbs": kvb / (ms * 1e-3) / 1e9}), flush=True)
+            print(json.dumps({"quick": True, "workload": w.name, "chunk_pages": args.chunk_pages,
+                              "ms_per_step": ms, "kv_gbs": kvb / (ms * 1e-3) / 1e9}), flush=True)
         return None
     ms = max_over_ranks(ms, world)
     all_kv = sum_over_ranks(kvb, world)
@@ -454,6 +454,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama8b_serving", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--chunk-pages", type=int, default=0,
+                    help="pages per split (0: the planner chooses)")
     ap.add_argument("--quick", action="store_true",
                     help="warm-up and timed steps only, no JSON line (for profiler captures)")
     args = ap.parse_args(argv)

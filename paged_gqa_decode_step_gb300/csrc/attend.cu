@@ -7,9 +7,12 @@
 // attention), with the cache addressed through the page table of the paged
 // entries (llama-3.1-8b-instruct architecture page, `decode_paged`).
 //
-// Design (one persistent CTA per SM, 5 warps):
-//   * warp 4 (producer) takes (row, kv head, chunk) items from the plan with
-//     an atomic cursor, and for every page of the chunk issues TMA loads of
+// Design (one persistent CTA per SM, 6 warps):
+//   * warp 5 (scheduler) takes (row, kv head, chunk) items from the plan with
+//     an atomic cursor, loads each item's descriptor and page ids, and queues
+//     them in shared memory a few items ahead, so that no global-memory
+//     latency sits between two TMA issues.
+//   * warp 4 (producer) pops items and, for every page, issues TMA loads of
 //     the page's K and V tiles (64 tokens x D, 128-byte swizzled) into a ring
 //     of shared-memory stages, plus a bulk copy of the item's query group on
 //     its first page.  Full / empty mbarriers hand stages over.
@@ -31,7 +34,12 @@
 namespace pdattn {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kSchedulerWarp = kConsumerWarps + 1;
+constexpr int kEpilogueWarp = kConsumerWarps + 2;
+constexpr int kThreads = (kConsumerWarps + 3) * 32;
+constexpr int kItemSlots = 4;           // items the scheduler may queue ahead
+constexpr int kEpiSlots = 2;            // finished items waiting for the epilogue warp
 constexpr float kNegBig = -1.0e30f;     // running-max start: finite, so exp2(m - m) = 1
 
 enum : int { kFirst = 1, kLast = 2, kValid = 4, kTerm = 8, kPartial = 16 };
@@ -56,9 +64,15 @@ struct Cfg {
     static constexpr int kOffMerge = kOffQ + kStages * kQBytes;
     static constexpr int kWarpQBytes = (kElem == 4) ? kConsumerWarps * kQBytes : 0;  // f32: private copies
     static constexpr int kOffWarpQ = kOffMerge + kMergeFloats * 4;
-    static constexpr int kOffMeta = kOffWarpQ + kWarpQBytes;
+    static constexpr int kOffItems = kOffWarpQ + kWarpQBytes;    // kItemSlots x (ItemDesc + 64 page ids)
+    static constexpr int kItemBytes = (int)sizeof(ItemDesc) + kChunkMax * 4;
+    // epilogue slots: Meta, (M, L) per head, O[head][D] (fp32, unnormalised)
+    static constexpr int kEpiBytes = (int)sizeof(Meta) + kMaxGroup * 8 + kMaxGroup * D * 4;
+    static constexpr int kOffEpi = kOffItems + kItemSlots * kItemBytes;
+    static constexpr int kOffMeta = kOffEpi + kEpiSlots * kEpiBytes;
     static constexpr int kOffBar = kOffMeta + kStages * (int)sizeof(Meta);
-    static constexpr int kOffMisc = kOffBar + 3 * kStages * 8 + 8;
+    static constexpr int kNumBars = 2 * kStages + 1 + 2 * kItemSlots + 2 * kEpiSlots;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffMisc + 16 + 1024;           // + alignment slack
     static_assert(kSmem <= 232448, "shared memory per CTA");
     static_assert(kOffBar % 8 == 0, "mbarrier alignment");
@@ -97,13 +111,13 @@ __device__ __forceinline__ void store8<float>(float* dst, const float (&v)[8]) {
 // ---------------------------------------------------------------------------
 // Consumer state and page processing
 // ---------------------------------------------------------------------------
-template <typename T, int D>
+template <typename T, int D, int G>
 struct Consumer;
 
-// bf16: tensor-core tiles.  Lane layout of the m16n8 accumulators:
+// bf16: tensor-core tiles (always 8 heads wide; G is unused).  Lane layout of the m16n8 accumulators:
 // row = lane / 4 (+8), column pair = 2 * (lane % 4).
-template <int D>
-struct Consumer<__nv_bfloat16, D> {
+template <int D, int G>
+struct Consumer<__nv_bfloat16, D, G> {
     static constexpr int KS = D / 16;     // k-steps over D for QK, m-tiles over D for PV
     uint32_t qf[KS][2];
     float o[KS][4];
@@ -130,13 +144,34 @@ struct Consumer<__nv_bfloat16, D> {
         // ---- S^T = K Q^T: 16 tokens x 8 heads
         float c[4] = {0.f, 0.f, 0.f, 0.f};
         {
+            // Issue every K fragment load before the MMAs (the loads stay in
+            // program order), then accumulate in two independent chains.
+            uint32_t ka[KS][4];
             const int tok = tok0 + ri + ((mi & 1) << 3);
             #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 const int chunk = ks * 2 + (mi >> 1);
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(swz128(kbase + (chunk >> 3) * 8192, tok, chunk & 7), a0, a1, a2, a3);
-                mma_bf16_16816(c, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+                ldsm_x4(swz128(kbase + (chunk >> 3) * 8192, tok, chunk & 7), ka[ks][0], ka[ks][1], ka[ks][2],
+                        ka[ks][3]);
+            }
+            float c2[4] = {0.f, 0.f, 0.f, 0.f};
+            #pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                if (ks & 1) mma_bf16_16816(c2, ka[ks][0], ka[ks][1], ka[ks][2], ka[ks][3], qf[ks][0], qf[ks][1]);
+                else mma_bf16_16816(c, ka[ks][0], ka[ks][1], ka[ks][2], ka[ks][3], qf[ks][0], qf[ks][1]);
+            }
+            #pragma unroll
+            for (int i = 0; i < 4; ++i) c[i] += c2[i];
+        }
+        // ---- V^T fragments, loaded now so their latency overlaps the softmax
+        uint32_t va_[KS][4];
+        {
+            const int tok = tok0 + ri + ((mi >> 1) << 3);
+            #pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                const int chunk = mt * 2 + (mi & 1);
+                ldsm_x4_trans(swz128(vbase + (chunk >> 3) * 8192, tok, chunk & 7), va_[mt][0], va_[mt][1],
+                              va_[mt][2], va_[mt][3]);
             }
         }
         // ---- online softmax (log2 domain)
@@ -169,8 +204,7 @@ struct Consumer<__nv_bfloat16, D> {
         }
         // ---- P^T into B-operand layout: B[k = token][n = head]
         const uint32_t b0 = movmatrix_trans(pa), b1 = movmatrix_trans(pb);
-        // ---- O^T += V^T P^T: V^T tiles from the V page with transposed ldmatrix
-        const int tok = tok0 + ri + ((mi >> 1) << 3);
+        // ---- O^T += V^T P^T with the V^T tiles loaded above
         uint32_t keep_a = 0xffffffffu, keep_b = 0xffffffffu;
         if (partial) {
             // zero V of invisible tokens: their slots may hold anything, NaN included
@@ -181,13 +215,9 @@ struct Consumer<__nv_bfloat16, D> {
                      ((t + 9 >= t_lo && t + 9 < t_hi) ? 0xffff0000u : 0u);
         }
         #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-            const int chunk = mt * 2 + (mi & 1);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_trans(swz128(vbase + (chunk >> 3) * 8192, tok, chunk & 7), a0, a1, a2, a3);
-            a0 &= keep_a; a1 &= keep_a; a2 &= keep_b; a3 &= keep_b;
-            mma_bf16_16816(o[mt], a0, a1, a2, a3, b0, b1);
-        }
+        for (int mt = 0; mt < KS; ++mt)
+            mma_bf16_16816(o[mt], va_[mt][0] & keep_a, va_[mt][1] & keep_a, va_[mt][2] & keep_b,
+                           va_[mt][3] & keep_b, b0, b1);
     }
 
     // Put this warp's (m, l, o) for heads 0..7 into the merge buffer.
@@ -218,30 +248,26 @@ struct Consumer<__nv_bfloat16, D> {
 };
 
 // f32: FP32 FMAs.  Scores: lane = (token lane % 16, half of D lane / 16).
-// Values: lane = dimension (lane + 32 e).
-template <int D>
-struct Consumer<float, D> {
+// Values: lane = dimension (lane + 32 e).  G bounds the group at compile time
+// so that the per-head state stays in registers.
+template <int D, int G>
+struct Consumer<float, D, G> {
     static constexpr int E = D / 32;
-    float o[kMaxGroup][E];
-    float m[kMaxGroup], l[kMaxGroup];
-    uint32_t qbuf_addr;
+    float o[G][E];
+    float m[G], l[G];
+    const float* wq;       // this warp's copy of the query group [g][D]
     int g;
 
     // The stage's query buffer can be refilled for a later item while this
     // item is still running, so each warp keeps its own copy.
-    __device__ void begin(uint32_t qbuf, uint32_t warp_q, int lane, int group) {
-        qbuf_addr = warp_q;
+    __device__ void begin(const float* qbuf, float* warp_q, int lane, int group) {
+        wq = warp_q;
         g = group;
-        for (int i = lane; i < group * D / 4; i += 32) {
-            float4 v;
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(qbuf + i * 16));
-            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
-                         :: "r"(warp_q + i * 16), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
-        }
+        for (int i = lane; i < group * D / 4; i += 32)
+            reinterpret_cast<float4*>(warp_q)[i] = reinterpret_cast<const float4*>(qbuf)[i];
         __syncwarp();
         #pragma unroll
-        for (int j = 0; j < kMaxGroup; ++j) {
+        for (int j = 0; j < G; ++j) {
             m[j] = kNegBig;
             l[j] = 0.f;
             #pragma unroll
@@ -249,29 +275,24 @@ struct Consumer<float, D> {
         }
     }
 
-    __device__ void page(uint32_t kbase, uint32_t vbase, int warp, int lane, int t_lo, int t_hi,
+    __device__ void page(const uint8_t* kbase, const uint8_t* vbase, int warp, int lane, int t_lo, int t_hi,
                          bool partial, float sl2) {
         const int tok0 = warp * 16;
         const int t = tok0 + (lane & 15), half = lane >> 4;
         constexpr int kChunks = D / 8;            // 16-byte chunks in half a row
-        float acc[kMaxGroup];
+        float acc[G];
         #pragma unroll
-        for (int j = 0; j < kMaxGroup; ++j) acc[j] = 0.f;
-        #pragma unroll
+        for (int j = 0; j < G; ++j) acc[j] = 0.f;
+        // partial unroll: enough loads in flight without hoisting every query chunk
+        #pragma unroll (G >= 4 ? 2 : 8)
         for (int c = 0; c < kChunks; ++c) {
             const int col = half * (D / 2) + c * 4;          // first dimension of the chunk
             const int box = col / 32, cin = (col % 32) / 4;
-            float4 kv;
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(kv.x), "=f"(kv.y), "=f"(kv.z), "=f"(kv.w)
-                         : "r"(swz128(kbase + box * 8192, t, cin)));
+            const float4 kv = *reinterpret_cast<const float4*>(kbase + swz128(box * 8192, t, cin));
             #pragma unroll
-            for (int j = 0; j < kMaxGroup; ++j) {
+            for (int j = 0; j < G; ++j) {
                 if (j < g) {
-                    float4 qv;
-                    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                                 : "=f"(qv.x), "=f"(qv.y), "=f"(qv.z), "=f"(qv.w)
-                                 : "r"(qbuf_addr + (j * D + col) * 4));
+                    const float4 qv = *reinterpret_cast<const float4*>(wq + j * D + col);
                     acc[j] = fmaf(kv.x, qv.x, acc[j]);
                     acc[j] = fmaf(kv.y, qv.y, acc[j]);
                     acc[j] = fmaf(kv.z, qv.z, acc[j]);
@@ -280,9 +301,9 @@ struct Consumer<float, D> {
             }
         }
         const bool valid = t >= t_lo && t < t_hi;
-        float p[kMaxGroup];
+        float p[G];
         #pragma unroll
-        for (int j = 0; j < kMaxGroup; ++j) {
+        for (int j = 0; j < G; ++j) {
             if (j < g) {
                 float s = acc[j] + __shfl_xor_sync(0xffffffffu, acc[j], 16);
                 s = valid ? s * sl2 : -INFINITY;
@@ -302,17 +323,14 @@ struct Consumer<float, D> {
             }
         }
         const int tt_lo = max(t_lo - tok0, 0), tt_hi = min(t_hi - tok0, 16);
-        #pragma unroll 1
+        #pragma unroll 4
         for (int tt = tt_lo; tt < tt_hi; ++tt) {
             float v[E];
             #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                asm volatile("ld.shared.f32 %0, [%1];"
-                             : "=f"(v[e])
-                             : "r"(swz128(vbase + e * 8192, tok0 + tt, lane >> 2) + (lane & 3) * 4));
-            }
+            for (int e = 0; e < E; ++e)
+                v[e] = *reinterpret_cast<const float*>(vbase + swz128(e * 8192, tok0 + tt, lane >> 2) + (lane & 3) * 4);
             #pragma unroll
-            for (int j = 0; j < kMaxGroup; ++j) {
+            for (int j = 0; j < G; ++j) {
                 if (j < g) {
                     const float pj = __shfl_sync(0xffffffffu, p[j], tt);
                     #pragma unroll
@@ -325,7 +343,7 @@ struct Consumer<float, D> {
 
     __device__ void stash(float* sm_m, float* sm_l, float* sm_o, int warp, int lane) {
         #pragma unroll
-        for (int j = 0; j < kMaxGroup; ++j) {
+        for (int j = 0; j < G; ++j) {
             if (j < g) {
                 if (lane == 0) {
                     sm_m[warp * kMaxGroup + j] = m[j];
@@ -341,7 +359,7 @@ struct Consumer<float, D> {
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <typename T, int D>
+template <typename T, int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
 attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
               const __grid_constant__ AttendArgs a) {
@@ -350,14 +368,20 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar_full = sbase + C::kOffBar;             // S barriers
-    const uint32_t bar_empty = bar_full + 8 * S;              // S barriers
+    const uint32_t bar_full = sbase + C::kOffBar;             // S barriers: stage holds data
+    const uint32_t bar_empty = bar_full + 8 * S;              // S barriers: stage may be refilled
     const uint32_t bar_sync = bar_empty + 8 * S;              // consumer barrier
+    const uint32_t bar_ifull = bar_sync + 8;                  // kItemSlots: item queued
+    const uint32_t bar_iempty = bar_ifull + 8 * kItemSlots;   // kItemSlots: item slot free
+    const uint32_t bar_efull = bar_iempty + 8 * kItemSlots;   // kEpiSlots: finished item queued
+    const uint32_t bar_eempty = bar_efull + 8 * kEpiSlots;    // kEpiSlots: epilogue slot free
     Meta* meta = reinterpret_cast<Meta*>(smem + C::kOffMeta);
     float* sm_m = reinterpret_cast<float*>(smem + C::kOffMerge);
     float* sm_l = sm_m + kConsumerWarps * kMaxGroup;
     float* sm_o = sm_l + kConsumerWarps * kMaxGroup;
     int* s_flag = reinterpret_cast<int*>(smem + C::kOffMisc);
+    uint8_t* item_q = smem + C::kOffItems;
+    uint8_t* epi_q = smem + C::kOffEpi;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -366,13 +390,21 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             mbar_init(bar_empty + 8 * s, kConsumerWarps);
         }
         mbar_init(bar_sync, kConsumerWarps * 32);
+        for (int s = 0; s < kItemSlots; ++s) {
+            mbar_init(bar_ifull + 8 * s, 1);
+            mbar_init(bar_iempty + 8 * s, 1);
+        }
+        for (int s = 0; s < kEpiSlots; ++s) {
+            mbar_init(bar_efull + 8 * s, kConsumerWarps * 32);
+            mbar_init(bar_eempty + 8 * s, 1);
+        }
         fence_barrier_init();
     }
     // Query-group buffers: rows past the group stay zero.
     for (int i = threadIdx.x; i < S * C::kQBytes / 16; i += kThreads)
         reinterpret_cast<uint4*>(smem + C::kOffQ)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_shared();
-    if (warp == kConsumerWarps && lane == 0) {
+    if (warp == kProducerWarp && lane == 0) {
         prefetch_tensormap(&k_map);
         prefetch_tensormap(&v_map);
     }
@@ -382,8 +414,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     griddep_wait();
 
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(a.ws + a.L.ctrl);
-    const int4* row_info = reinterpret_cast<const int4*>(a.ws + a.L.row_info);
-    const int2* items = reinterpret_cast<const int2*>(a.ws + a.L.items);
+    const ItemDesc* items = reinterpret_cast<const ItemDesc*>(a.ws + a.L.items);
     int* merge_cnt = reinterpret_cast<int*>(a.ws + a.L.merge_cnt);
     float2* part_ml = reinterpret_cast<float2*>(a.ws + a.L.part_ml);
     float* part_o = reinterpret_cast<float*>(a.ws + a.L.part_o);
@@ -400,46 +431,99 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         return;
     }
 
-    if (warp == kConsumerWarps) {
+    if (warp == kSchedulerWarp) {
+        // ================= scheduler =================
+        // Item slot layout: ItemDesc (npg < 0 marks the end), then 64 page ids.
+        int islot = 0;
+        uint32_t iphase = 0;
+        bool ok = true;
+        while (true) {
+            int it = 0;
+            if (lane == 0) it = atomicAdd(&ctrl->next_item, 1);
+            it = __shfl_sync(0xffffffffu, it, 0);
+            const bool term = it >= n_items;
+            int4 d0 = make_int4(0, 0, 0, 0), d1 = make_int4(0, -1, 0, 0);
+            int pid0 = -1, pid1 = -1;
+            bool good = true;
+            if (!term) {
+                d0 = __ldcg(reinterpret_cast<const int4*>(items + it));
+                d1 = __ldcg(reinterpret_cast<const int4*>(items + it) + 1);
+                const int row = d0.x, kvh = d0.y >> 16, chunk = d0.y & 0xffff, nch = d0.z, slot = d0.w;
+                const int first = d1.x, npg = d1.y, pos = d1.z, lo = d1.w;
+                good = row >= 0 && row < a.rows && kvh < Hk && chunk < nch && slot >= 0 && slot < n_items &&
+                       npg >= 1 && npg <= chunk_pages && first >= 0 && pos >= 0 && lo >= 0 && lo <= pos &&
+                       pos < a.pages_per_row * kPageSize && first + npg - 1 <= pos / kPageSize &&
+                       first >= lo / kPageSize;
+                if (good) {
+                    const int* trow = a.table + (size_t)row * a.pages_per_row + first;
+                    if (lane < npg) pid0 = __ldg(trow + lane);
+                    if (lane + 32 < npg) pid1 = __ldg(trow + lane + 32);
+                } else if (lane == 0) {
+                    set_error(ctrl, kErrBadPlan);
+                }
+            }
+            if (!good) continue;
+            int waited = 1;
+            if (lane == 0) waited = mbar_wait(bar_iempty + 8 * islot, iphase ^ 1) ? 1 : 0;
+            waited = __shfl_sync(0xffffffffu, waited, 0);
+            if (!waited) { ok = false; break; }
+            uint8_t* slotp = item_q + islot * C::kItemBytes;
+            if (lane == 0) {
+                if (term) d1.y = -1;
+                reinterpret_cast<int4*>(slotp)[0] = d0;
+                reinterpret_cast<int4*>(slotp)[1] = d1;
+            }
+            int* pids = reinterpret_cast<int*>(slotp + sizeof(ItemDesc));
+            pids[lane] = pid0;
+            pids[lane + 32] = pid1;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_ifull + 8 * islot);
+            if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
+            if (term) break;
+        }
+        if (lane == 0) {
+            if (ok) {
+                // Last CTA to finish fetching rewinds the cursor for the next launch.
+                __threadfence();
+                if (atomicAdd(&ctrl->done_ctas, 1) == (int)gridDim.x - 1) {
+                    ctrl->next_item = 0;
+                    ctrl->done_ctas = 0;
+                }
+            } else {
+                set_error(ctrl, kErrTimeout);
+            }
+        }
+        return;
+    }
+
+    if (warp == kProducerWarp) {
         // ================= producer =================
         int stage = 0;
         uint32_t phase = 0;
+        int islot = 0;
+        uint32_t iphase = 0;
         uint32_t armed = 0;                 // bit s: stage s has an unfinished arm
         uint32_t armed_par = 0;             // parity armed on stage s
         bool ok = true;
-        int it = 0;
-        if (lane == 0) it = atomicAdd(&ctrl->next_item, 1);
-        it = __shfl_sync(0xffffffffu, it, 0);
-        while (ok && it < n_items) {
-            int nxt = 0;
-            if (lane == 0) nxt = atomicAdd(&ctrl->next_item, 1);
-            const int2 item = __ldcg(items + it);
-            const int row = item.x, kvh = item.y >> 16, chunk = item.y & 0xffff;
-            bool good = row >= 0 && row < a.rows && kvh < Hk;
-            int4 ri = make_int4(-1, 0, 0, 0);
-            if (good) ri = __ldcg(row_info + row);
-            const int pos = ri.x, lo = ri.y, nch = ri.z;
-            const int slot = ri.w + kvh * nch + chunk;
-            good = good && pos >= 0 && lo >= 0 && lo <= pos && chunk < nch &&
-                   pos < a.pages_per_row * kPageSize && slot >= 0 && slot < n_items;
-            if (!good) {
-                if (lane == 0) set_error(ctrl, kErrBadPlan);
-                it = __shfl_sync(0xffffffffu, nxt, 0);
-                continue;
-            }
-            const int first_page = lo / kPageSize + chunk * chunk_pages;
-            const int last_page = min(first_page + chunk_pages - 1, pos / kPageSize);
-            const int npg = last_page - first_page + 1;
-            const int* trow = a.table + (size_t)row * a.pages_per_row;
-            const int pid0 = lane < npg ? __ldg(trow + first_page + lane) : -1;
-            const int pid1 = lane + 32 < npg ? __ldg(trow + first_page + lane + 32) : -1;
+        while (ok) {
+            int waited = 1;
+            if (lane == 0) waited = mbar_wait(bar_ifull + 8 * islot, iphase) ? 1 : 0;
+            waited = __shfl_sync(0xffffffffu, waited, 0);
+            if (!waited) { ok = false; break; }
+            const uint8_t* slotp = item_q + islot * C::kItemBytes;
+            const int4 d0 = reinterpret_cast<const int4*>(slotp)[0];
+            const int4 d1 = reinterpret_cast<const int4*>(slotp)[1];
+            const int* pids = reinterpret_cast<const int*>(slotp + sizeof(ItemDesc));
+            const int npg = d1.y;
+            if (npg < 0) break;             // end of the work
+            const int row = d0.x, kvh = d0.y >> 16, chunk = d0.y & 0xffff, nch = d0.z, slot = d0.w;
+            const int first_page = d1.x, pos = d1.z, lo = d1.w;
             for (int j = 0; j < npg; ++j) {
-                const int pid = __shfl_sync(0xffffffffu, j < 32 ? pid0 : pid1, j & 31);
-                int waited = 1;
                 if (lane == 0) waited = mbar_wait(bar_empty + 8 * stage, phase ^ 1) ? 1 : 0;
                 waited = __shfl_sync(0xffffffffu, waited, 0);
                 if (!waited) { ok = false; break; }
                 if (lane == 0) {
+                    const int pid = pids[j];
                     const bool pvalid = pid >= 0 && pid < a.num_pages;
                     if (!pvalid) set_error(ctrl, kErrBadPage);
                     const int p = first_page + j, t0 = p * kPageSize;
@@ -454,7 +538,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                                ((mt.t_lo > 0 || mt.t_hi < kPageSize) ? kPartial : 0);
                     mt.chunk = chunk;
                     meta[stage] = mt;
-                    uint32_t bytes = (pvalid ? C::kStageBytes : 0) + (j == 0 ? g * D * C::kElem : 0);
+                    const uint32_t bytes = (pvalid ? C::kStageBytes : 0) + (j == 0 ? g * D * C::kElem : 0);
                     const uint32_t fb = bar_full + 8 * stage;
                     mbar_arrive_expect_tx(fb, bytes);
                     const uint32_t dst = sbase + stage * C::kStageBytes;
@@ -476,7 +560,10 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                 __syncwarp();
                 if (++stage == S) { stage = 0; phase ^= 1; }
             }
-            it = __shfl_sync(0xffffffffu, nxt, 0);
+            if (!ok) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_iempty + 8 * islot);
+            if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
         }
         if (ok) {
             // Terminator: the next stage carries no data, only the end flag.
@@ -489,33 +576,110 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             }
             ok = waited != 0;
         }
-        if (lane == 0) {
-            if (ok) {
-                // Last CTA to finish fetching rewinds the cursor for the next launch.
-                __threadfence();
-                if (atomicAdd(&ctrl->done_ctas, 1) == (int)gridDim.x - 1) {
-                    ctrl->next_item = 0;
-                    ctrl->done_ctas = 0;
+        if (!ok && lane == 0) {
+            set_error(ctrl, kErrTimeout);
+            // Let copies in flight land before the CTA's shared memory goes away.
+            for (int s = 0; s < S; ++s)
+                if (armed & (1u << s)) mbar_wait(bar_full + 8 * s, (armed_par >> s) & 1u, 200000000ull);
+        }
+        return;
+    }
+
+    if (warp == kEpilogueWarp) {
+        // ================= epilogue =================
+        // Writes finished items: the output when the (row, kv head) is one
+        // chunk, else the chunk's fp32 partial; the last chunk of a (row, kv
+        // head) to arrive merges every partial and writes the output.
+        int eslot = 0;
+        uint32_t ephase = 0;
+        while (true) {
+            int waited = 1;
+            if (lane == 0) waited = mbar_wait(bar_efull + 8 * eslot, ephase) ? 1 : 0;
+            waited = __shfl_sync(0xffffffffu, waited, 0);
+            if (!waited) { if (lane == 0) set_error(ctrl, kErrTimeout); break; }
+            const uint8_t* ep = epi_q + eslot * C::kEpiBytes;
+            const Meta mt = *reinterpret_cast<const Meta*>(ep);
+            if (mt.flags & kTerm) break;
+            const float2* eml = reinterpret_cast<const float2*>(ep + sizeof(Meta));
+            const float* eo = reinterpret_cast<const float*>(ep + sizeof(Meta) + kMaxGroup * 8);
+            const int row = mt.row, kvh = mt.kvh, nch = mt.nch, slot = mt.slot;
+            T* out_base = static_cast<T*>(a.out) + ((size_t)row * a.heads + kvh * g) * D;
+            if (nch == 1) {
+                for (int u = lane; u < g * D / 8; u += 32) {
+                    const int j = u / (D / 8), d0 = (u % (D / 8)) * 8;
+                    const float inv = 1.f / eml[j].y;
+                    float O[8];
+                    #pragma unroll
+                    for (int e = 0; e < 8; ++e) O[e] = eo[j * D + d0 + e] * inv;
+                    store8<T>(out_base + j * D + d0, O);
                 }
             } else {
-                set_error(ctrl, kErrTimeout);
-                // Let copies in flight land before the CTA's shared memory goes away.
-                for (int s = 0; s < S; ++s)
-                    if (armed & (1u << s)) mbar_wait(bar_full + 8 * s, (armed_par >> s) & 1u, 200000000ull);
+                for (int u = lane; u < g * D / 8; u += 32) {
+                    const int j = u / (D / 8), d0 = (u % (D / 8)) * 8;
+                    float4* dst = reinterpret_cast<float4*>(part_o + ((size_t)slot * g + j) * D + d0);
+                    dst[0] = *reinterpret_cast<const float4*>(eo + j * D + d0);
+                    dst[1] = *reinterpret_cast<const float4*>(eo + j * D + d0 + 4);
+                }
+                if (lane < g) part_ml[(size_t)slot * g + lane] = eml[lane];
+                __syncwarp();
+                int last = 0;
+                if (lane == 0) {
+                    __threadfence();
+                    const int done = atomicAdd(merge_cnt + (size_t)row * Hk + kvh, 1);
+                    last = done == nch - 1;
+                    if (last) {
+                        merge_cnt[(size_t)row * Hk + kvh] = 0;
+                        __threadfence();
+                    }
+                }
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    // out = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c over the chunks
+                    const int slot0 = slot - mt.chunk;
+                    for (int u = lane; u < g * D / 8; u += 32) {
+                        const int j = u / (D / 8), d0 = (u % (D / 8)) * 8;
+                        float M = kNegBig;
+                        for (int c = 0; c < nch; ++c) M = fmaxf(M, __ldcg(part_ml + (size_t)(slot0 + c) * g + j).x);
+                        float L = 0.f, O[8];
+                        #pragma unroll
+                        for (int e = 0; e < 8; ++e) O[e] = 0.f;
+                        #pragma unroll 4
+                        for (int c = 0; c < nch; ++c) {
+                            const float2 ml = __ldcg(part_ml + (size_t)(slot0 + c) * g + j);
+                            const float4* src = reinterpret_cast<const float4*>(part_o + ((size_t)(slot0 + c) * g + j) * D + d0);
+                            const float4 p0 = __ldcg(src), p1 = __ldcg(src + 1);
+                            const float f = exp2_approx(ml.x - M);
+                            L += f * ml.y;
+                            O[0] += f * p0.x; O[1] += f * p0.y; O[2] += f * p0.z; O[3] += f * p0.w;
+                            O[4] += f * p1.x; O[5] += f * p1.y; O[6] += f * p1.z; O[7] += f * p1.w;
+                        }
+                        const float inv = 1.f / L;
+                        #pragma unroll
+                        for (int e = 0; e < 8; ++e) O[e] *= inv;
+                        store8<T>(out_base + j * D + d0, O);
+                    }
+                }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_eempty + 8 * eslot);
+            if (++eslot == kEpiSlots) { eslot = 0; ephase ^= 1; }
         }
         return;
     }
 
     // ================= consumers =================
-    Consumer<T, D> cs;
+    Consumer<T, D, G> cs;
     ConsumerSync csync{bar_sync, 0};
     int stage = 0;
     uint32_t phase = 0;
+    int eslot = 0;
+    uint32_t ephase = 0;
     const int tid = threadIdx.x;     // 0..127
+    bool ok = true;
     while (true) {
         if (!mbar_wait(bar_full + 8 * stage, phase)) {
             if (lane == 0) set_error(ctrl, kErrTimeout);
+            ok = false;
             break;
         }
         const Meta mt = meta[stage];
@@ -525,21 +689,32 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             if constexpr (sizeof(T) == 2)
                 cs.begin(sbase + C::kOffQ + stage * C::kQBytes, lane);
             else
-                cs.begin(sbase + C::kOffQ + stage * C::kQBytes, sbase + C::kOffWarpQ + warp * C::kQBytes,
-                         lane, g);
+                cs.begin(reinterpret_cast<const float*>(smem + C::kOffQ + stage * C::kQBytes),
+                         reinterpret_cast<float*>(smem + C::kOffWarpQ + warp * C::kQBytes), lane, g);
         }
-        if (mt.flags & kValid)
-            cs.page(kbase, kbase + C::kTileBytes, warp, lane, mt.t_lo, mt.t_hi, (mt.flags & kPartial) != 0,
-                    a.scale_log2);
+        if (mt.flags & kValid) {
+            if constexpr (sizeof(T) == 2)
+                cs.page(kbase, kbase + C::kTileBytes, warp, lane, mt.t_lo, mt.t_hi, (mt.flags & kPartial) != 0,
+                        a.scale_log2);
+            else
+                cs.page(smem + stage * C::kStageBytes, smem + stage * C::kStageBytes + C::kTileBytes, warp, lane,
+                        mt.t_lo, mt.t_hi, (mt.flags & kPartial) != 0, a.scale_log2);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
         if (++stage == S) { stage = 0; phase ^= 1; }
         if (!(mt.flags & kLast)) continue;
 
-        // ---- item done: merge the four warps
+        // ---- item done: merge the four warps into an epilogue slot
         cs.stash(sm_m, sm_l, sm_o, warp, lane);
-        if (!csync.sync()) { if (lane == 0) set_error(ctrl, kErrTimeout); break; }
-        const int row = mt.row, kvh = mt.kvh, nch = mt.nch, slot = mt.slot;
+        if (!csync.sync() || !mbar_wait(bar_eempty + 8 * eslot, ephase ^ 1)) {
+            if (lane == 0) set_error(ctrl, kErrTimeout);
+            ok = false;
+            break;
+        }
+        uint8_t* ep = epi_q + eslot * C::kEpiBytes;
+        float2* eml = reinterpret_cast<float2*>(ep + sizeof(Meta));
+        float* eo = reinterpret_cast<float*>(ep + sizeof(Meta) + kMaxGroup * 8);
         const int units = D / 8;
         const int j = tid / units, d0 = (tid % units) * 8;
         if (j < g) {
@@ -557,64 +732,35 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                 #pragma unroll
                 for (int e = 0; e < 8; ++e) O[e] += f * src[e];
             }
-            if (nch == 1) {
-                const float inv = 1.f / L;
-                #pragma unroll
-                for (int e = 0; e < 8; ++e) O[e] *= inv;
-                store8<T>(static_cast<T*>(a.out) + ((size_t)row * a.heads + kvh * g + j) * D + d0, O);
-            } else {
-                float* dst = part_o + ((size_t)slot * g + j) * D + d0;
-                reinterpret_cast<float4*>(dst)[0] = make_float4(O[0], O[1], O[2], O[3]);
-                reinterpret_cast<float4*>(dst)[1] = make_float4(O[4], O[5], O[6], O[7]);
-                if (d0 == 0) part_ml[(size_t)slot * g + j] = make_float2(M, L);
-            }
+            reinterpret_cast<float4*>(eo + j * D + d0)[0] = make_float4(O[0], O[1], O[2], O[3]);
+            reinterpret_cast<float4*>(eo + j * D + d0)[1] = make_float4(O[4], O[5], O[6], O[7]);
+            if (d0 == 0) eml[j] = make_float2(M, L);
         }
-        if (nch > 1) {
-            __threadfence();
-            if (!csync.sync()) { if (lane == 0) set_error(ctrl, kErrTimeout); break; }
-            if (tid == 0) {
-                const int done = atomicAdd(merge_cnt + (size_t)row * Hk + kvh, 1);
-                *s_flag = (done == nch - 1);
-                if (done == nch - 1) merge_cnt[(size_t)row * Hk + kvh] = 0;
-            }
-            if (!csync.sync()) { if (lane == 0) set_error(ctrl, kErrTimeout); break; }
-            if (*s_flag && j < g) {
-                // Last chunk of this (row, kv head) to finish: merge every
-                // chunk's partial, out = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c.
-                __threadfence();
-                const int slot0 = slot - mt.chunk;
-                float M = kNegBig;
-                for (int c = 0; c < nch; ++c) M = fmaxf(M, __ldcg(part_ml + (size_t)(slot0 + c) * g + j).x);
-                float L = 0.f, O[8];
-                #pragma unroll
-                for (int e = 0; e < 8; ++e) O[e] = 0.f;
-                for (int c = 0; c < nch; ++c) {
-                    const float2 ml = __ldcg(part_ml + (size_t)(slot0 + c) * g + j);
-                    const float f = exp2_approx(ml.x - M);
-                    L += f * ml.y;
-                    const float4* src = reinterpret_cast<const float4*>(part_o + ((size_t)(slot0 + c) * g + j) * D + d0);
-                    const float4 u = __ldcg(src), v = __ldcg(src + 1);
-                    O[0] += f * u.x; O[1] += f * u.y; O[2] += f * u.z; O[3] += f * u.w;
-                    O[4] += f * v.x; O[5] += f * v.y; O[6] += f * v.z; O[7] += f * v.w;
-                }
-                const float inv = 1.f / L;
-                #pragma unroll
-                for (int e = 0; e < 8; ++e) O[e] *= inv;
-                store8<T>(static_cast<T*>(a.out) + ((size_t)row * a.heads + kvh * g + j) * D + d0, O);
-            }
+        if (tid == 0) *reinterpret_cast<Meta*>(ep) = mt;
+        mbar_arrive(bar_efull + 8 * eslot);
+        if (++eslot == kEpiSlots) { eslot = 0; ephase ^= 1; }
+        // the stash buffers are rewritten by the next item
+        if (!csync.sync()) { if (lane == 0) set_error(ctrl, kErrTimeout); ok = false; break; }
+    }
+    if (ok) {
+        // Tell the epilogue warp that no more items follow.
+        if (mbar_wait(bar_eempty + 8 * eslot, ephase ^ 1)) {
+            if (tid == 0) reinterpret_cast<Meta*>(epi_q + eslot * C::kEpiBytes)->flags = kTerm;
+            mbar_arrive(bar_efull + 8 * eslot);
+        } else if (lane == 0) {
+            set_error(ctrl, kErrTimeout);
         }
-        if (!csync.sync()) { if (lane == 0) set_error(ctrl, kErrTimeout); break; }
     }
 }
 
 // ---------------------------------------------------------------------------
 // Host launcher
 // ---------------------------------------------------------------------------
-template <typename T, int D>
+template <typename T, int D, int G>
 static cudaError_t launch_one(const AttendArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
                               int grid, bool programmatic, cudaStream_t stream) {
     using C = Cfg<T, D>;
-    auto kern = attend_kernel<T, D>;
+    auto kern = attend_kernel<T, D, G>;
     // The shared-memory opt-in is per function and device; setting it again is cheap.
     static int configured_mask = 0;   // bit per device id < 31
     int dev = 0;
@@ -638,16 +784,23 @@ static cudaError_t launch_one(const AttendArgs& a, const CUtensorMap& k_map, con
     return cudaLaunchKernelEx(&cfg, kern, k_map, v_map, a);
 }
 
+template <int D>
+static cudaError_t launch_f32(const AttendArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map, int grid,
+                              bool programmatic, cudaStream_t stream) {
+    if (a.group <= 1) return launch_one<float, D, 1>(a, k_map, v_map, grid, programmatic, stream);
+    if (a.group <= 2) return launch_one<float, D, 2>(a, k_map, v_map, grid, programmatic, stream);
+    if (a.group <= 4) return launch_one<float, D, 4>(a, k_map, v_map, grid, programmatic, stream);
+    return launch_one<float, D, 8>(a, k_map, v_map, grid, programmatic, stream);
+}
+
 cudaError_t launch_attend(const AttendArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
                           int dtype, int grid, bool programmatic, cudaStream_t stream) {
     if (dtype == 0 && a.head_dim == 128)
-        return launch_one<__nv_bfloat16, 128>(a, k_map, v_map, grid, programmatic, stream);
+        return launch_one<__nv_bfloat16, 128, kMaxGroup>(a, k_map, v_map, grid, programmatic, stream);
     if (dtype == 0 && a.head_dim == 64)
-        return launch_one<__nv_bfloat16, 64>(a, k_map, v_map, grid, programmatic, stream);
-    if (dtype == 1 && a.head_dim == 128)
-        return launch_one<float, 128>(a, k_map, v_map, grid, programmatic, stream);
-    if (dtype == 1 && a.head_dim == 64)
-        return launch_one<float, 64>(a, k_map, v_map, grid, programmatic, stream);
+        return launch_one<__nv_bfloat16, 64, kMaxGroup>(a, k_map, v_map, grid, programmatic, stream);
+    if (dtype == 1 && a.head_dim == 128) return launch_f32<128>(a, k_map, v_map, grid, programmatic, stream);
+    if (dtype == 1 && a.head_dim == 64) return launch_f32<64>(a, k_map, v_map, grid, programmatic, stream);
     return cudaErrorInvalidValue;
 }
 

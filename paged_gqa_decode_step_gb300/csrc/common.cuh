@@ -14,7 +14,7 @@ namespace pdattn {
 constexpr int kPageSize = 64;
 constexpr int kMaxGroup = 8;          // query heads per kv head (the MMA's N)
 constexpr int kChunkMax = 64;         // largest pages-per-split the planner picks
-constexpr int kItemsPerCta = 8;       // planner's target work items per persistent CTA
+constexpr int kItemsPerCta = 4;       // planner's target work items per persistent CTA
 constexpr uint32_t kPlanMagic = 0x70646174u;
 
 // Status bits in the workspace's status word.
@@ -35,6 +35,15 @@ struct Ctrl {
     int pad[52];
 };
 static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
+
+// One work item of the plan: pages [first_page, first_page + npg) of one
+// (row, kv head), chunk `chunk` of `nch`; `slot` indexes its fp32 partial.
+// Self-contained so that the scheduler needs one load per item.
+struct __align__(32) ItemDesc {
+    int row, kvh_chunk, nch, slot;     // kvh_chunk = kv_head << 16 | chunk
+    int first_page, npg, pos, lo;      // visible positions of the row: [lo, pos]
+};
+static_assert(sizeof(ItemDesc) == 32, "item descriptor is 32 bytes");
 
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
@@ -68,7 +77,7 @@ __host__ __device__ inline WsLayout ws_layout(int rows, int heads, int kv_heads,
     size_t off = 0;
     L.ctrl = off; off += 256;
     L.row_info = off; off = align256(off + sizeof(int4) * (size_t)rows);
-    L.items = off; off = align256(off + sizeof(int2) * (size_t)L.max_items);
+    L.items = off; off = align256(off + sizeof(ItemDesc) * (size_t)L.max_items);
     L.merge_cnt = off; off = align256(off + sizeof(int) * (size_t)rows * kv_heads);
     L.part_ml = off; off = align256(off + sizeof(float2) * (size_t)L.max_items * g);
     L.part_o = off; off = align256(off + sizeof(float) * (size_t)L.max_items * g * head_dim);
@@ -188,9 +197,11 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
                  : "r"(addr));
 }
 
+// Register-only instructions are not volatile so the compiler may schedule
+// them around the (volatile, ordered) shared-memory loads.
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     uint32_t y;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
     return y;
 }
 
@@ -198,7 +209,7 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
                                                uint32_t a2, uint32_t a3, uint32_t b0,
                                                uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
         "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])

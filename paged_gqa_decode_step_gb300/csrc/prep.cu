@@ -181,7 +181,8 @@ __device__ __forceinline__ int row_lo(int pos, int window) {
 // One block.  Splits every row's visible pages [lo / 64, pos / 64] into
 // chunks of C pages and lists the (row, kv head, chunk) items sorted by size,
 // largest first (a counting sort over the C sizes), so that the persistent
-// attention kernel hands out long items before short ones.
+// attention kernel hands out long items before short ones.  Each row reserves
+// its items' places with one atomic per size it uses.
 __device__ void build_plan(const PrepArgs& a) {
     __shared__ int s_cnt[kChunkMax + 1];
     __shared__ int s_cur[kChunkMax + 1];
@@ -190,7 +191,7 @@ __device__ void build_plan(const PrepArgs& a) {
     __shared__ int s_chunk;
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(a.ws + a.L.ctrl);
     int4* row_info = reinterpret_cast<int4*>(a.ws + a.L.row_info);
-    int2* items = reinterpret_cast<int2*>(a.ws + a.L.items);
+    ItemDesc* items = reinterpret_cast<ItemDesc*>(a.ws + a.L.items);
     int* merge_cnt = reinterpret_cast<int*>(a.ws + a.L.merge_cnt);
     const int tid = threadIdx.x, R = a.rows, Hk = a.kv_heads, max_pos = a.pages_per_row * kPageSize;
 
@@ -203,7 +204,8 @@ __device__ void build_plan(const PrepArgs& a) {
         const int pos = __ldg(a.positions + r);
         if (pos >= 0 && pos < max_pos) w += pos / kPageSize - row_lo(pos, a.window) / kPageSize + 1;
     }
-    if (w) atomicAdd(&s_work, w);
+    w = __reduce_add_sync(0xffffffffu, (unsigned)w);
+    if ((tid & 31) == 0 && w) atomicAdd(&s_work, w);
     __syncthreads();
     if (tid == 0) {
         int c = a.chunk_pages;
@@ -241,14 +243,32 @@ __device__ void build_plan(const PrepArgs& a) {
     const int n_items = s_cnt[0];
     const bool fits = n_items <= a.L.max_items;
     if (fits) {
-        for (long long pr = tid; pr < (long long)R * Hk; pr += blockDim.x) {
-            const int r = (int)(pr / Hk), h = (int)(pr % Hk);
-            const int pos = __ldg(a.positions + r);
-            if (pos < 0 || pos >= max_pos) continue;
-            const int n = pos / kPageSize - row_lo(pos, a.window) / kPageSize + 1;
+        for (int r = tid; r < R; r += blockDim.x) {
+            const int4 ri = row_info[r];
+            const int pos = ri.x, lo = ri.y, nch = ri.z, base = ri.w;
+            if (pos < 0) continue;
+            const int first = lo / kPageSize;
+            const int n = pos / kPageSize - first + 1;
             const int full = n / C, tail = n % C;
-            for (int c = 0; c < full; ++c) items[atomicAdd(&s_cur[C], 1)] = make_int2(r, (h << 16) | c);
-            if (tail) items[atomicAdd(&s_cur[tail], 1)] = make_int2(r, (h << 16) | full);
+            const int at_full = full ? atomicAdd(&s_cur[C], full * Hk) : 0;
+            const int at_tail = tail ? atomicAdd(&s_cur[tail], Hk) : 0;
+            for (int c = 0; c < nch; ++c) {
+                const int npg = c < full ? C : tail;
+                for (int h = 0; h < Hk; ++h) {
+                    ItemDesc d;
+                    d.row = r;
+                    d.kvh_chunk = (h << 16) | c;
+                    d.nch = nch;
+                    d.slot = base + h * nch + c;
+                    d.first_page = first + c * C;
+                    d.npg = npg;
+                    d.pos = pos;
+                    d.lo = lo;
+                    const int at = c < full ? at_full + c * Hk + h : at_tail + h;
+                    reinterpret_cast<int4*>(items + at)[0] = make_int4(d.row, d.kvh_chunk, d.nch, d.slot);
+                    reinterpret_cast<int4*>(items + at)[1] = make_int4(d.first_page, d.npg, d.pos, d.lo);
+                }
+            }
         }
     }
     __syncthreads();

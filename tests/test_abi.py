@@ -123,7 +123,7 @@ def test_workspace_layout_bound_covers_every_plan():
     import math
     import random
     rnd = random.Random(3)
-    items_per_cta, chunk_max = 8, 64
+    items_per_cta, chunk_max = 4, 64
     for _ in range(300):
         R, Hk, Pg, grid = rnd.randint(1, 300), rnd.choice([1, 2, 8, 12]), rnd.randint(1, 128), rnd.choice([1, 20, 152])
         pos = [rnd.randint(0, Pg * 64 - 1) for _ in range(R)]
