@@ -38,7 +38,7 @@ constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kSchedulerWarp = kConsumerWarps + 1;
 constexpr int kEpilogueWarp = kConsumerWarps + 2;
 constexpr int kThreads = (kConsumerWarps + 3) * 32;
-constexpr int kItemSlots = 4;           // items the scheduler may queue ahead
+constexpr int kItemSlots = 1;           // items the scheduler may hold ahead of the producer
 constexpr int kEpiSlots = 2;            // finished items waiting for the epilogue warp
 constexpr float kNegBig = -1.0e30f;     // running-max start: finite, so exp2(m - m) = 1
 
@@ -63,8 +63,10 @@ struct Cfg {
     static constexpr int kOffQ = kStages * kStageBytes;
     static constexpr int kOffMerge = kOffQ + kStages * kQBytes;
     static constexpr int kWarpQBytes = (kElem == 4) ? kConsumerWarps * kQBytes : 0;  // f32: private copies
+    static constexpr int kWarpPBytes = (kElem == 4) ? kConsumerWarps * kMaxGroup * 16 * 4 : 0;  // f32: p buffers
     static constexpr int kOffWarpQ = kOffMerge + kMergeFloats * 4;
-    static constexpr int kOffItems = kOffWarpQ + kWarpQBytes;    // kItemSlots x (ItemDesc + 64 page ids)
+    static constexpr int kOffWarpP = kOffWarpQ + kWarpQBytes;
+    static constexpr int kOffItems = kOffWarpP + kWarpPBytes;    // kItemSlots x (ItemDesc + 64 page ids)
     static constexpr int kItemBytes = (int)sizeof(ItemDesc) + kChunkMax * 4;
     // epilogue slots: Meta, (M, L) per head, O[head][D] (fp32, unnormalised)
     static constexpr int kEpiBytes = (int)sizeof(Meta) + kMaxGroup * 8 + kMaxGroup * D * 4;
@@ -247,52 +249,72 @@ struct Consumer<__nv_bfloat16, D, G> {
     }
 };
 
-// f32: FP32 FMAs.  Scores: lane = (token lane % 16, half of D lane / 16).
-// Values: lane = dimension (lane + 32 e).  G bounds the group at compile time
-// so that the per-head state stays in registers.
+// f32: FP32 FMAs.
+//   scores: lane = (token tok0 + lane % 16, half of D lane / 16), the halves
+//           summed with one shuffle;
+//   values: lane = (token parity lane / 16, VD consecutive dimensions
+//           (lane % 16) * VD), so each lane loads 16-byte pieces of V rows and
+//           the two parities are summed once per item in stash().
+// The probabilities go through a small per-warp buffer (read back as
+// broadcast float4s).  G bounds the group at compile time; a one-head group
+// keeps its query in registers.
 template <int D, int G>
 struct Consumer<float, D, G> {
-    static constexpr int E = D / 32;
-    float o[G][E];
+    static constexpr int VD = D / 16;          // value dimensions per lane
+    static constexpr bool kQRegs = (G == 1);
+    float o[G][VD];
     float m[G], l[G];
-    const float* wq;       // this warp's copy of the query group [g][D]
+    float qr[kQRegs ? D / 2 : 1];
+    const float* wq;       // this warp's copy of the query group [g][D] (G > 1)
+    float* sp;             // this warp's probabilities [kMaxGroup][16]
     int g;
 
-    // The stage's query buffer can be refilled for a later item while this
-    // item is still running, so each warp keeps its own copy.
-    __device__ void begin(const float* qbuf, float* warp_q, int lane, int group) {
-        wq = warp_q;
+    __device__ void begin(const float* qbuf, float* warp_q, float* warp_p, int lane, int group) {
         g = group;
-        for (int i = lane; i < group * D / 4; i += 32)
-            reinterpret_cast<float4*>(warp_q)[i] = reinterpret_cast<const float4*>(qbuf)[i];
-        __syncwarp();
+        sp = warp_p;
+        if constexpr (kQRegs) {
+            const int half = lane >> 4;
+            #pragma unroll
+            for (int i = 0; i < D / 8; ++i) {
+                const float4 v = reinterpret_cast<const float4*>(qbuf + half * (D / 2))[i];
+                qr[4 * i] = v.x; qr[4 * i + 1] = v.y; qr[4 * i + 2] = v.z; qr[4 * i + 3] = v.w;
+            }
+            wq = nullptr;
+        } else {
+            // The stage's query buffer can be refilled for a later item while
+            // this item is still running, so each warp keeps its own copy.
+            wq = warp_q;
+            for (int i = lane; i < group * D / 4; i += 32)
+                reinterpret_cast<float4*>(warp_q)[i] = reinterpret_cast<const float4*>(qbuf)[i];
+            __syncwarp();
+        }
         #pragma unroll
         for (int j = 0; j < G; ++j) {
             m[j] = kNegBig;
             l[j] = 0.f;
             #pragma unroll
-            for (int e = 0; e < E; ++e) o[j][e] = 0.f;
+            for (int e = 0; e < VD; ++e) o[j][e] = 0.f;
         }
     }
 
     __device__ void page(const uint8_t* kbase, const uint8_t* vbase, int warp, int lane, int t_lo, int t_hi,
                          bool partial, float sl2) {
         const int tok0 = warp * 16;
-        const int t = tok0 + (lane & 15), half = lane >> 4;
-        constexpr int kChunks = D / 8;            // 16-byte chunks in half a row
+        const int tl = lane & 15, half = lane >> 4, t = tok0 + tl;
         float acc[G];
         #pragma unroll
         for (int j = 0; j < G; ++j) acc[j] = 0.f;
-        // partial unroll: enough loads in flight without hoisting every query chunk
-        #pragma unroll (G >= 4 ? 2 : 8)
-        for (int c = 0; c < kChunks; ++c) {
+        // full unroll when the query sits in registers (its index must be static)
+        #pragma unroll (G >= 4 ? 2 : D / 8)
+        for (int c = 0; c < D / 8; ++c) {
             const int col = half * (D / 2) + c * 4;          // first dimension of the chunk
-            const int box = col / 32, cin = (col % 32) / 4;
-            const float4 kv = *reinterpret_cast<const float4*>(kbase + swz128(box * 8192, t, cin));
+            const float4 kv = *reinterpret_cast<const float4*>(kbase + swz128((col / 32) * 8192, t, (col % 32) / 4));
             #pragma unroll
             for (int j = 0; j < G; ++j) {
                 if (j < g) {
-                    const float4 qv = *reinterpret_cast<const float4*>(wq + j * D + col);
+                    float4 qv;
+                    if constexpr (kQRegs) qv = make_float4(qr[4 * c], qr[4 * c + 1], qr[4 * c + 2], qr[4 * c + 3]);
+                    else qv = *reinterpret_cast<const float4*>(wq + j * D + col);
                     acc[j] = fmaf(kv.x, qv.x, acc[j]);
                     acc[j] = fmaf(kv.y, qv.y, acc[j]);
                     acc[j] = fmaf(kv.z, qv.z, acc[j]);
@@ -301,44 +323,56 @@ struct Consumer<float, D, G> {
             }
         }
         const bool valid = t >= t_lo && t < t_hi;
-        float p[G];
         #pragma unroll
         for (int j = 0; j < G; ++j) {
             if (j < g) {
-                float s = acc[j] + __shfl_xor_sync(0xffffffffu, acc[j], 16);
-                s = valid ? s * sl2 : -INFINITY;
-                float x = s;
+                float sc = acc[j] + __shfl_xor_sync(0xffffffffu, acc[j], 16);
+                sc = valid ? sc * sl2 : -INFINITY;
+                float x = sc;
                 #pragma unroll
                 for (int sh = 1; sh < 16; sh <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, sh));
                 const float n = fmaxf(m[j], x);
                 const float al = exp2_approx(m[j] - n);
                 m[j] = n;
-                p[j] = exp2_approx(s - n);
-                float ps = p[j];
+                const float pj = exp2_approx(sc - n);
+                float ps = pj;
                 #pragma unroll
                 for (int sh = 1; sh < 16; sh <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, sh);
                 l[j] = l[j] * al + ps;
                 #pragma unroll
-                for (int e = 0; e < E; ++e) o[j][e] *= al;
+                for (int e = 0; e < VD; ++e) o[j][e] *= al;
+                // token tl goes to slot parity * 8 + index within its parity
+                if (half == 0) sp[j * 16 + (tl & 1) * 8 + (tl >> 1)] = pj;
             }
         }
-        const int tt_lo = max(t_lo - tok0, 0), tt_hi = min(t_hi - tok0, 16);
-        #pragma unroll 4
-        for (int tt = tt_lo; tt < tt_hi; ++tt) {
-            float v[E];
+        __syncwarp();
+        const int par = half, dg = tl * VD;
+        #pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int row = tok0 + 2 * k + par;
+            float v[VD];
             #pragma unroll
-            for (int e = 0; e < E; ++e)
-                v[e] = *reinterpret_cast<const float*>(vbase + swz128(e * 8192, tok0 + tt, lane >> 2) + (lane & 3) * 4);
+            for (int q4 = 0; q4 < VD / 4; ++q4) {
+                const int col = dg + 4 * q4;
+                const float4 w4 = *reinterpret_cast<const float4*>(vbase + swz128((col / 32) * 8192, row, (col % 32) / 4));
+                v[4 * q4] = w4.x; v[4 * q4 + 1] = w4.y; v[4 * q4 + 2] = w4.z; v[4 * q4 + 3] = w4.w;
+            }
+            if (partial) {
+                // invisible tokens have p = 0, but their slots may hold NaN
+                const bool vis = row >= t_lo && row < t_hi;
+                #pragma unroll
+                for (int e = 0; e < VD; ++e) v[e] = vis ? v[e] : 0.f;
+            }
             #pragma unroll
             for (int j = 0; j < G; ++j) {
                 if (j < g) {
-                    const float pj = __shfl_sync(0xffffffffu, p[j], tt);
+                    const float pk = sp[j * 16 + par * 8 + k];
                     #pragma unroll
-                    for (int e = 0; e < E; ++e) o[j][e] = fmaf(pj, v[e], o[j][e]);
+                    for (int e = 0; e < VD; ++e) o[j][e] = fmaf(pk, v[e], o[j][e]);
                 }
             }
         }
-        (void)partial;
+        __syncwarp();   // sp is rewritten by the next page
     }
 
     __device__ void stash(float* sm_m, float* sm_l, float* sm_o, int warp, int lane) {
@@ -350,7 +384,10 @@ struct Consumer<float, D, G> {
                     sm_l[warp * kMaxGroup + j] = l[j];
                 }
                 #pragma unroll
-                for (int e = 0; e < E; ++e) sm_o[(warp * kMaxGroup + j) * (D + 4) + e * 32 + lane] = o[j][e];
+                for (int e = 0; e < VD; ++e) {
+                    const float tot = o[j][e] + __shfl_xor_sync(0xffffffffu, o[j][e], 16);
+                    if (lane < 16) sm_o[(warp * kMaxGroup + j) * (D + 4) + lane * VD + e] = tot;
+                }
             }
         }
     }
@@ -420,13 +457,21 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     float* part_o = reinterpret_cast<float*>(a.ws + a.L.part_o);
     const int g = a.group, Hk = a.kv_heads;
 
+    // The scheduler's first item is this CTA's index; its descriptor load is
+    // issued before the plan header is checked (the index is inside the
+    // workspace whatever the plan says) and used only once the check passed.
+    int4 first_d0 = make_int4(0, 0, 0, 0), first_d1 = make_int4(0, 0, 0, 0);
+    if (warp == kSchedulerWarp && (int)blockIdx.x < a.L.max_items) {
+        first_d0 = __ldcg(reinterpret_cast<const int4*>(items + blockIdx.x));
+        first_d1 = __ldcg(reinterpret_cast<const int4*>(items + blockIdx.x) + 1);
+    }
     const uint32_t magic = __ldcg(&ctrl->magic);
     const int n_items = __ldcg(&ctrl->n_items);
     const int chunk_pages = __ldcg(&ctrl->chunk_pages);
     if (magic != kPlanMagic || __ldcg(&ctrl->rows) != a.rows || __ldcg(&ctrl->kv_heads) != Hk ||
         __ldcg(&ctrl->pages_per_row) != a.pages_per_row || __ldcg(&ctrl->max_items) != a.L.max_items ||
         __ldcg(&ctrl->group) != g || __ldcg(&ctrl->head_dim) != D || chunk_pages < 1 ||
-        chunk_pages > kChunkMax || n_items > a.L.max_items) {
+        chunk_pages > kChunkMax || n_items > a.L.max_items || __ldcg(&ctrl->grid) != (int)gridDim.x) {
         if (threadIdx.x == 0) set_error(ctrl, kErrBadPlan);
         return;
     }
@@ -437,17 +482,25 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         int islot = 0;
         uint32_t iphase = 0;
         bool ok = true;
+        bool first = true;
         while (true) {
-            int it = 0;
-            if (lane == 0) it = atomicAdd(&ctrl->next_item, 1);
-            it = __shfl_sync(0xffffffffu, it, 0);
+            int it = (int)blockIdx.x;
+            if (!first) {
+                if (lane == 0) it = atomicAdd(&ctrl->next_item, 1);
+                it = __shfl_sync(0xffffffffu, it, 0);
+            }
             const bool term = it >= n_items;
             int4 d0 = make_int4(0, 0, 0, 0), d1 = make_int4(0, -1, 0, 0);
             int pid0 = -1, pid1 = -1;
             bool good = true;
             if (!term) {
-                d0 = __ldcg(reinterpret_cast<const int4*>(items + it));
-                d1 = __ldcg(reinterpret_cast<const int4*>(items + it) + 1);
+                if (first) {
+                    d0 = first_d0;
+                    d1 = first_d1;
+                } else {
+                    d0 = __ldcg(reinterpret_cast<const int4*>(items + it));
+                    d1 = __ldcg(reinterpret_cast<const int4*>(items + it) + 1);
+                }
                 const int row = d0.x, kvh = d0.y >> 16, chunk = d0.y & 0xffff, nch = d0.z, slot = d0.w;
                 const int first = d1.x, npg = d1.y, pos = d1.z, lo = d1.w;
                 good = row >= 0 && row < a.rows && kvh < Hk && chunk < nch && slot >= 0 && slot < n_items &&
@@ -462,6 +515,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                     set_error(ctrl, kErrBadPlan);
                 }
             }
+            first = false;
             if (!good) continue;
             int waited = 1;
             if (lane == 0) waited = mbar_wait(bar_iempty + 8 * islot, iphase ^ 1) ? 1 : 0;
@@ -486,7 +540,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                 // Last CTA to finish fetching rewinds the cursor for the next launch.
                 __threadfence();
                 if (atomicAdd(&ctrl->done_ctas, 1) == (int)gridDim.x - 1) {
-                    ctrl->next_item = 0;
+                    ctrl->next_item = (int)gridDim.x;
                     ctrl->done_ctas = 0;
                 }
             } else {
@@ -510,20 +564,27 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             if (lane == 0) waited = mbar_wait(bar_ifull + 8 * islot, iphase) ? 1 : 0;
             waited = __shfl_sync(0xffffffffu, waited, 0);
             if (!waited) { ok = false; break; }
+            // Take the item into registers (page ids: two per lane) and free the
+            // slot at once, so the scheduler reserves the next item now and
+            // never more than one ahead.
             const uint8_t* slotp = item_q + islot * C::kItemBytes;
             const int4 d0 = reinterpret_cast<const int4*>(slotp)[0];
             const int4 d1 = reinterpret_cast<const int4*>(slotp)[1];
             const int* pids = reinterpret_cast<const int*>(slotp + sizeof(ItemDesc));
+            const int my_pid0 = pids[lane], my_pid1 = pids[lane + 32];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_iempty + 8 * islot);
+            if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
             const int npg = d1.y;
             if (npg < 0) break;             // end of the work
             const int row = d0.x, kvh = d0.y >> 16, chunk = d0.y & 0xffff, nch = d0.z, slot = d0.w;
             const int first_page = d1.x, pos = d1.z, lo = d1.w;
             for (int j = 0; j < npg; ++j) {
+                const int pid = __shfl_sync(0xffffffffu, j < 32 ? my_pid0 : my_pid1, j & 31);
                 if (lane == 0) waited = mbar_wait(bar_empty + 8 * stage, phase ^ 1) ? 1 : 0;
                 waited = __shfl_sync(0xffffffffu, waited, 0);
                 if (!waited) { ok = false; break; }
                 if (lane == 0) {
-                    const int pid = pids[j];
                     const bool pvalid = pid >= 0 && pid < a.num_pages;
                     if (!pvalid) set_error(ctrl, kErrBadPage);
                     const int p = first_page + j, t0 = p * kPageSize;
@@ -561,9 +622,6 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                 if (++stage == S) { stage = 0; phase ^= 1; }
             }
             if (!ok) break;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_iempty + 8 * islot);
-            if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
         }
         if (ok) {
             // Terminator: the next stage carries no data, only the end flag.
@@ -690,7 +748,8 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                 cs.begin(sbase + C::kOffQ + stage * C::kQBytes, lane);
             else
                 cs.begin(reinterpret_cast<const float*>(smem + C::kOffQ + stage * C::kQBytes),
-                         reinterpret_cast<float*>(smem + C::kOffWarpQ + warp * C::kQBytes), lane, g);
+                         reinterpret_cast<float*>(smem + C::kOffWarpQ + warp * C::kQBytes),
+                         reinterpret_cast<float*>(smem + C::kOffWarpP + warp * kMaxGroup * 16 * 4), lane, g);
         }
         if (mt.flags & kValid) {
             if constexpr (sizeof(T) == 2)

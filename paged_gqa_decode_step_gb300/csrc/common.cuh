@@ -26,13 +26,14 @@ constexpr int kErrBadPlan = 8;
 // Control block at the start of the workspace (256 bytes).
 struct Ctrl {
     int status;        // OR of kErr* bits; cleared by pdattn_check_status
-    int next_item;     // persistent-scheduler cursor
+    int next_item;     // persistent-scheduler cursor (starts at `grid`)
     int done_ctas;     // CTAs that finished fetching work
     int n_items;       // work items in the plan
     int chunk_pages;   // pages per split chosen by the plan
     uint32_t magic;    // kPlanMagic once a plan is written
     int rows, kv_heads, pages_per_row, max_items, group, head_dim;
-    int pad[52];
+    int grid;          // persistent CTAs of the attention launch: CTA b starts with item b
+    int pad[51];
 };
 static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
 

@@ -276,7 +276,8 @@ __device__ void build_plan(const PrepArgs& a) {
         if (!fits) set_error(ctrl, kErrBadPlan);
         ctrl->n_items = fits ? n_items : 0;
         ctrl->chunk_pages = C;
-        ctrl->next_item = 0;
+        ctrl->grid = a.grid_attend;
+        ctrl->next_item = a.grid_attend;   // CTA b takes item b first without an atomic
         ctrl->done_ctas = 0;
         ctrl->rows = R;
         ctrl->kv_heads = Hk;
