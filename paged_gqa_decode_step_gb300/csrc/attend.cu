@@ -38,7 +38,8 @@ constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kSchedulerWarp = kConsumerWarps + 1;
 constexpr int kEpilogueWarp = kConsumerWarps + 2;
 constexpr int kThreads = (kConsumerWarps + 3) * 32;
-constexpr int kItemSlots = 1;           // items the scheduler may hold ahead of the producer
+constexpr int kItemSlots = 4;           // items the scheduler may hold ahead of the producer
+constexpr int kBacklogBytes = 256 << 10;  // K/V bytes queued ahead of the TMA issue point
 constexpr int kEpiSlots = 2;            // finished items waiting for the epilogue warp
 constexpr float kNegBig = -1.0e30f;     // running-max start: finite, so exp2(m - m) = 1
 
@@ -76,6 +77,8 @@ struct Cfg {
     static constexpr int kNumBars = 2 * kStages + 1 + 2 * kItemSlots + 2 * kEpiSlots;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffMisc + 16 + 1024;           // + alignment slack
+    // pages the scheduler keeps queued beyond the producer's issue point
+    static constexpr int kBacklogPages = kBacklogBytes / kStageBytes > 2 ? kBacklogBytes / kStageBytes : 2;
     static_assert(kSmem <= 232448, "shared memory per CTA");
     static_assert(kOffBar % 8 == 0, "mbarrier alignment");
 };
@@ -417,6 +420,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     float* sm_l = sm_m + kConsumerWarps * kMaxGroup;
     float* sm_o = sm_l + kConsumerWarps * kMaxGroup;
     int* s_flag = reinterpret_cast<int*>(smem + C::kOffMisc);
+    volatile int* s_issued = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);  // pages issued so far
     uint8_t* item_q = smem + C::kOffItems;
     uint8_t* epi_q = smem + C::kOffEpi;
 
@@ -427,6 +431,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             mbar_init(bar_empty + 8 * s, kConsumerWarps);
         }
         mbar_init(bar_sync, kConsumerWarps * 32);
+        *s_issued = 0;
         for (int s = 0; s < kItemSlots; ++s) {
             mbar_init(bar_ifull + 8 * s, 1);
             mbar_init(bar_iempty + 8 * s, 1);
@@ -483,9 +488,22 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         uint32_t iphase = 0;
         bool ok = true;
         bool first = true;
+        int queued = 0;                     // pages handed to the producer so far
         while (true) {
             int it = (int)blockIdx.x;
             if (!first) {
+                // Reserve the next item only when fewer than kBacklogPages
+                // queued pages wait to be issued: short items pipeline, long
+                // ones do not hold back work other CTAs could take.
+                if (lane == 0) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (queued - *s_issued >= C::kBacklogPages) {
+                        __nanosleep(32);
+                        if (globaltimer_ns() - t0 > 2000000000ull) { ok = false; break; }
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
                 if (lane == 0) it = atomicAdd(&ctrl->next_item, 1);
                 it = __shfl_sync(0xffffffffu, it, 0);
             }
@@ -534,6 +552,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             if (lane == 0) mbar_arrive(bar_ifull + 8 * islot);
             if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
             if (term) break;
+            queued += d1.y;
         }
         if (lane == 0) {
             if (ok) {
@@ -564,9 +583,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             if (lane == 0) waited = mbar_wait(bar_ifull + 8 * islot, iphase) ? 1 : 0;
             waited = __shfl_sync(0xffffffffu, waited, 0);
             if (!waited) { ok = false; break; }
-            // Take the item into registers (page ids: two per lane) and free the
-            // slot at once, so the scheduler reserves the next item now and
-            // never more than one ahead.
+            // Take the item into registers (page ids: two per lane) and free the slot.
             const uint8_t* slotp = item_q + islot * C::kItemBytes;
             const int4 d0 = reinterpret_cast<const int4*>(slotp)[0];
             const int4 d1 = reinterpret_cast<const int4*>(slotp)[1];
@@ -617,6 +634,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                     }
                     armed |= 1u << stage;
                     armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+                    *s_issued = *s_issued + 1;
                 }
                 __syncwarp();
                 if (++stage == S) { stage = 0; phase ^= 1; }
