@@ -43,11 +43,17 @@ constexpr int kBacklogBytes = 256 << 10;  // K/V bytes queued ahead of the TMA i
 constexpr int kEpiSlots = 2;            // finished items waiting for the epilogue warp
 constexpr float kNegBig = -1.0e30f;     // running-max start: finite, so exp2(m - m) = 1
 
-enum : int { kFirst = 1, kLast = 2, kValid = 4, kTerm = 8, kPartial = 16 };
+enum : int { kFirst = 1, kLast = 2, kTerm = 8 };
 
+// Per-stage meta.  t_lo / t_hi: visible token range in stage coordinates
+// (page p of the stage holds tokens [64 p, 64 p + 64)); flags: kFirst /
+// kLast / kTerm, the number of pages in bits 8-11 and a valid bit per page
+// from bit 16.
 struct Meta {
     int row, kvh, nch, slot, t_lo, t_hi, flags, chunk;
 };
+constexpr int kPagesShift = 8;
+constexpr int kValidShift = 16;
 
 template <typename T, int D>
 struct Cfg {
@@ -56,7 +62,10 @@ struct Cfg {
     static constexpr int kBoxes = D / kBoxCols;                  // boxes per K (or V) page
     static constexpr int kBoxBytes = kPageSize * 128;            // 8 KiB
     static constexpr int kTileBytes = kBoxes * kBoxBytes;        // one page of K (or V)
-    static constexpr int kStageBytes = 2 * kTileBytes;
+    // Small pages travel two to a stage, so the producer's per-stage work
+    // (barrier, meta, arm) is spread over 32 KiB like the larger pages.
+    static constexpr int kPagesPerStage = (kTileBytes == kBoxBytes && kElem == 2) ? 2 : 1;
+    static constexpr int kStageBytes = 2 * kPagesPerStage * kTileBytes;   // K pages, then V pages
     static constexpr int kStages = (kStageBytes <= 16384) ? 10 : (kStageBytes <= 32768 ? 5 : 2);
     static constexpr int kQBytes = kMaxGroup * D * kElem;
     static constexpr int kORow = D + 4;                          // padded row of the merge buffer
@@ -571,93 +580,96 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
 
     if (warp == kProducerWarp) {
         // ================= producer =================
-        int stage = 0;
-        uint32_t phase = 0;
-        int islot = 0;
-        uint32_t iphase = 0;
-        uint32_t armed = 0;                 // bit s: stage s has an unfinished arm
-        uint32_t armed_par = 0;             // parity armed on stage s
-        bool ok = true;
-        while (ok) {
-            int waited = 1;
-            if (lane == 0) waited = mbar_wait(bar_ifull + 8 * islot, iphase) ? 1 : 0;
-            waited = __shfl_sync(0xffffffffu, waited, 0);
-            if (!waited) { ok = false; break; }
-            // Take the item into registers (page ids: two per lane) and free the slot.
-            const uint8_t* slotp = item_q + islot * C::kItemBytes;
-            const int4 d0 = reinterpret_cast<const int4*>(slotp)[0];
-            const int4 d1 = reinterpret_cast<const int4*>(slotp)[1];
-            const int* pids = reinterpret_cast<const int*>(slotp + sizeof(ItemDesc));
-            const int my_pid0 = pids[lane], my_pid1 = pids[lane + 32];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_iempty + 8 * islot);
-            if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
-            const int npg = d1.y;
-            if (npg < 0) break;             // end of the work
-            const int row = d0.x, kvh = d0.y >> 16, chunk = d0.y & 0xffff, nch = d0.z, slot = d0.w;
-            const int first_page = d1.x, pos = d1.z, lo = d1.w;
-            for (int j = 0; j < npg; ++j) {
-                const int pid = __shfl_sync(0xffffffffu, j < 32 ? my_pid0 : my_pid1, j & 31);
-                if (lane == 0) waited = mbar_wait(bar_empty + 8 * stage, phase ^ 1) ? 1 : 0;
-                waited = __shfl_sync(0xffffffffu, waited, 0);
-                if (!waited) { ok = false; break; }
-                if (lane == 0) {
-                    const bool pvalid = pid >= 0 && pid < a.num_pages;
-                    if (!pvalid) set_error(ctrl, kErrBadPage);
-                    const int p = first_page + j, t0 = p * kPageSize;
-                    Meta mt;
-                    mt.row = row;
-                    mt.kvh = kvh;
-                    mt.nch = nch;
-                    mt.slot = slot;
-                    mt.t_lo = max(lo, t0) - t0;
-                    mt.t_hi = min(pos, t0 + kPageSize - 1) - t0 + 1;
-                    mt.flags = (j == 0 ? kFirst : 0) | (j == npg - 1 ? kLast : 0) | (pvalid ? kValid : 0) |
-                               ((mt.t_lo > 0 || mt.t_hi < kPageSize) ? kPartial : 0);
-                    mt.chunk = chunk;
-                    meta[stage] = mt;
-                    const uint32_t bytes = (pvalid ? C::kStageBytes : 0) + (j == 0 ? g * D * C::kElem : 0);
+        // One lane runs the page loop: per page it waits for a free stage,
+        // writes the stage's meta, arms the full barrier and issues the TMA
+        // copies.  No warp-wide collectives sit in the loop.
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int islot = 0;
+            uint32_t iphase = 0;
+            uint32_t armed = 0;                 // bit s: stage s has an unfinished arm
+            uint32_t armed_par = 0;             // parity armed on stage s
+            int issued = 0;
+            bool ok = true;
+            while (ok) {
+                if (!mbar_wait(bar_ifull + 8 * islot, iphase)) { ok = false; break; }
+                const uint8_t* slotp = item_q + islot * C::kItemBytes;
+                const int4 d0 = reinterpret_cast<const int4*>(slotp)[0];
+                const int4 d1 = reinterpret_cast<const int4*>(slotp)[1];
+                const int* pids = reinterpret_cast<const int*>(slotp + sizeof(ItemDesc));
+                const int npg = d1.y;
+                if (npg < 0) break;             // end of the work
+                const int row = d0.x, kvh = d0.y >> 16, chunk = d0.y & 0xffff, nch = d0.z, slot = d0.w;
+                const int first_page = d1.x, pos = d1.z, lo = d1.w;
+                const int y_kv = kvh * kPageSize;
+                const T* qsrc = static_cast<const T*>(a.q) + ((size_t)row * a.heads + kvh * g) * D;
+                constexpr int P = C::kPagesPerStage;
+                for (int j = 0; j < npg; j += P) {
+                    const int np = min(P, npg - j);
+                    if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1)) { ok = false; break; }
+                    const int t0 = (first_page + j) * kPageSize;
+                    const int t_lo = max(lo, t0) - t0;
+                    const int t_hi = min(pos, t0 + np * kPageSize - 1) - t0 + 1;
+                    int flags = (j == 0 ? kFirst : 0) | (j + np == npg ? kLast : 0) | (np << kPagesShift);
+                    uint32_t bytes = (j == 0 ? g * D * C::kElem : 0);
                     const uint32_t fb = bar_full + 8 * stage;
-                    mbar_arrive_expect_tx(fb, bytes);
                     const uint32_t dst = sbase + stage * C::kStageBytes;
-                    if (pvalid) {
-                        const int y = (pid * Hk + kvh) * kPageSize;
-                        #pragma unroll
-                        for (int b = 0; b < C::kBoxes; ++b) {
-                            tma_load_2d(dst + b * C::kBoxBytes, &k_map, b * C::kBoxCols, y, fb);
-                            tma_load_2d(dst + C::kTileBytes + b * C::kBoxBytes, &v_map, b * C::kBoxCols, y, fb);
+                    int pidv[P];
+                    #pragma unroll
+                    for (int p = 0; p < P; ++p) {
+                        pidv[p] = p < np ? pids[j + p] : -1;
+                        if (p < np && pidv[p] >= 0 && pidv[p] < a.num_pages) {
+                            flags |= 1 << (kValidShift + p);
+                            bytes += 2 * C::kTileBytes;
+                        } else if (p < np) {
+                            set_error(ctrl, kErrBadPage);
                         }
                     }
-                    if (j == 0) {
-                        const T* qsrc = static_cast<const T*>(a.q) + ((size_t)row * a.heads + kvh * g) * D;
-                        bulk_load(sbase + C::kOffQ + stage * C::kQBytes, qsrc, g * D * C::kElem, fb);
+                    int4* mp = reinterpret_cast<int4*>(meta + stage);
+                    mp[0] = make_int4(row, kvh, nch, slot);
+                    mp[1] = make_int4(t_lo, t_hi, flags, chunk);
+                    mbar_arrive_expect_tx(fb, bytes);
+                    #pragma unroll
+                    for (int p = 0; p < P; ++p) {
+                        if (flags & (1 << (kValidShift + p))) {
+                            const int y = pidv[p] * Hk * kPageSize + y_kv;
+                            #pragma unroll
+                            for (int bx = 0; bx < C::kBoxes; ++bx) {
+                                tma_load_2d(dst + p * C::kTileBytes + bx * C::kBoxBytes, &k_map, bx * C::kBoxCols, y, fb);
+                                tma_load_2d(dst + (P + p) * C::kTileBytes + bx * C::kBoxBytes, &v_map, bx * C::kBoxCols, y,
+                                            fb);
+                            }
+                        }
                     }
+                    if (j == 0) bulk_load(sbase + C::kOffQ + stage * C::kQBytes, qsrc, g * D * C::kElem, fb);
                     armed |= 1u << stage;
                     armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-                    *s_issued = *s_issued + 1;
+                    issued += np;
+                    *s_issued = issued;
+                    if (++stage == S) { stage = 0; phase ^= 1; }
                 }
-                __syncwarp();
-                if (++stage == S) { stage = 0; phase ^= 1; }
+                if (!ok) break;
+                mbar_arrive(bar_iempty + 8 * islot);
+                if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
             }
-            if (!ok) break;
-        }
-        if (ok) {
-            // Terminator: the next stage carries no data, only the end flag.
-            int waited = 1;
-            if (lane == 0) waited = mbar_wait(bar_empty + 8 * stage, phase ^ 1) ? 1 : 0;
-            waited = __shfl_sync(0xffffffffu, waited, 0);
-            if (waited && lane == 0) {
-                meta[stage].flags = kTerm;
-                mbar_arrive(bar_full + 8 * stage);
+            if (ok) {
+                // Terminator: the next stage carries no data, only the end flag.
+                if (mbar_wait(bar_empty + 8 * stage, phase ^ 1)) {
+                    meta[stage].flags = kTerm;
+                    mbar_arrive(bar_full + 8 * stage);
+                } else {
+                    ok = false;
+                }
             }
-            ok = waited != 0;
+            if (!ok) {
+                set_error(ctrl, kErrTimeout);
+                // Let copies in flight land before the CTA's shared memory goes away.
+                for (int s2 = 0; s2 < S; ++s2)
+                    if (armed & (1u << s2)) mbar_wait(bar_full + 8 * s2, (armed_par >> s2) & 1u, 200000000ull);
+            }
         }
-        if (!ok && lane == 0) {
-            set_error(ctrl, kErrTimeout);
-            // Let copies in flight land before the CTA's shared memory goes away.
-            for (int s = 0; s < S; ++s)
-                if (armed & (1u << s)) mbar_wait(bar_full + 8 * s, (armed_par >> s) & 1u, 200000000ull);
-        }
+        __syncwarp();
         return;
     }
 
@@ -769,13 +781,23 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                          reinterpret_cast<float*>(smem + C::kOffWarpQ + warp * C::kQBytes),
                          reinterpret_cast<float*>(smem + C::kOffWarpP + warp * kMaxGroup * 16 * 4), lane, g);
         }
-        if (mt.flags & kValid) {
-            if constexpr (sizeof(T) == 2)
-                cs.page(kbase, kbase + C::kTileBytes, warp, lane, mt.t_lo, mt.t_hi, (mt.flags & kPartial) != 0,
-                        a.scale_log2);
-            else
-                cs.page(smem + stage * C::kStageBytes, smem + stage * C::kStageBytes + C::kTileBytes, warp, lane,
-                        mt.t_lo, mt.t_hi, (mt.flags & kPartial) != 0, a.scale_log2);
+        {
+            constexpr int P = C::kPagesPerStage;
+            const int np = (mt.flags >> kPagesShift) & 15;
+            #pragma unroll
+            for (int p = 0; p < P; ++p) {
+                if (p < np && (mt.flags & (1 << (kValidShift + p)))) {
+                    const int lo_p = mt.t_lo - p * kPageSize, hi_p = mt.t_hi - p * kPageSize;
+                    const bool partial = lo_p > 0 || hi_p < kPageSize;
+                    if constexpr (sizeof(T) == 2)
+                        cs.page(kbase + p * C::kTileBytes, kbase + (P + p) * C::kTileBytes, warp, lane, lo_p, hi_p,
+                                partial, a.scale_log2);
+                    else
+                        cs.page(smem + stage * C::kStageBytes + p * C::kTileBytes,
+                                smem + stage * C::kStageBytes + (P + p) * C::kTileBytes, warp, lane, lo_p, hi_p, partial,
+                                a.scale_log2);
+                }
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * stage);

@@ -134,10 +134,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking check of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete; gives up after
 // `timeout_ns` and returns false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           uint64_t timeout_ns = 2000000000ull) {
+    if (mbar_test_wait(bar, parity)) return true;
     #pragma unroll 1
     for (int i = 0; i < 256; ++i)
         if (mbar_try_wait(bar, parity)) return true;
