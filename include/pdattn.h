@@ -76,6 +76,9 @@ typedef struct {
     const void* rope_sin;   /* both NULL or both set */
     int32_t rope_len;       /* rows of the rope tables; positions must be below it */
     int32_t chunk_pages;    /* 0: the planner picks pages per split; else fixed */
+    const void* sinks;      /* NULL, or [heads] of T: one attention-sink logit per query head
+                               (gpt-oss-20b page, SinkAttention `param sinks`), read as an
+                               extra softmax logit that carries no value */
 } pdattn_params;
 
 /*
@@ -128,7 +131,8 @@ pdattn_status pdattn_plan(const pdattn_params* p, const int32_t* positions, void
  * rsqrt(f32(D)), seen)`), following the plan last made in this workspace
  * for the same positions: out[r, h] = sum_t softmax_t(scale * q[r, h] .
  * K[t, h / g]) V[t, h / g] over t in [lo, pos], fp32 online softmax,
- * split chunks merged on the device, result rounded to T.
+ * split chunks merged on the device, result rounded to T.  With sinks,
+ * the softmax denominator also holds exp(sinks[h]) (the sink is not scaled).
  */
 pdattn_status pdattn_attend(const pdattn_params* p, const void* q_rot, const int32_t* positions,
                             const int32_t* table, const void* k_pool, const void* v_pool,

@@ -14,7 +14,9 @@ Functions and the passages they follow (page title, section):
                   (``decode_paged`` signature, ``PageSize = 64``)
   decode          Llama example page, ``src/attention.linnet`` (``decode``:
                   ``seen[s] = s <= pos``, ``rsqrt(f32(head dim))``,
-                  ``grouped_attention``), window from the gpt-oss-20b page
+                  ``grouped_attention``), window from the gpt-oss-20b page;
+                  optional attention sinks (gpt-oss-20b page, SinkAttention
+                  ``param sinks``) as one value-less logit per query head
   step            rope_write_kv followed by decode
 
 Every function is pinned by tests under ``tests/test_oracle_*.py`` against
@@ -54,10 +56,12 @@ def lib():
         L.oracle_rope_tables.argtypes = [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp]
         L.oracle_rope_write_kv.argtypes = [ctypes.POINTER(Shape)] + [vp] * 8
         L.oracle_decode.argtypes = [ctypes.POINTER(Shape)] + [vp] * 7
+        L.oracle_decode_sinks.argtypes = [ctypes.POINTER(Shape)] + [vp] * 8
         L.oracle_step.argtypes = [ctypes.POINTER(Shape)] + [vp] * 10
         L.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
         L.oracle_f32_to_bf16.restype = ctypes.c_uint16
-        for f in (L.oracle_rope_tables, L.oracle_rope_write_kv, L.oracle_decode, L.oracle_step):
+        for f in (L.oracle_rope_tables, L.oracle_rope_write_kv, L.oracle_decode, L.oracle_decode_sinks,
+                  L.oracle_step):
             f.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -100,12 +104,12 @@ def rope_write_kv(shape, q, k_new, v_new, positions, table, k_pool, v_pool):
     return q_out, rc
 
 
-def decode(shape, q_rot, positions, table, k_pool, v_pool):
-    """Returns (out in T, out in float64, status)."""
+def decode(shape, q_rot, positions, table, k_pool, v_pool, sinks=None):
+    """Returns (out in T, out in float64, status).  sinks: [Hq] of T or None."""
     out = np.zeros(q_rot.shape, dtype=q_rot.dtype)
     out64 = np.zeros(q_rot.shape, dtype=np.float64)
-    rc = lib().oracle_decode(ctypes.byref(shape), _ptr(q_rot), _ptr(positions), _ptr(table),
-                             _ptr(k_pool), _ptr(v_pool), _ptr(out), _ptr(out64))
+    rc = lib().oracle_decode_sinks(ctypes.byref(shape), _ptr(q_rot), _ptr(positions), _ptr(table),
+                                   _ptr(k_pool), _ptr(v_pool), _ptr(sinks), _ptr(out), _ptr(out64))
     return out, out64, rc
 
 

@@ -19,12 +19,15 @@
  *                        (`decode_paged`, `table: Tensor[Rows, Pages; i32]`)
  *                        and the `PageSize: Dim = 64` generic of
  *                        GroupedQueryAttention.
- *   oracle_decode        Llama example page, "src/attention.linnet"
+ *   oracle_decode(_sinks) Llama example page, "src/attention.linnet"
  *                        (`decode`): mask seen[s] = s <= pos, scale
  *                        rsqrt(f32(head dim)), grouped attention where query
  *                        head h reads kv head h / (Heads / KvHeads) ("Key
  *                        ideas", grouped-query attention); sliding window from
- *                        the gpt-oss-20b architecture page (`window: i32`).
+ *                        the gpt-oss-20b architecture page (`window: i32`);
+ *                        attention sinks from the same page (SinkAttention
+ *                        `param sinks`), read as one extra value-less logit
+ *                        per query head in the softmax.
  *
  * Readings where the pages leave a step open:
  *   - rope(x, cos, sin) = x * cos + rotate_half(x) * sin with
@@ -202,11 +205,15 @@ int oracle_rope_write_kv(const oracle_shape* p, const void* q, const void* k_new
 /*
  * Attention of the rotated queries q_rot [R, Hq, D] over the cached positions
  * of each row.  out [R, Hq, D] is rounded to T; out64 (may be NULL) receives
- * the unrounded double result.
+ * the unrounded double result.  sinks (may be NULL) holds one logit per
+ * query head [Hq] of T (gpt-oss-20b architecture page, SinkAttention
+ * `param sinks: Tensor[Heads; T]`); its reading: the sink joins the softmax
+ * as one more logit that carries no value, so it only enlarges the
+ * denominator.
  */
-int oracle_decode(const oracle_shape* p, const void* q_rot, const int32_t* positions,
-                  const int32_t* table, const void* k_pool, const void* v_pool, void* out,
-                  double* out64) {
+int oracle_decode_sinks(const oracle_shape* p, const void* q_rot, const int32_t* positions,
+                        const int32_t* table, const void* k_pool, const void* v_pool,
+                        const void* sinks, void* out, double* out64) {
     if (!shape_ok(p)) return ORACLE_EINVAL;
     const int D = p->head_dim, Hq = p->heads, Hk = p->kv_heads, PS = p->page_size;
     const int group = Hq / Hk;
@@ -231,6 +238,7 @@ int oracle_decode(const oracle_shape* p, const void* q_rot, const int32_t* posit
             int kvh = h / group;
             size_t qo = ((size_t)r * Hq + h) * D;
             double m = -INFINITY;
+            const double sink = sinks ? (double)load_t(sinks, (size_t)h, p->dtype) : -INFINITY;
             for (int t = lo; t <= pos; ++t) {
                 int page = table[(size_t)r * p->pages_per_row + t / PS];
                 size_t ko = pool_index(p, page, kvh, t % PS, 0);
@@ -240,7 +248,8 @@ int oracle_decode(const oracle_shape* p, const void* q_rot, const int32_t* posit
                 scores[t - lo] = scale * dot;
                 if (scores[t - lo] > m) m = scores[t - lo];
             }
-            double l = 0.0;
+            if (sink > m) m = sink;
+            double l = sinks ? exp(sink - m) : 0.0;
             for (int t = lo; t <= pos; ++t) {
                 scores[t - lo] = exp(scores[t - lo] - m);
                 l += scores[t - lo];
@@ -261,6 +270,12 @@ int oracle_decode(const oracle_shape* p, const void* q_rot, const int32_t* posit
     free(scores);
     free(acc);
     return status;
+}
+
+int oracle_decode(const oracle_shape* p, const void* q_rot, const int32_t* positions,
+                  const int32_t* table, const void* k_pool, const void* v_pool, void* out,
+                  double* out64) {
+    return oracle_decode_sinks(p, q_rot, positions, table, k_pool, v_pool, NULL, out, out64);
 }
 
 /*

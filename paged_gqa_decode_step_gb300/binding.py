@@ -32,6 +32,7 @@ class Params(ctypes.Structure):
         ("pages_per_row", ctypes.c_int32), ("num_pages", ctypes.c_int32), ("dtype", ctypes.c_int32),
         ("window", ctypes.c_int32), ("scale", ctypes.c_float), ("rope_cos", ctypes.c_void_p),
         ("rope_sin", ctypes.c_void_p), ("rope_len", ctypes.c_int32), ("chunk_pages", ctypes.c_int32),
+        ("sinks", ctypes.c_void_p),
     ]
 
 
@@ -78,10 +79,15 @@ def _stream(stream=None):
 
 
 def make_params(rows, heads, kv_heads, head_dim, pages_per_row, num_pages, dtype, window=0, scale=0.0,
-                rope_cos=None, rope_sin=None, chunk_pages=0):
-    """Parameter block; rope tables (torch tensors [len, D]) keep rotation on."""
+                rope_cos=None, rope_sin=None, chunk_pages=0, sinks=None):
+    """Parameter block; rope tables (torch tensors [len, D]) keep rotation on;
+    sinks: optional [heads] tensor of the element type (attention sinks)."""
     p = Params(rows, heads, kv_heads, head_dim, 64, pages_per_row, num_pages, _DTYPES[dtype], window,
-               scale, None, None, 0, chunk_pages)
+               scale, None, None, 0, chunk_pages, None)
+    if sinks is not None:
+        _expect("sinks", sinks, (heads,), dtype)
+        p.sinks = sinks.data_ptr()
+        p._sinks = sinks
     if rope_cos is not None:
         for name, t in (("rope_cos", rope_cos), ("rope_sin", rope_sin)):
             _expect(name, t, (rope_cos.shape[0], head_dim), dtype)

@@ -170,6 +170,7 @@ pdattn_status attend_impl(const pdattn_params* p, const void* q_rot, const int32
     a.scale_log2 = scale_log2(p);
     a.q = q_rot;
     a.table = table;
+    a.sinks = p->sinks;
     a.out = out;
     a.ws = ws;
     a.L = L;

@@ -106,6 +106,28 @@ struct ConsumerSync {
 };
 
 template <typename T>
+__device__ __forceinline__ float load_f32(const void* base, int i);
+template <>
+__device__ __forceinline__ float load_f32<__nv_bfloat16>(const void* base, int i) {
+    return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[i]);
+}
+template <>
+__device__ __forceinline__ float load_f32<float>(const void* base, int i) {
+    return static_cast<const float*>(base)[i];
+}
+
+// Final normalisation of one head's (M, L, O) (base-2 logits): with a sink
+// logit s (natural units) the softmax denominator gains e^s, i.e. with
+// M' = max(M, s log2 e): O e^(M - M') / (L e^(M - M') + e^(s log2 e - M')).
+// Returns the factor to multiply O with.
+__device__ __forceinline__ float out_scale(float M, float L, bool has_sink, float sink_log2) {
+    if (!has_sink) return 1.f / L;
+    const float Mp = fmaxf(M, sink_log2);
+    const float f = exp2_approx(M - Mp);
+    return f / (L * f + exp2_approx(sink_log2 - Mp));
+}
+
+template <typename T>
 __device__ __forceinline__ void store8(T* dst, const float (&v)[8]);
 template <>
 __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* dst, const float (&v)[8]) {
@@ -692,10 +714,12 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             const float* eo = reinterpret_cast<const float*>(ep + sizeof(Meta) + kMaxGroup * 8);
             const int row = mt.row, kvh = mt.kvh, nch = mt.nch, slot = mt.slot;
             T* out_base = static_cast<T*>(a.out) + ((size_t)row * a.heads + kvh * g) * D;
+            const bool has_sink = a.sinks != nullptr;
             if (nch == 1) {
                 for (int u = lane; u < g * D / 8; u += 32) {
                     const int j = u / (D / 8), d0 = (u % (D / 8)) * 8;
-                    const float inv = 1.f / eml[j].y;
+                    const float sk = has_sink ? load_f32<T>(a.sinks, kvh * g + j) * 1.4426950408889634f : 0.f;
+                    const float inv = out_scale(eml[j].x, eml[j].y, has_sink, sk);
                     float O[8];
                     #pragma unroll
                     for (int e = 0; e < 8; ++e) O[e] = eo[j * D + d0 + e] * inv;
@@ -741,7 +765,8 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                             O[0] += f * p0.x; O[1] += f * p0.y; O[2] += f * p0.z; O[3] += f * p0.w;
                             O[4] += f * p1.x; O[5] += f * p1.y; O[6] += f * p1.z; O[7] += f * p1.w;
                         }
-                        const float inv = 1.f / L;
+                        const float sk = has_sink ? load_f32<T>(a.sinks, kvh * g + j) * 1.4426950408889634f : 0.f;
+                        const float inv = out_scale(M, L, has_sink, sk);
                         #pragma unroll
                         for (int e = 0; e < 8; ++e) O[e] *= inv;
                         store8<T>(out_base + j * D + d0, O);

@@ -30,6 +30,7 @@ struct AttendArgs {
     float scale_log2;       // score scale times log2(e)
     const void* q;          // rotated queries [rows, heads, D]
     const int* table;
+    const void* sinks;      // nullptr, or [heads] of T
     void* out;
     char* ws;
     WsLayout L;

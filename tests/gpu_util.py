@@ -22,11 +22,11 @@ def oracle_shape(w, num_pages, rows=None):
                              window=w.window, rope_theta=w.rope_theta)
 
 
-def gpu_params(b, w, num_pages, tables, chunk_pages=0, rows=None):
+def gpu_params(b, w, num_pages, tables, chunk_pages=0, rows=None, sinks=None):
     cos, sin = tables if tables is not None else (None, None)
     return b.make_params(rows if rows is not None else w.rows, w.heads, w.kv_heads, w.head_dim,
                          w.pages_per_row, num_pages, w.torch_dtype, window=w.window, rope_cos=cos,
-                         rope_sin=sin, chunk_pages=chunk_pages)
+                         rope_sin=sin, chunk_pages=chunk_pages, sinks=sinks)
 
 
 def rope_tables_for(b, w):
@@ -51,19 +51,28 @@ def assert_close(got_t, want64, dtype, what=""):
     return err.max(), err.mean()
 
 
-def run_step(w, poison=False, chunk_pages=0, mode="fused", seed=None):
-    """One step on the GPU and in the oracle; returns the comparison data."""
+def run_step(w, poison=False, chunk_pages=0, mode="fused", seed=None, sinks=None):
+    """One step on the GPU and in the oracle; returns the comparison data.
+    sinks: None, or a list of per-head sink logits (rounded to the element type)."""
     b = binding()
     t = wl.generate(w, "cpu", poison=poison, seed=seed)
     a = {k: wl.to_numpy(v) for k, v in t.items()}
     num_pages = a["k_pool"].shape[0]
     kp, vp = a["k_pool"].copy(), a["v_pool"].copy()
-    q_rot, _, out64, rc = oracle.step(oracle_shape(w, num_pages), a["q"], a["k_new"], a["v_new"],
-                                      a["positions"], a["table"], kp, vp)
-    assert rc == 0
+    shape = oracle_shape(w, num_pages)
+    sink_t = None
+    if sinks is None:
+        q_rot, _, out64, rc = oracle.step(shape, a["q"], a["k_new"], a["v_new"], a["positions"], a["table"], kp, vp)
+        assert rc == 0
+    else:
+        sink_t = torch.tensor(sinks, dtype=torch.float32).to(w.torch_dtype)
+        q_rot, rc = oracle.rope_write_kv(shape, a["q"], a["k_new"], a["v_new"], a["positions"], a["table"], kp, vp)
+        assert rc == 0
+        _, out64, rc = oracle.decode(shape, q_rot, a["positions"], a["table"], kp, vp, wl.to_numpy(sink_t))
+        assert rc == 0
     d = {k: v.cuda() for k, v in t.items()}
     tables = rope_tables_for(b, w)
-    p = gpu_params(b, w, num_pages, tables, chunk_pages)
+    p = gpu_params(b, w, num_pages, tables, chunk_pages, sinks=None if sink_t is None else sink_t.cuda())
     ws = b.new_workspace(p)
     out = torch.empty_like(d["q"])
     if mode == "fused":

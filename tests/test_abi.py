@@ -59,9 +59,10 @@ def test_params_struct_layout_matches_header(lib):
 #include <stdio.h>
 #include "pdattn.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu\n", sizeof(pdattn_params), offsetof(pdattn_params, scale),
+  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(pdattn_params), offsetof(pdattn_params, scale),
          offsetof(pdattn_params, rope_cos), offsetof(pdattn_params, rope_sin),
-         offsetof(pdattn_params, rope_len), offsetof(pdattn_params, chunk_pages));
+         offsetof(pdattn_params, rope_len), offsetof(pdattn_params, chunk_pages),
+         offsetof(pdattn_params, sinks));
   return 0;
 }
 '''
@@ -72,7 +73,7 @@ int main(void) {
     got = [int(x) for x in subprocess.run([exe], capture_output=True, text=True).stdout.split()]
     P = lib.Params
     want = [ctypes.sizeof(P), P.scale.offset, P.rope_cos.offset, P.rope_sin.offset, P.rope_len.offset,
-            P.chunk_pages.offset]
+            P.chunk_pages.offset, P.sinks.offset]
     assert got == want
 
 

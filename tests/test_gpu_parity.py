@@ -96,6 +96,23 @@ def test_many_rows_short_contexts():
     run_step(W(R=300, Pg=2, Hq=8, Hk=2, D=64, theta=10000.0, positions=tuple(int(x) for x in rng.integers(0, 128, 300))))
 
 
+# ----------------------------------------------------- attention sinks -----
+@pytest.mark.parametrize("window,chunk_pages", [(0, 0), (128, 0), (0, 2), (100, 1)])
+def test_attention_sinks_gptoss_shape(window, chunk_pages):
+    # gpt-oss-20b page, SinkAttention `param sinks: Tensor[Heads; T]`
+    rng = np.random.default_rng(window + chunk_pages)
+    sinks = rng.standard_normal(64).tolist()
+    run_step(W(Hq=64, Hk=8, D=64, Pg=8, window=window, theta=150000.0,
+               positions=(0, 5, 63, 64, 200, 511, 300)), chunk_pages=chunk_pages, sinks=sinks)
+
+
+def test_attention_sinks_extreme_values_and_f32():
+    sinks = [12.0, -12.0, 0.0, 3.0] * 4
+    run_step(W(Hq=16, Hk=4, D=128, Pg=4, positions=(0, 100, 255), theta=10000.0), sinks=sinks)
+    run_step(W(Hq=16, Hk=4, D=64, dtype="f32", theta=0.0, Pg=4, positions=(0, 100, 255)), sinks=sinks,
+             chunk_pages=1)
+
+
 # ------------------------------------------------------- repeat / reuse -----
 def test_attend_twice_on_one_plan_is_identical():
     b = binding()

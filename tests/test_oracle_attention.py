@@ -269,3 +269,57 @@ def test_split_merge_of_any_partition_reproduces_the_whole():
         num = sum(np.exp(p[0] - M)[:, None] * p[2] for p in parts)
         den = sum(np.exp(p[0] - M) * p[1] for p in parts)
         assert np.abs(num / den[:, None] - out64[0]).max() <= 1e-12
+
+
+# ---- attention sinks (gpt-oss-20b page, SinkAttention `param sinks`) ------
+def test_sink_at_minus_infinity_changes_nothing():
+    w, a, shape, od = case(R=2, Hq=8, Hk=2, D=64, dtype="f32", positions=(40, 300))
+    _, base, _ = oracle.decode(shape, a["q"], a["positions"], a["table"], a["k_pool"], a["v_pool"])
+    sinks = np.full(8, -np.inf, dtype=np.float32)
+    _, with_sink, _ = oracle.decode(shape, a["q"], a["positions"], a["table"], a["k_pool"], a["v_pool"], sinks)
+    assert np.array_equal(base, with_sink)
+
+
+def test_sink_weights_closed_form():
+    # With every score equal (q = 0) each of the n visible positions weighs
+    # 1 / (n + e^(sink - 0)) and the sink takes the rest; V = one-hot rows
+    # expose the weights.
+    R, Hq, Hk, D, pos = 1, 4, 1, 64, 50
+    shape = oracle.make_shape(R, Hq, Hk, D, 1, 1, oracle.F32)
+    q = np.zeros((R, Hq, D), np.float32)
+    kp = np.random.default_rng(0).standard_normal((1, 1, 64, D)).astype(np.float32)
+    vp = np.zeros((1, 1, 64, D), np.float32)
+    vp[0, 0, np.arange(64), np.arange(64)] = 1.0
+    sinks = np.array([-2.0, 0.0, 1.5, 4.0], np.float32)
+    _, out64, rc = oracle.decode(shape, q, np.array([pos], np.int32), np.zeros((1, 1), np.int32), kp, vp, sinks)
+    assert rc == 0
+    n = pos + 1
+    for h in range(Hq):
+        wgt = 1.0 / (n + math.exp(float(sinks[h])))
+        assert np.abs(out64[0, h, :n] - wgt).max() <= 1e-15
+        assert abs(out64[0, h].sum() - n * wgt) <= 1e-12
+
+
+def test_sinks_against_dense_reference():
+    w, a, shape, od = case(R=3, Hq=16, Hk=4, D=64, dtype="bf16", positions=(0, 70, 380), window=100)
+    rng = np.random.default_rng(4)
+    sinks = torch.from_numpy(rng.standard_normal(16).astype(np.float32)).to(torch.bfloat16)
+    sb = sinks.view(torch.int16).numpy().view(np.uint16)
+    _, out64, rc = oracle.decode(shape, a["q"], a["positions"], a["table"], a["k_pool"], a["v_pool"], sb)
+    assert rc == 0
+    K, V = contiguous_cache(a, shape)
+    q = f64(a["q"], od)
+    Kf, Vf = f64(K, od), f64(V, od)
+    S = Kf.shape[2]
+    t = np.arange(S)
+    for r in range(3):
+        pos = int(a["positions"][r])
+        lo = max(0, pos - 100 + 1)
+        mask = (t <= pos) & (t >= lo)
+        for h in range(16):
+            s = (Kf[r, h // 4] @ q[r, h]) * 0.125
+            logits = np.concatenate([s[mask], [float(sinks[h])]])
+            p = np.exp(logits - logits.max())
+            p /= p.sum()
+            want = p[:-1] @ Vf[r, h // 4][mask]
+            assert np.abs(out64[r, h] - want).max() <= 1e-12
