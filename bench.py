@@ -304,6 +304,30 @@ def run_ours(args, w, world, rank, local):
     rows_all = w.rows * world
     value = all_kv / (ms * 1e-3) / 1e9
 
+    # ---- the same step captured once in a CUDA graph and replayed
+    graph_ms = None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_g = max(10, min(args.steps, 1000))
+        if large:
+            g0.record()
+            for _ in range(n_g):
+                graph.replay()
+            g1.record()
+            torch.cuda.synchronize()
+            graph_ms = g0.elapsed_time(g1) / n_g
+        b.check_status(ws)
+        del graph
+    except Exception as exc:  # capture is an extra measurement; the step above stands on its own
+        print(f"graph capture skipped: {exc}", file=sys.stderr)
+    graph_ms = max_over_ranks(graph_ms, world) if graph_ms is not None else None
+
     # ---- roofline: the attention kernel alone, events around every launch
     q_rot = torch.empty_like(t["q"])
     b.rope_write_kv(p, t["q"], t["k_new"], t["v_new"], t["positions"], t["table"], q_rot, t["k_pool"], t["v_pool"], ws)
@@ -397,6 +421,9 @@ def run_ours(args, w, world, rank, local):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_s * 1e3},
+        "graph": None if graph_ms is None else {
+            "ms_per_step": graph_ms, "value": all_kv / (graph_ms * 1e-3) / 1e9, "unit": "GB/s",
+            "what": "the same step captured once in a CUDA graph and replayed"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
