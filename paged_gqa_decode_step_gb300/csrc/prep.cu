@@ -183,7 +183,119 @@ __device__ __forceinline__ int row_lo(int pos, int window) {
 // largest first (a counting sort over the C sizes), so that the persistent
 // attention kernel hands out long items before short ones.  Each row reserves
 // its items' places with one atomic per size it uses.
+constexpr int kPlanRowsCap = 2048;   // rows whose item places fit the planner's shared array
+
+__device__ __forceinline__ void write_item(ItemDesc* items, int at, int r, int h, int c, int nch, int base,
+                                           int first_page, int npg, int pos, int lo) {
+    int4* dst = reinterpret_cast<int4*>(items + at);
+    dst[0] = make_int4(r, (h << 16) | c, nch, base + h * nch + c);
+    dst[1] = make_int4(first_page, npg, pos, lo);
+}
+
+// One row per thread (rows <= block size): every value stays in registers or
+// shared memory after the positions are read once, so the plan costs one
+// global round trip plus its stores.
+__device__ bool build_plan_small(const PrepArgs& a) {
+    __shared__ int4 s_row[512];
+    __shared__ int2 s_at2[512];
+    __shared__ int s_cnt[kChunkMax + 1];
+    __shared__ int s_cur[kChunkMax + 1];
+    __shared__ int s_warp[16];
+    __shared__ int s_slots;
+    __shared__ int s_chunk;
+    const int tid = threadIdx.x, R = a.rows, Hk = a.kv_heads, max_pos = a.pages_per_row * kPageSize;
+    if (R > (int)blockDim.x || R > 512) return false;
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(a.ws + a.L.ctrl);
+    int4* row_info = reinterpret_cast<int4*>(a.ws + a.L.row_info);
+    ItemDesc* items = reinterpret_cast<ItemDesc*>(a.ws + a.L.items);
+    int* merge_cnt = reinterpret_cast<int*>(a.ws + a.L.merge_cnt);
+
+    const bool mine = tid < R;
+    const int pos = mine ? __ldg(a.positions + tid) : -1;
+    const bool ok = mine && pos >= 0 && pos < max_pos;
+    if (mine && !ok) set_error(ctrl, kErrBadPos);
+    const int lo = ok ? row_lo(pos, a.window) : 0;
+    const int first = lo / kPageSize;
+    const int n = ok ? pos / kPageSize - first + 1 : 0;
+    for (int i = tid; i <= kChunkMax; i += blockDim.x) s_cnt[i] = 0;
+    if (tid == 0) s_slots = 0;
+    const int wsum = __reduce_add_sync(0xffffffffu, (unsigned)n);
+    if ((tid & 31) == 0) s_warp[tid >> 5] = wsum;
+    __syncthreads();
+    if (tid == 0) {
+        long long total = 0;
+        for (int w = 0; w < (int)(blockDim.x + 31) / 32; ++w) total += s_warp[w];
+        int c = a.chunk_pages;
+        if (c <= 0) {
+            const long long per = (long long)kItemsPerCta * a.grid_attend;
+            long long cc = (total * Hk + per - 1) / per;
+            c = (int)(cc < 1 ? 1 : (cc > kChunkMax ? kChunkMax : cc));
+        }
+        s_chunk = c;
+    }
+    __syncthreads();
+    const int C = s_chunk;
+    const int nch = (n + C - 1) / C, full = n / C, tail = n % C;
+    int base = 0;
+    if (ok) {
+        if (full) atomicAdd(&s_cnt[C], full * Hk);
+        if (tail) atomicAdd(&s_cnt[tail], Hk);
+        base = nch ? atomicAdd(&s_slots, nch * Hk) : 0;
+    }
+    if (mine) row_info[tid] = make_int4(ok ? pos : -1, lo, nch, base);
+    __syncthreads();
+    if (tid == 0) {
+        int off = 0;
+        for (int q = C; q >= 1; --q) { s_cur[q] = off; off += s_cnt[q]; }
+        s_cnt[0] = off;
+    }
+    __syncthreads();
+    const int n_items = s_cnt[0];
+    const bool fits = n_items <= a.L.max_items;
+    if (mine) {
+        int at_full = 0, at_tail = 0;
+        if (ok && fits) {
+            at_full = full ? atomicAdd(&s_cur[C], full * Hk) : 0;
+            at_tail = tail ? atomicAdd(&s_cur[tail], Hk) : 0;
+        }
+        s_row[tid] = make_int4(ok ? pos : -1, lo, nch, base);
+        s_at2[tid] = make_int2(at_full, at_tail);
+    }
+    __syncthreads();
+    for (int pr = tid; pr < R * Hk; pr += blockDim.x) {
+        const int r = pr / Hk, h = pr % Hk;
+        merge_cnt[pr] = 0;
+        const int4 ri = s_row[r];
+        if (!fits || ri.x < 0) continue;
+        const int2 at = s_at2[r];
+        const int rf = ri.y / kPageSize, rn = ri.x / kPageSize - rf + 1;
+        const int rfull = rn / C, rtail = rn % C;
+        for (int c = 0; c < ri.z; ++c)
+            write_item(items, c < rfull ? at.x + c * Hk + h : at.y + h, r, h, c, ri.z, ri.w, rf + c * C,
+                       c < rfull ? C : rtail, ri.x, ri.y);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        if (!fits) set_error(ctrl, kErrBadPlan);
+        ctrl->n_items = fits ? n_items : 0;
+        ctrl->chunk_pages = C;
+        ctrl->grid = a.grid_attend;
+        ctrl->next_item = a.grid_attend;   // CTA b takes item b first without an atomic
+        ctrl->done_ctas = 0;
+        ctrl->rows = R;
+        ctrl->kv_heads = Hk;
+        ctrl->pages_per_row = a.pages_per_row;
+        ctrl->max_items = a.L.max_items;
+        ctrl->group = a.heads / Hk;
+        ctrl->head_dim = a.head_dim;
+        ctrl->magic = kPlanMagic;
+    }
+    return true;
+}
+
 __device__ void build_plan(const PrepArgs& a) {
+    if (build_plan_small(a)) return;
+    __shared__ int2 s_at[kPlanRowsCap];
     __shared__ int s_cnt[kChunkMax + 1];
     __shared__ int s_cur[kChunkMax + 1];
     __shared__ unsigned long long s_work;
@@ -231,7 +343,6 @@ __device__ void build_plan(const PrepArgs& a) {
         if (n % C) atomicAdd(&s_cnt[n % C], Hk);
         const int base = nch ? atomicAdd(&s_slots, nch * Hk) : 0;
         row_info[r] = make_int4(ok ? pos : -1, lo, nch, base);
-        for (int h = 0; h < Hk; ++h) merge_cnt[(size_t)r * Hk + h] = 0;
     }
     __syncthreads();
     if (tid == 0) {
@@ -242,34 +353,48 @@ __device__ void build_plan(const PrepArgs& a) {
     __syncthreads();
     const int n_items = s_cnt[0];
     const bool fits = n_items <= a.L.max_items;
+    // Each row reserves its places (one atomic per size it uses); then the
+    // (row, kv head) pairs write their items in parallel.  Rows past the
+    // shared array's capacity write their own items.
     if (fits) {
         for (int r = tid; r < R; r += blockDim.x) {
+            const int4 ri = row_info[r];
+            const int pos = ri.x, lo = ri.y, nch = ri.z, base = ri.w;
+            int at_full = 0, at_tail = 0;
+            if (pos >= 0) {
+                const int first = lo / kPageSize;
+                const int n = pos / kPageSize - first + 1;
+                const int full = n / C, tail = n % C;
+                at_full = full ? atomicAdd(&s_cur[C], full * Hk) : 0;
+                at_tail = tail ? atomicAdd(&s_cur[tail], Hk) : 0;
+                if (r >= kPlanRowsCap) {
+                    for (int c = 0; c < nch; ++c)
+                        for (int h = 0; h < Hk; ++h)
+                            write_item(items, c < full ? at_full + c * Hk + h : at_tail + h, r, h, c, nch, base,
+                                       first + c * C, c < full ? C : tail, pos, lo);
+                }
+            }
+            if (r < kPlanRowsCap) s_at[r] = make_int2(at_full, at_tail);
+        }
+        __syncthreads();
+        const int Rc = R < kPlanRowsCap ? R : kPlanRowsCap;
+        for (long long pr = tid; pr < (long long)R * Hk; pr += blockDim.x) {
+            const int r = (int)(pr / Hk), h = (int)(pr % Hk);
+            merge_cnt[pr] = 0;
+            if (r >= Rc) continue;
             const int4 ri = row_info[r];
             const int pos = ri.x, lo = ri.y, nch = ri.z, base = ri.w;
             if (pos < 0) continue;
             const int first = lo / kPageSize;
             const int n = pos / kPageSize - first + 1;
             const int full = n / C, tail = n % C;
-            const int at_full = full ? atomicAdd(&s_cur[C], full * Hk) : 0;
-            const int at_tail = tail ? atomicAdd(&s_cur[tail], Hk) : 0;
-            for (int c = 0; c < nch; ++c) {
-                const int npg = c < full ? C : tail;
-                for (int h = 0; h < Hk; ++h) {
-                    ItemDesc d;
-                    d.row = r;
-                    d.kvh_chunk = (h << 16) | c;
-                    d.nch = nch;
-                    d.slot = base + h * nch + c;
-                    d.first_page = first + c * C;
-                    d.npg = npg;
-                    d.pos = pos;
-                    d.lo = lo;
-                    const int at = c < full ? at_full + c * Hk + h : at_tail + h;
-                    reinterpret_cast<int4*>(items + at)[0] = make_int4(d.row, d.kvh_chunk, d.nch, d.slot);
-                    reinterpret_cast<int4*>(items + at)[1] = make_int4(d.first_page, d.npg, d.pos, d.lo);
-                }
-            }
+            const int2 at = s_at[r];
+            for (int c = 0; c < nch; ++c)
+                write_item(items, c < full ? at.x + c * Hk + h : at.y + h, r, h, c, nch, base, first + c * C,
+                           c < full ? C : tail, pos, lo);
         }
+    } else {
+        for (long long pr = tid; pr < (long long)R * Hk; pr += blockDim.x) merge_cnt[pr] = 0;
     }
     __syncthreads();
     if (tid == 0) {
@@ -290,7 +415,7 @@ __device__ void build_plan(const PrepArgs& a) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepArgs a) {
+__global__ void __launch_bounds__(512) prep_kernel(const __grid_constant__ PrepArgs a) {
     // Let the attention kernel that follows start its prologue now; it waits
     // for this grid's completion before it reads anything written here.
     griddep_launch_dependents();
@@ -323,9 +448,9 @@ cudaError_t launch_prep(const PrepArgs& a, int dtype, cudaStream_t stream) {
     const int blocks = a.rope_blocks + (a.do_plan ? 1 : 0);
     if (blocks == 0) return cudaSuccess;
     if (dtype == 0)
-        prep_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(a);
+        prep_kernel<__nv_bfloat16><<<blocks, 512, 0, stream>>>(a);
     else
-        prep_kernel<float><<<blocks, 256, 0, stream>>>(a);
+        prep_kernel<float><<<blocks, 512, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

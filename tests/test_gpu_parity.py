@@ -96,6 +96,14 @@ def test_many_rows_short_contexts():
     run_step(W(R=300, Pg=2, Hq=8, Hk=2, D=64, theta=10000.0, positions=tuple(int(x) for x in rng.integers(0, 128, 300))))
 
 
+@pytest.mark.parametrize("chunk_pages", [0, 1])
+def test_more_rows_than_the_planner_block(chunk_pages):
+    # 700 rows take the planner's general path (more rows than threads)
+    rng = np.random.default_rng(6)
+    run_step(W(R=700, Pg=3, Hq=8, Hk=2, D=64, theta=10000.0,
+               positions=tuple(int(x) for x in rng.integers(0, 192, 700))), chunk_pages=chunk_pages)
+
+
 # ----------------------------------------------------- attention sinks -----
 @pytest.mark.parametrize("window,chunk_pages", [(0, 0), (128, 0), (0, 2), (100, 1)])
 def test_attention_sinks_gptoss_shape(window, chunk_pages):
