@@ -18,6 +18,9 @@ Functions and the passages they follow (page title, section):
                   optional attention sinks (gpt-oss-20b page, SinkAttention
                   ``param sinks``) as one value-less logit per query head
   step            rope_write_kv followed by decode
+  prefill_paged   packed prompt tokens: rope, write at their pool slots, then
+                  each token's causal attention over its row (the
+                  llama-3.1-8b-instruct page's ``prefill_paged`` signature)
 
 Every function is pinned by tests under ``tests/test_oracle_*.py`` against
 closed forms, brute force and invariants; the rotation direction of RoPE is
@@ -58,10 +61,11 @@ def lib():
         L.oracle_decode.argtypes = [ctypes.POINTER(Shape)] + [vp] * 7
         L.oracle_decode_sinks.argtypes = [ctypes.POINTER(Shape)] + [vp] * 8
         L.oracle_step.argtypes = [ctypes.POINTER(Shape)] + [vp] * 10
+        L.oracle_prefill_paged.argtypes = [ctypes.POINTER(Shape), ctypes.c_int] + [vp] * 13
         L.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
         L.oracle_f32_to_bf16.restype = ctypes.c_uint16
         for f in (L.oracle_rope_tables, L.oracle_rope_write_kv, L.oracle_decode, L.oracle_decode_sinks,
-                  L.oracle_step):
+                  L.oracle_step, L.oracle_prefill_paged):
             f.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -121,6 +125,17 @@ def step(shape, q, k_new, v_new, positions, table, k_pool, v_pool):
     rc = lib().oracle_step(ctypes.byref(shape), _ptr(q), _ptr(k_new), _ptr(v_new),
                            _ptr(positions), _ptr(table), _ptr(k_pool), _ptr(v_pool),
                            _ptr(q_rot), _ptr(out), _ptr(out64))
+    return q_rot, out, out64, rc
+
+
+def prefill_paged(shape, q, k_new, v_new, positions, rows, slots, table, k_pool, v_pool, sinks=None):
+    """Prefill of packed tokens; pools updated in place.  Returns (q_rot, out, out64, status)."""
+    q_rot = np.empty_like(q)
+    out = np.zeros(q.shape, dtype=q.dtype)
+    out64 = np.zeros(q.shape, dtype=np.float64)
+    rc = lib().oracle_prefill_paged(ctypes.byref(shape), int(q.shape[0]), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                    _ptr(positions), _ptr(rows), _ptr(slots), _ptr(table), _ptr(k_pool),
+                                    _ptr(v_pool), _ptr(sinks), _ptr(q_rot), _ptr(out), _ptr(out64))
     return q_rot, out, out64, rc
 
 

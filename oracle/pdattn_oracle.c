@@ -19,6 +19,9 @@
  *                        (`decode_paged`, `table: Tensor[Rows, Pages; i32]`)
  *                        and the `PageSize: Dim = 64` generic of
  *                        GroupedQueryAttention.
+ *   oracle_prefill_paged rope + write of packed prompt tokens at their slots,
+ *                        then each token's causal attention over its row
+ *                        (llama-3.1-8b-instruct page, `prefill_paged`).
  *   oracle_decode(_sinks) Llama example page, "src/attention.linnet"
  *                        (`decode`): mask seen[s] = s <= pos, scale
  *                        rsqrt(f32(head dim)), grouped attention where query
@@ -288,6 +291,58 @@ int oracle_step(const oracle_shape* p, const void* q, const void* k_new, const v
     int s1 = oracle_rope_write_kv(p, q, k_new, v_new, positions, table, q_rot, k_pool, v_pool);
     int s2 = oracle_decode(p, q_rot, positions, table, k_pool, v_pool, out, out64);
     return s1 != ORACLE_OK ? s1 : s2;
+}
+
+/*
+ * Prefill of packed prompt tokens over the paged cache (llama-3.1-8b-instruct
+ * architecture page, `prefill_paged(x: Tensor[1, P, H; T], positions:
+ * Tensor[P; i32], rows: Tensor[P; i32], slots: Tensor[P; i32], table:
+ * Tensor[Rows, Pages; i32])`).  Reading: token i belongs to cache row
+ * rows[i] at position positions[i]; slots[i] is its flat pool slot (page *
+ * PageSize + offset), where its rotated k and its v are written.  All tokens
+ * are written first; then each token attends, like `decode`, over its row's
+ * cached positions [lo, pos] read through the table.  q, k_new, v_new, out:
+ * [P, heads or kv_heads, D].  sinks may be NULL.
+ */
+int oracle_prefill_paged(const oracle_shape* p, int n_tokens, const void* q, const void* k_new,
+                         const void* v_new, const int32_t* positions, const int32_t* rows,
+                         const int32_t* slots, const int32_t* table, void* k_pool, void* v_pool,
+                         const void* sinks, void* q_rot, void* out, double* out64) {
+    if (!shape_ok(p) || n_tokens < 0) return ORACLE_EINVAL;
+    const int D = p->head_dim, Hq = p->heads, Hk = p->kv_heads, PS = p->page_size;
+    int status = ORACLE_OK;
+    /* 1. rotate q and k at each token's position; write k and v at its slot */
+    for (int i = 0; i < n_tokens; ++i) {
+        int pos = positions[i];
+        int slot = slots[i];
+        int page = slot / PS, off = slot % PS;
+        for (int h = 0; h < Hq; ++h) {
+            size_t o = ((size_t)i * Hq + h) * D;
+            if (p->rope_theta > 0.0f) rope_vector(q, o, q_rot, o, D, pos, p->rope_theta, p->dtype);
+            else for (int d = 0; d < D; ++d) copy_t(q_rot, o + d, q, o + d, p->dtype);
+        }
+        if (slot < 0 || page >= p->num_pages) { status = ORACLE_EBADPAGE; continue; }
+        for (int h = 0; h < Hk; ++h) {
+            size_t o = ((size_t)i * Hk + h) * D;
+            size_t dst = pool_index(p, page, h, off, 0);
+            if (p->rope_theta > 0.0f) rope_vector(k_new, o, k_pool, dst, D, pos, p->rope_theta, p->dtype);
+            else for (int d = 0; d < D; ++d) copy_t(k_pool, dst + d, k_new, o + d, p->dtype);
+            for (int d = 0; d < D; ++d) copy_t(v_pool, dst + d, v_new, o + d, p->dtype);
+        }
+    }
+    /* 2. each token attends over its row's cache through the table */
+    oracle_shape one = *p;
+    one.rows = 1;
+    for (int i = 0; i < n_tokens; ++i) {
+        int r = rows[i];
+        if (r < 0 || r >= p->rows) { status = ORACLE_EINVAL; continue; }
+        int st = oracle_decode_sinks(&one, (const char*)q_rot + (size_t)i * Hq * D * (p->dtype == 0 ? 2 : 4),
+                                     positions + i, table + (size_t)r * p->pages_per_row, k_pool, v_pool,
+                                     sinks, (char*)out + (size_t)i * Hq * D * (p->dtype == 0 ? 2 : 4),
+                                     out64 ? out64 + (size_t)i * Hq * D : NULL);
+        if (st != ORACLE_OK) status = st;
+    }
+    return status;
 }
 
 /* Exposed for pins on the rounding helper itself. */

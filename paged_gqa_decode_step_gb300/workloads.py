@@ -185,3 +185,74 @@ def from_numpy(a, dtype) -> torch.Tensor:
     if dtype == torch.bfloat16:
         return t.view(torch.int16).view(torch.bfloat16)
     return t
+
+
+@dataclass(frozen=True)
+class PrefillWorkload:
+    """Packed prompt chunks: row r holds `prefix[r]` cached positions and gets
+    `chunk[r]` new tokens at positions prefix[r] .. prefix[r] + chunk[r] - 1,
+    packed row after row."""
+    name: str
+    prefix: Sequence[int]
+    chunk: Sequence[int]
+    heads: int
+    kv_heads: int
+    head_dim: int
+    pages_per_row: int
+    dtype: str = "bf16"
+    rope_theta: float = 10000.0
+    window: int = 0
+    seed: int = 0
+
+    @property
+    def rows(self) -> int:
+        return len(self.prefix)
+
+    @property
+    def tokens(self) -> int:
+        return int(sum(self.chunk))
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    @property
+    def max_seq(self) -> int:
+        return self.pages_per_row * PAGE_SIZE
+
+
+def generate_prefill(w: PrefillWorkload, device="cpu", seed: Optional[int] = None):
+    """Inputs of one prefill call: q [P, Hq, D], k_new / v_new [P, Hk, D],
+    positions / rows / slots [P] i32 (slot = page * 64 + offset of the token's
+    position in its row), table [R, Pages] i32, pools [NumPages, Hk, 64, D].
+    Draw order: page permutation -> q -> k_new -> v_new -> k_pool -> v_pool;
+    the pool is N(0, 1) everywhere, so every prefix position holds a key."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed if seed is None else seed)
+    ends = [p + c for p, c in zip(w.prefix, w.chunk)]
+    assert max(ends) <= w.max_seq
+    need = [(e + PAGE_SIZE - 1) // PAGE_SIZE for e in ends]
+    total = sum(need)
+    num_pages = total + math.ceil(total * 0.1)
+    perm = torch.randperm(num_pages, generator=gen, device=device).to(torch.int32).cpu()
+    table = torch.full((w.rows, w.pages_per_row), -1, dtype=torch.int32)
+    off = 0
+    for r, n in enumerate(need):
+        table[r, :n] = perm[off:off + n]
+        off += n
+    positions, rows, slots = [], [], []
+    for r, (p0, c) in enumerate(zip(w.prefix, w.chunk)):
+        for t in range(p0, p0 + c):
+            positions.append(t)
+            rows.append(r)
+            slots.append(int(table[r, t // PAGE_SIZE]) * PAGE_SIZE + t % PAGE_SIZE)
+
+    def normal(*shape):
+        return torch.randn(*shape, generator=gen, device=device, dtype=torch.float32).to(w.torch_dtype)
+
+    P, Hq, Hk, D = w.tokens, w.heads, w.kv_heads, w.head_dim
+    i32 = lambda x: torch.tensor(x, dtype=torch.int32, device=device)
+    return dict(q=normal(P, Hq, D), k_new=normal(P, Hk, D), v_new=normal(P, Hk, D), positions=i32(positions),
+                rows=i32(rows), slots=i32(slots), table=table.to(device),
+                k_pool=normal(num_pages, Hk, PAGE_SIZE, D), v_pool=normal(num_pages, Hk, PAGE_SIZE, D))
