@@ -17,6 +17,11 @@ Default workload: the Llama-3.1-8B serving batch (256 rows, 32 query heads,
 * cpu_baseline: the CPU oracle on the host (single thread), timed on whole
   steps of the same workload.
 * --impl reference: the CPU oracle alone, each step a bounded sample of rows.
+
+--workload llama8b_prefill measures the paged prefill instead (8 rows x 1024
+new tokens on cached prefixes 0 .. 7168, Llama-3.1-8B attention shape): value
+= attention TFLOP/s of whole prefill calls (4 * D * heads * visible keys per
+token), roofline against the measured bf16 tensor peak.
 """
 import argparse
 import glob
@@ -472,13 +477,202 @@ def run_reference(args, w, world, rank):
     }
 
 
+# ---------------------------------------------------------------- prefill --
+PREFILL_METRIC = "paged prefill attention TFLOP/s (% of GB300 bf16 tensor peak)"
+
+
+def prefill_flops(w, positions):
+    """4 * D * heads per visible (query token, key) pair: QK^T and PV."""
+    return sum(4 * w.head_dim * w.heads * visible(w, int(p))[1] for p in positions)
+
+
+def measured_tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def cpu_oracle_prefill_rate(w, host, budget_s, max_tokens=None, seed=0):
+    """The oracle's prefill on random samples of the packed tokens (each call
+    writes and attends its sample) for about budget_s; returns
+    (TFLOP/s, seconds, description, tokens)."""
+    import numpy as np
+    import oracle
+    P = len(host["positions"])
+    shape = oracle.make_shape(w.rows, w.heads, w.kv_heads, w.head_dim, w.pages_per_row, host["k_pool"].shape[0],
+                              oracle.BF16, window=w.window, rope_theta=w.rope_theta)
+    rng = np.random.default_rng(seed)
+    flops, spent, tokens = 0, 0.0, 0
+    while True:
+        idx = np.sort(rng.choice(P, 8, replace=False))
+        sub = {k: np.ascontiguousarray(host[k][idx]) for k in ("q", "k_new", "v_new", "positions", "rows", "slots")}
+        t0 = time.perf_counter()
+        _, _, _, rc = oracle.prefill_paged(shape, sub["q"], sub["k_new"], sub["v_new"], sub["positions"],
+                                           sub["rows"], sub["slots"], host["table"], host["k_pool"], host["v_pool"])
+        spent += time.perf_counter() - t0
+        assert rc == 0
+        flops += prefill_flops(w, sub["positions"])
+        tokens += len(idx)
+        if (max_tokens and tokens >= max_tokens) or (not max_tokens and spent >= budget_s):
+            break
+    desc = f"oracle prefill of {tokens} tokens sampled at random from the {P} (8 per call), single thread"
+    return flops / spent / 1e12, spent, desc, tokens
+
+
+def run_prefill(args, w, world, rank, local):
+    from paged_gqa_decode_step_gb300 import build
+    build.build()
+    from paged_gqa_decode_step_gb300 import binding as b
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    t = wl.generate_prefill(w, dev, seed=rank_seed(w, rank))
+    P = w.tokens
+    pos_list = t["positions"].cpu().tolist()
+    num_pages = t["k_pool"].shape[0]
+    cos, sin = b.rope_tables(w.rope_theta, w.head_dim, w.max_seq, torch.bfloat16)
+    p = b.make_params(w.rows, w.heads, w.kv_heads, w.head_dim, w.pages_per_row, num_pages, torch.bfloat16,
+                      window=w.window, rope_cos=cos, rope_sin=sin)
+    ws = b.new_prefill_workspace(p, P)
+    out = torch.empty_like(t["q"])
+    flops = prefill_flops(w, pos_list)
+    flush = torch.empty(4 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+    names = ("q", "k_new", "v_new", "positions", "rows", "slots", "table", "k_pool", "v_pool")
+
+    def step():
+        b.prefill_paged(p, *(t[k] for k in names), out, ws)
+
+    for _ in range(args.warmup):
+        step()
+    b.check_status(ws)
+    launches_per_step = b.last_launch_count()
+
+    def timed(fn, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize()
+        for e0, e1 in evs:
+            flush.fill_(1)
+            e0.record()
+            fn()
+            e1.record()
+        torch.cuda.synchronize()
+        return sum(e0.elapsed_time(e1) for e0, e1 in evs) / n
+
+    with ClockSampler(dev) as clocks:
+        barrier(world)
+        ms = timed(step, args.steps)
+        barrier(world)
+    clk = clocks.summary()
+    b.check_status(ws)
+    ms = max_over_ranks(ms, world)
+    all_flops = sum_over_ranks(flops, world)
+    value = all_flops / (ms * 1e-3) / 1e12
+
+    # roofline: the attention kernel alone (prefill_attend), events around each launch
+    att_ms = timed(lambda: b.prefill_attend(p, t["positions"], t["table"], t["k_pool"], t["v_pool"], out, ws),
+                   max(20, min(args.steps, 200)))
+    b.check_status(ws)
+    peak, peak_kind = measured_tensor_peak()
+    achieved = flops / (att_ms * 1e-3) / 1e12
+
+    # end to end: pinned host inputs in, output back, every call
+    host_in = {k: t[k].cpu().pin_memory() for k in ("q", "k_new", "v_new", "positions", "rows", "slots", "table")}
+    dev_in = {k: torch.empty_like(t[k]) for k in host_in}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    stream = torch.cuda.current_stream()
+
+    def e2e_step():
+        for k in host_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        b.prefill_paged(p, dev_in["q"], dev_in["k_new"], dev_in["v_new"], dev_in["positions"], dev_in["rows"],
+                        dev_in["slots"], dev_in["table"], t["k_pool"], t["v_pool"], out, ws)
+        host_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    n_e2e = max(10, min(args.steps, 100))
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        e2e_step()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, world)
+    b.check_status(ws)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = {k: wl.to_numpy(v) for k, v in t.items()}
+        rate, spent, desc, _ = cpu_oracle_prefill_rate(w, host, args.cpu_baseline_seconds)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": desc,
+               "seconds": round(spent, 2), "cpu": cpu_model()}
+    if rank != 0:
+        return None
+    return {
+        "metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v and prefilled pool, shuffled page table)",
+        "config": {
+            "workload": w.name, "rows_per_gpu": w.rows, "tokens_per_gpu": P, "prefix": list(w.prefix),
+            "chunk": list(w.chunk), "heads": w.heads, "kv_heads": w.kv_heads, "head_dim": w.head_dim,
+            "page_size": 64, "window": w.window, "rope_theta": w.rope_theta, "flops_per_step_per_gpu": flops,
+            "l2": "L2 flushed (512 MB write) between timed steps, outside the events",
+            "parallelism": f"replicas x{world} (rows sharded across ranks, no exchange)",
+        },
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": f"prefill_kernel<{w.head_dim}>",
+                     "flops_per_launch": flops, "launch_us": att_ms * 1e3, "peak_kind": peak_kind},
+        "cpu_baseline": cpu,
+        "e2e": {"value": all_flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+
+
+def run_prefill_reference(args, w, world, rank):
+    if rank != 0:
+        return None
+    t = wl.generate_prefill(w, "cpu", seed=rank_seed(w, 0))
+    host = {k: wl.to_numpy(v) for k, v in t.items()}
+    del t
+    per_step = max(8, int(min(5.0, 90.0 / max(1, args.steps + args.warmup)) / 0.05) // 8 * 8)
+    if args.warmup:
+        cpu_oracle_prefill_rate(w, host, 0, max_tokens=8 * args.warmup, seed=1)
+    rates = []
+    spent_all, toks = 0.0, 0
+    for k in range(max(1, args.steps)):
+        r, spent, desc, n = cpu_oracle_prefill_rate(w, host, 0, max_tokens=per_step, seed=2 + k)
+        rates.append(r)
+        spent_all += spent
+        toks += n
+    rate = sum(rates) / len(rates)
+    desc = f"oracle prefill of {toks} tokens sampled at random from the {w.tokens} (8 per call), single thread"
+    return {
+        "metric": PREFILL_METRIC, "value": rate, "unit": "TFLOP/s", "n_gpus": world, "steps": len(rates),
+        "warmup": args.warmup, "ms_per_step": spent_all / len(rates) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name, "tokens_per_step": per_step, "tokens": w.tokens},
+        "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": desc, "value": rate, "unit": "TFLOP/s",
+                         "cpu": cpu_model()},
+        "e2e": {"value": rate, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama8b_serving", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--workload", default="llama8b_serving",
+                    choices=sorted(wl.WORKLOADS) + sorted(wl.PREFILL_WORKLOADS))
     ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--chunk-pages", type=int, default=0,
@@ -488,8 +682,20 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    w = wl.WORKLOADS[args.workload]
     world, rank, local = dist_setup()
+    if args.workload in wl.PREFILL_WORKLOADS:
+        w = wl.PREFILL_WORKLOADS[args.workload]
+        if args.impl == "reference":
+            line = run_prefill_reference(args, w, world, rank)
+        else:
+            line = run_prefill(args, w, world, rank, local)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    w = wl.WORKLOADS[args.workload]
     if args.impl == "reference":
         line = run_reference(args, w, world, rank)
     else:

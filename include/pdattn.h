@@ -178,6 +178,52 @@ pdattn_status pdattn_decode_fused_noalloc(const pdattn_params* p, const void* q,
                                           void* out, pdattn_stream stream);
 
 /*
+ * Bytes of workspace pdattn_prefill_paged needs for n_tokens packed tokens
+ * (256-byte aligned; 0 if the parameters are invalid).
+ */
+size_t pdattn_prefill_workspace_size(const pdattn_params* p, int32_t n_tokens);
+
+/*
+ * Paged prefill of packed prompt tokens: `prefill_paged(…, positions, rows,
+ * slots, table)` of the llama-3.1-8b-instruct architecture page, the prefill
+ * half of its `step_paged`.  For each of the n_tokens tokens i:
+ *   q_rot[i] = rope(q[i], positions[i]); the rotated k_new[i] and v_new[i]
+ *   are written at pool slot slots[i] (page slots[i] / 64, offset
+ *   slots[i] % 64).  Every token is written before any is read; then
+ *   out[i, h] = sum_t softmax_t(scale * q_rot[i, h] . K[t, h / g]) V[t, h / g]
+ *   over the positions t in [lo_i, positions[i]] of table row rows[i]
+ *   (lo_i = 0, or positions[i] - window + 1 with a window), read through
+ *   table[rows[i], t / 64], with the sinks of p as in pdattn_attend.
+ * Layouts: q, out [n_tokens, heads, head_dim]; k_new, v_new [n_tokens,
+ * kv_heads, head_dim]; positions, rows, slots [n_tokens] int32; table
+ * [p->rows, pages_per_row].  p->rows is the number of table rows.  Tokens
+ * of one row should be contiguous (consecutive positions give the best
+ * tiles) but need not be.  The attention runs on the tensor cores and needs
+ * dtype bf16 (PDATTN_EUNSUPPORTED otherwise).  The workspace
+ * (pdattn_prefill_workspace_size) holds the rotated queries and the tile
+ * list; a row index outside [0, rows) or a bad position is recorded as
+ * PDATTN_EBADPOS and the call writes no output; a slot outside the pools
+ * is recorded as PDATTN_EBADPAGE and that token's k / v are not written.
+ */
+pdattn_status pdattn_prefill_paged(const pdattn_params* p, int32_t n_tokens, const void* q,
+                                   const void* k_new, const void* v_new, const int32_t* positions,
+                                   const int32_t* rows, const int32_t* slots, const int32_t* table,
+                                   void* k_pool, void* v_pool, void* out, void* workspace,
+                                   size_t workspace_bytes, pdattn_stream stream);
+
+/*
+ * The attention half of pdattn_prefill_paged alone: re-runs it over the
+ * rotated queries and the tile list that the last pdattn_prefill_paged call
+ * on this workspace left there, with the same parameters, n_tokens,
+ * positions and table, against the pools as they are now.  For callers that
+ * write the cache once and attend again (and for timing the attention).
+ */
+pdattn_status pdattn_prefill_attend(const pdattn_params* p, int32_t n_tokens, const int32_t* positions,
+                                    const int32_t* table, const void* k_pool, const void* v_pool,
+                                    void* out, void* workspace, size_t workspace_bytes,
+                                    pdattn_stream stream);
+
+/*
  * Synchronises `stream`, reads the workspace's device status word, clears
  * it and returns the first error it recorded (PDATTN_OK if none).
  */

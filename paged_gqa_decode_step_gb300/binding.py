@@ -51,6 +51,9 @@ def _load():
         "pdattn_decode": (i32, [P, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "pdattn_decode_fused": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "pdattn_decode_fused_noalloc": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
+        "pdattn_prefill_workspace_size": (sz, [P, i32]),
+        "pdattn_prefill_paged": (i32, [P, i32] + [vp] * 11 + [sz, vp]),
+        "pdattn_prefill_attend": (i32, [P, i32] + [vp] * 6 + [sz, vp]),
         "pdattn_check_status": (i32, [vp, vp]),
         "pdattn_last_error": (ctypes.c_char_p, []),
         "pdattn_last_launch_count": (i32, []),
@@ -196,6 +199,50 @@ def decode_fused_noalloc(p, q, k_new, v_new, positions, table, k_pool, v_pool, o
     _check_q(p, q=q, k_new=k_new, v_new=v_new, out=out)
     _check(lib.pdattn_decode_fused_noalloc(ctypes.byref(p), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions),
                                            _ptr(table), _ptr(k_pool), _ptr(v_pool), _ptr(out), _stream(stream)))
+
+
+def prefill_workspace_size(p, n_tokens):
+    n = lib.pdattn_prefill_workspace_size(ctypes.byref(p), n_tokens)
+    if n == 0:
+        raise PdattnError(EINVAL, lib.pdattn_last_error().decode() or "invalid parameters")
+    return n
+
+
+def new_prefill_workspace(p, n_tokens, device="cuda"):
+    return torch.zeros(prefill_workspace_size(p, n_tokens), dtype=torch.uint8, device=device)
+
+
+def prefill_paged(p, q, k_new, v_new, positions, rows, slots, table, k_pool, v_pool, out, ws, stream=None):
+    """Packed prompt tokens: q / out [P, heads, D], k_new / v_new [P, kv_heads, D],
+    positions / rows / slots [P] int32; p.rows is the number of table rows."""
+    n = q.shape[0] if isinstance(q, torch.Tensor) else -1
+    _expect("table", table, (p.rows, p.pages_per_row), torch.int32)
+    pool = (p.num_pages, p.kv_heads, 64, p.head_dim)
+    _expect("k_pool", k_pool, pool, _dt(p))
+    _expect("v_pool", v_pool, pool, _dt(p))
+    for name, t in (("positions", positions), ("rows", rows), ("slots", slots)):
+        _expect(name, t, (n,), torch.int32)
+    for name, t, h in (("q", q, p.heads), ("k_new", k_new, p.kv_heads), ("v_new", v_new, p.kv_heads),
+                       ("out", out, p.heads)):
+        _expect(name, t, (n, h, p.head_dim), _dt(p))
+    w, nb = _ws(ws)
+    _check(lib.pdattn_prefill_paged(ctypes.byref(p), n, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions),
+                                    _ptr(rows), _ptr(slots), _ptr(table), _ptr(k_pool), _ptr(v_pool), _ptr(out),
+                                    w, nb, _stream(stream)))
+
+
+def prefill_attend(p, positions, table, k_pool, v_pool, out, ws, stream=None):
+    """Attention half of prefill_paged, over what its last call left in ws."""
+    n = out.shape[0] if isinstance(out, torch.Tensor) else -1
+    _expect("positions", positions, (n,), torch.int32)
+    _expect("table", table, (p.rows, p.pages_per_row), torch.int32)
+    pool = (p.num_pages, p.kv_heads, 64, p.head_dim)
+    _expect("k_pool", k_pool, pool, _dt(p))
+    _expect("v_pool", v_pool, pool, _dt(p))
+    _expect("out", out, (n, p.heads, p.head_dim), _dt(p))
+    w, nb = _ws(ws)
+    _check(lib.pdattn_prefill_attend(ctypes.byref(p), n, _ptr(positions), _ptr(table), _ptr(k_pool), _ptr(v_pool),
+                                     _ptr(out), w, nb, _stream(stream)))
 
 
 def check_status(ws, stream=None):

@@ -343,6 +343,134 @@ pdattn_status pdattn_decode_fused(const pdattn_params* p, const void* q, const v
     return s;
 }
 
+size_t pdattn_prefill_workspace_size(const pdattn_params* p, int32_t n_tokens) {
+    if (check_params(p) != PDATTN_OK || n_tokens < 0) return 0;
+    return pf_layout(n_tokens, p->heads, p->head_dim, elem_bytes(p)).total;
+}
+
+// Shared body of the two prefill entry points; with_prep false re-runs the
+// attention only, over the tile list and rotated queries in the workspace.
+static pdattn_status prefill_impl(const pdattn_params* p, int32_t n_tokens, const void* q, const void* k_new,
+                                  const void* v_new, const int32_t* positions, const int32_t* rows,
+                                  const int32_t* slots, const int32_t* table, void* k_pool, void* v_pool,
+                                  void* out, void* workspace, size_t workspace_bytes, pdattn_stream stream,
+                                  bool with_prep) {
+    g_launches = 0;
+    pdattn_status s = check_params(p);
+    if (s != PDATTN_OK) return s;
+    if (n_tokens < 0) return fail(PDATTN_EINVAL, "n_tokens < 0");
+    if (p->dtype != PDATTN_BF16) return fail(PDATTN_EUNSUPPORTED, "prefill runs on the tensor cores: dtype must be bf16");
+    if (p->rows <= 0) return fail(PDATTN_EINVAL, "prefill needs at least one table row");
+    if (n_tokens == 0) return PDATTN_OK;
+    if (!positions || !table || !k_pool || !v_pool || !out ||
+        (with_prep && (!q || !k_new || !v_new || !rows || !slots)))
+        return fail(PDATTN_EINVAL, "NULL data pointer");
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
+        (with_prep && (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new))))
+        return fail(PDATTN_EINVAL, "q, k_new, v_new, the pools and out must be 16-byte aligned");
+    if (!workspace) return fail(PDATTN_EINVAL, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+        return fail(PDATTN_EINVAL, "workspace must be 256-byte aligned");
+    const PfLayout L = pf_layout(n_tokens, p->heads, p->head_dim, 2);
+    if (workspace_bytes < L.total)
+        return fail(PDATTN_EINVAL, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, L.total);
+    const int sms = sm_count();
+    if (sms <= 0) return fail(PDATTN_ECUDA, "no CUDA device");
+    char* ws = static_cast<char*>(workspace);
+    const int g = p->heads / p->kv_heads;
+    const int tile_tokens = kPfRows / g;
+
+    // Rotated queries [n_tokens, heads, D] as a 3-D tensor (D, heads, tokens):
+    // one box = the g heads of a kv head for tile_tokens tokens, 64 columns wide.
+    auto fn = encode_fn();
+    if (!fn) return fail(PDATTN_ECUDA, "cuTensorMapEncodeTiled is not available");
+    CUtensorMap qm, km, vm;
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)p->head_dim, (cuuint64_t)p->heads, (cuuint64_t)n_tokens};
+        cuuint64_t strides[2] = {(cuuint64_t)p->head_dim * 2, (cuuint64_t)p->heads * p->head_dim * 2};
+        cuuint32_t box[3] = {64, (cuuint32_t)g, (cuuint32_t)tile_tokens};
+        cuuint32_t estr[3] = {1, 1, 1};
+        CUresult r = fn(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ws + L.q_rot, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(PDATTN_ECUDA, "cuTensorMapEncodeTiled (queries) failed (%d)", (int)r);
+    }
+    s = make_pool_map(&km, k_pool, p);
+    if (s != PDATTN_OK) return s;
+    s = make_pool_map(&vm, v_pool, p);
+    if (s != PDATTN_OK) return s;
+
+    int launches = 0;
+    if (with_prep) {
+        PrefillPrepArgs pa = {};
+        pa.n_tokens = n_tokens;
+        pa.rows = p->rows;
+        pa.heads = p->heads;
+        pa.kv_heads = p->kv_heads;
+        pa.head_dim = p->head_dim;
+        pa.pages_per_row = p->pages_per_row;
+        pa.num_pages = p->num_pages;
+        pa.window = p->window;
+        pa.rope_len = p->rope_len;
+        pa.tile_tokens = tile_tokens;
+        pa.q = q;
+        pa.k_new = k_new;
+        pa.v_new = v_new;
+        pa.positions = positions;
+        pa.row_of = rows;
+        pa.slots = slots;
+        pa.rope_cos = p->rope_cos;
+        pa.rope_sin = p->rope_sin;
+        pa.k_pool = k_pool;
+        pa.v_pool = v_pool;
+        pa.ws = ws;
+        pa.L = L;
+        cudaError_t e = launch_prefill_prep(pa, p->dtype, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill rope/write/tile launch");
+        ++launches;
+    }
+
+    PrefillArgs aa = {};
+    aa.n_tokens = n_tokens;
+    aa.heads = p->heads;
+    aa.kv_heads = p->kv_heads;
+    aa.group = g;
+    aa.tile_tokens = tile_tokens;
+    aa.head_dim = p->head_dim;
+    aa.pages_per_row = p->pages_per_row;
+    aa.num_pages = p->num_pages;
+    aa.window = p->window;
+    aa.scale_log2 = scale_log2(p);
+    aa.positions = positions;
+    aa.table = table;
+    aa.sinks = p->sinks;
+    aa.out = out;
+    aa.ws = ws;
+    aa.L = L;
+    const long long units = (long long)n_tokens * p->kv_heads;   // bound on tiles x kv heads
+    const int grid = (int)(units < sms ? units : sms);
+    cudaError_t e = launch_prefill(aa, qm, km, vm, grid, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
+    g_launches = launches + 1;
+    return PDATTN_OK;
+}
+
+pdattn_status pdattn_prefill_paged(const pdattn_params* p, int32_t n_tokens, const void* q, const void* k_new,
+                                   const void* v_new, const int32_t* positions, const int32_t* rows,
+                                   const int32_t* slots, const int32_t* table, void* k_pool, void* v_pool,
+                                   void* out, void* workspace, size_t workspace_bytes, pdattn_stream stream) {
+    return prefill_impl(p, n_tokens, q, k_new, v_new, positions, rows, slots, table, k_pool, v_pool, out,
+                        workspace, workspace_bytes, stream, true);
+}
+
+pdattn_status pdattn_prefill_attend(const pdattn_params* p, int32_t n_tokens, const int32_t* positions,
+                                    const int32_t* table, const void* k_pool, const void* v_pool, void* out,
+                                    void* workspace, size_t workspace_bytes, pdattn_stream stream) {
+    return prefill_impl(p, n_tokens, nullptr, nullptr, nullptr, positions, nullptr, nullptr, table,
+                        const_cast<void*>(k_pool), const_cast<void*>(v_pool), out, workspace, workspace_bytes,
+                        stream, false);
+}
+
 pdattn_status pdattn_check_status(void* workspace, pdattn_stream stream) {
     if (!workspace) return fail(PDATTN_EINVAL, "workspace is NULL");
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);

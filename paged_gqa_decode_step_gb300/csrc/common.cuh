@@ -88,6 +88,35 @@ __host__ __device__ inline WsLayout ws_layout(int rows, int heads, int kv_heads,
 }
 
 // ---------------------------------------------------------------------------
+// Paged prefill: tiles of consecutive tokens of one row and the workspace.
+// ---------------------------------------------------------------------------
+constexpr int kPfRows = 128;          // MMA rows of a prefill tile: tokens x query heads of a group
+
+// Tokens [t0, t0 + ntok) of table row `row`; they see pages
+// [first_page, first_page + npg) of the row, positions [lo_min, pos_max].
+struct __align__(32) PfTile {
+    int t0, ntok, row, first_page;
+    int npg, lo_min, pos_max, pad;
+};
+static_assert(sizeof(PfTile) == 32, "prefill tile descriptor is 32 bytes");
+
+struct PfLayout {
+    size_t ctrl, tiles_raw, tiles, q_rot, total;
+};
+
+// Tiles never outnumber tokens.
+__host__ __device__ inline PfLayout pf_layout(int n_tokens, int heads, int head_dim, int elem_bytes) {
+    PfLayout L;
+    size_t off = 0;
+    L.ctrl = off; off += 256;
+    L.tiles_raw = off; off = align256(off + sizeof(PfTile) * (size_t)n_tokens);
+    L.tiles = off; off = align256(off + sizeof(PfTile) * (size_t)n_tokens);
+    L.q_rot = off; off = align256(off + (size_t)elem_bytes * n_tokens * heads * head_dim);
+    L.total = off;
+    return L;
+}
+
+// ---------------------------------------------------------------------------
 // PTX wrappers
 // ---------------------------------------------------------------------------
 

@@ -36,6 +36,34 @@ struct AttendArgs {
     WsLayout L;
 };
 
+struct PrefillPrepArgs {
+    int n_tokens, rows, heads, kv_heads, head_dim, pages_per_row, num_pages, window, rope_len;
+    int tile_tokens;        // tokens per tile: 128 / (heads / kv_heads)
+    const void* q;          // [n_tokens, heads, D]
+    const void* k_new;      // [n_tokens, kv_heads, D]
+    const void* v_new;
+    const int* positions;   // [n_tokens]
+    const int* row_of;      // [n_tokens] table row of each token
+    const int* slots;       // [n_tokens] page * 64 + offset
+    const void* rope_cos;   // nullptr: copy without rotation
+    const void* rope_sin;
+    void* k_pool;
+    void* v_pool;
+    char* ws;
+    PfLayout L;
+};
+
+struct PrefillArgs {
+    int n_tokens, heads, kv_heads, group, tile_tokens, head_dim, pages_per_row, num_pages, window;
+    float scale_log2;
+    const int* positions;
+    const int* table;
+    const void* sinks;      // nullptr, or [heads] of bf16
+    void* out;              // [n_tokens, heads, D]
+    char* ws;
+    PfLayout L;
+};
+
 cudaError_t launch_rope_tables(float theta, int D, int S, int dtype, void* cos_out, void* sin_out,
                                cudaStream_t stream);
 cudaError_t launch_prep(const PrepArgs& a, int dtype, cudaStream_t stream);
@@ -43,5 +71,11 @@ cudaError_t launch_prep(const PrepArgs& a, int dtype, cudaStream_t stream);
 cudaError_t launch_attend(const AttendArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
                           int dtype, int grid, bool programmatic, cudaStream_t stream);
 size_t attend_smem_bytes(int dtype, int head_dim);
+// Rope + write of every token at its slot; block 0 also builds the tile list.
+cudaError_t launch_prefill_prep(const PrefillPrepArgs& a, int dtype, cudaStream_t stream);
+// Tensor-core attention of the tiles (bf16, head dim 64 or 128).
+cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
+                           const CUtensorMap& v_map, int grid, cudaStream_t stream);
+size_t prefill_smem_bytes(int head_dim);
 
 }  // namespace pdattn

@@ -4,6 +4,8 @@
 // tables and "src/attention.linnet" (`decode`: rope on q and k at pos, then
 // `write_at` of k and v) for the write, with the paged slot of the
 // llama-3.1-8b-instruct architecture page (`decode_paged`, PageSize = 64).
+#include <climits>
+
 #include "internal.h"
 
 namespace pdattn {
@@ -117,31 +119,16 @@ __device__ __forceinline__ void rope_pair(const T* x, T* y, const T* cos_row, co
 // Prep kernel: blocks [0, rope_blocks) rotate and write one row each; the
 // last block (if plan) builds the split plan.
 // ---------------------------------------------------------------------------
+// Rotates the Hq query vectors q into q_out and the Hk key vectors kn into
+// pool slot (page, off), and copies the value vectors vn there; with
+// page_ok false only the queries.  cos_row == nullptr: plain copies.
 template <typename T>
-__device__ void rope_write_row(const PrepArgs& a, int row) {
-    Ctrl* ctrl = reinterpret_cast<Ctrl*>(a.ws + a.L.ctrl);
-    const int D = a.head_dim, half = D / 2, Hq = a.heads, Hk = a.kv_heads;
-    const int pos = __ldg(a.positions + row);
-    const bool rope = a.rope_cos != nullptr;
-    if (pos < 0 || pos >= a.pages_per_row * kPageSize || (rope && pos >= a.rope_len)) {
-        if (threadIdx.x == 0) set_error(ctrl, kErrBadPos);
-        return;
-    }
-    const int page = __ldg(a.table + (size_t)row * a.pages_per_row + pos / kPageSize);
-    const bool page_ok = page >= 0 && page < a.num_pages;
-    if (!page_ok && threadIdx.x == 0) set_error(ctrl, kErrBadPage);
-    const int off = pos % kPageSize;
-
+__device__ __forceinline__ void rope_write_vectors(const T* q, T* q_out, const T* kn, const T* vn, T* kp, T* vp,
+                                                   const T* cos_row, const T* sin_row, int Hq, int Hk, int D,
+                                                   bool page_ok, int page, int off) {
     constexpr int N = Vec16<T>::N;
-    const T* q = static_cast<const T*>(a.q) + (size_t)row * Hq * D;
-    T* q_out = static_cast<T*>(a.q_out) + (size_t)row * Hq * D;
-    const T* kn = static_cast<const T*>(a.k_new) + (size_t)row * Hk * D;
-    const T* vn = static_cast<const T*>(a.v_new) + (size_t)row * Hk * D;
-    T* kp = static_cast<T*>(a.k_pool);
-    T* vp = static_cast<T*>(a.v_pool);
-    const T* cos_row = rope ? static_cast<const T*>(a.rope_cos) + (size_t)pos * D : nullptr;
-    const T* sin_row = rope ? static_cast<const T*>(a.rope_sin) + (size_t)pos * D : nullptr;
-
+    const bool rope = cos_row != nullptr;
+    const int half = D / 2;
     const int per_head = rope ? half / N : D / N;  // work units per head vector
     const int uq = Hq * per_head, uk = Hk * per_head, uv = Hk * (D / N);
     for (int u = threadIdx.x; u < uq + uk + uv; u += blockDim.x) {
@@ -171,6 +158,29 @@ __device__ void rope_write_row(const PrepArgs& a, int row) {
                 __ldg(reinterpret_cast<const uint4*>(vn + (size_t)h * D + e0));
         }
     }
+}
+
+template <typename T>
+__device__ void rope_write_row(const PrepArgs& a, int row) {
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(a.ws + a.L.ctrl);
+    const int D = a.head_dim, Hq = a.heads, Hk = a.kv_heads;
+    const int pos = __ldg(a.positions + row);
+    const bool rope = a.rope_cos != nullptr;
+    if (pos < 0 || pos >= a.pages_per_row * kPageSize || (rope && pos >= a.rope_len)) {
+        if (threadIdx.x == 0) set_error(ctrl, kErrBadPos);
+        return;
+    }
+    const int page = __ldg(a.table + (size_t)row * a.pages_per_row + pos / kPageSize);
+    const bool page_ok = page >= 0 && page < a.num_pages;
+    if (!page_ok && threadIdx.x == 0) set_error(ctrl, kErrBadPage);
+    rope_write_vectors<T>(static_cast<const T*>(a.q) + (size_t)row * Hq * D,
+                          static_cast<T*>(a.q_out) + (size_t)row * Hq * D,
+                          static_cast<const T*>(a.k_new) + (size_t)row * Hk * D,
+                          static_cast<const T*>(a.v_new) + (size_t)row * Hk * D, static_cast<T*>(a.k_pool),
+                          static_cast<T*>(a.v_pool),
+                          rope ? static_cast<const T*>(a.rope_cos) + (size_t)pos * D : nullptr,
+                          rope ? static_cast<const T*>(a.rope_sin) + (size_t)pos * D : nullptr, Hq, Hk, D,
+                          page_ok, page, pos % kPageSize);
 }
 
 // Visible positions of a row: [lo, pos] with lo = 0 or pos - window + 1.
@@ -427,6 +437,179 @@ __global__ void __launch_bounds__(512) prep_kernel(const __grid_constant__ PrepA
 }
 
 // ---------------------------------------------------------------------------
+// Paged prefill (llama-3.1-8b-instruct page, `prefill_paged`): every packed
+// token's q and k are rotated at its own position, k and v written at its
+// slot (page * 64 + offset), and the tokens are cut into tiles for the
+// tensor-core attention: runs of consecutive tokens of one row, at most
+// tile_tokens long, listed by visible pages, largest first.
+// ---------------------------------------------------------------------------
+constexpr int kPfBuckets = 1024;     // sort buckets of tile sizes (pages, capped)
+
+// Inclusive block scan (sum, or max with kMax) of one int per thread;
+// blockDim.x a multiple of 32.  *total gets the block's sum or max.
+template <bool kMax>
+__device__ int block_scan(int v, int* s_warp, int* total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    #pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d) v = kMax ? max(v, o) : v + o;
+    }
+    if (lane == 31) s_warp[w] = v;
+    __syncthreads();
+    if (w == 0) {
+        int t = lane < nw ? s_warp[lane] : (kMax ? INT_MIN : 0);
+        #pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, t, d);
+            if (lane >= d) t = kMax ? max(t, o) : t + o;
+        }
+        if (lane < nw) s_warp[lane] = t;
+    }
+    __syncthreads();
+    if (w > 0) v = kMax ? max(v, s_warp[w - 1]) : v + s_warp[w - 1];
+    *total = s_warp[nw - 1];
+    __syncthreads();
+    return v;
+}
+
+__device__ void build_prefill_plan(const PrefillPrepArgs& a) {
+    __shared__ int s_warp[32];
+    __shared__ int s_off[kPfBuckets];
+    __shared__ int s_bad;
+    const int tid = threadIdx.x, n = a.n_tokens, Tq = a.tile_tokens;
+    const int max_pos = a.pages_per_row * kPageSize;
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(a.ws + a.L.ctrl);
+    PfTile* raw = reinterpret_cast<PfTile*>(a.ws + a.L.tiles_raw);
+    PfTile* tiles = reinterpret_cast<PfTile*>(a.ws + a.L.tiles);
+    for (int b = tid; b < kPfBuckets; b += blockDim.x) s_off[b] = 0;
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+
+    // 1. tile starts: a token starts a tile when it starts a run of its row
+    //    or lies a multiple of Tq tokens after its run's start.
+    int carry_run = 0, n_tiles = 0, bad = 0;
+    for (int base = 0; base < n; base += blockDim.x) {
+        const int i = base + tid;
+        const bool in = i < n;
+        const int r = in ? __ldg(a.row_of + i) : 0;
+        if (in) {
+            const int pos = __ldg(a.positions + i);
+            if (r < 0 || r >= a.rows || pos < 0 || pos >= max_pos || (a.rope_cos && pos >= a.rope_len))
+                bad = 1;
+        }
+        const bool run_start = in && (i == 0 || __ldg(a.row_of + i - 1) != r);
+        int last_start;
+        const int rs = block_scan<true>(run_start ? i : carry_run, s_warp, &last_start);
+        const bool tile_start = in && (i - rs) % Tq == 0;
+        int chunk_tiles;
+        const int at = block_scan<false>(tile_start ? 1 : 0, s_warp, &chunk_tiles);
+        if (tile_start) raw[n_tiles + at - 1].t0 = i;
+        carry_run = last_start;
+        n_tiles += chunk_tiles;
+    }
+    if (bad) atomicOr(&s_bad, 1);
+    __syncthreads();   // raw[].t0 visible to the block
+
+    // 2. each tile's tokens, row and visible pages; histogram of sizes
+    for (int base = 0; base < n_tiles; base += blockDim.x) {
+        const int b = base + tid;
+        int t0 = 0, t1 = 0;
+        if (b < n_tiles) {
+            t0 = raw[b].t0;
+            t1 = b + 1 < n_tiles ? raw[b + 1].t0 : n;
+        }
+        __syncthreads();   // every t0 read before any descriptor is rewritten
+        if (b < n_tiles) {
+            int lo_min = INT_MAX, pos_max = -1;
+            for (int t = t0; t < t1; ++t) {
+                int pos = __ldg(a.positions + t);
+                pos = pos < 0 ? 0 : (pos >= max_pos ? max_pos - 1 : pos);
+                lo_min = min(lo_min, row_lo(pos, a.window));
+                pos_max = max(pos_max, pos);
+            }
+            const int first = lo_min / kPageSize, npg = pos_max / kPageSize - first + 1;
+            int4* dst = reinterpret_cast<int4*>(raw + b);
+            dst[0] = make_int4(t0, t1 - t0, __ldg(a.row_of + t0), first);
+            dst[1] = make_int4(npg, lo_min, pos_max, 0);
+            atomicAdd(&s_off[npg < kPfBuckets ? npg : kPfBuckets - 1], 1);
+        }
+    }
+    __syncthreads();
+
+    // 3. counting sort, largest first: bucket kPfBuckets-1 first
+    {
+        const int per = kPfBuckets / (int)blockDim.x;   // buckets per thread (blockDim divides 1024)
+        int h[kPfBuckets / 256];
+        int sum = 0;
+        for (int k = 0; k < per; ++k) {
+            h[k] = s_off[kPfBuckets - 1 - (tid * per + k)];
+            sum += h[k];
+        }
+        int total;
+        const int inc = block_scan<false>(sum, s_warp, &total);
+        int off = inc - sum;
+        for (int k = 0; k < per; ++k) {
+            s_off[kPfBuckets - 1 - (tid * per + k)] = off;
+            off += h[k];
+        }
+    }
+    __syncthreads();
+    for (int b = tid; b < n_tiles; b += blockDim.x) {
+        const int4* src = reinterpret_cast<const int4*>(raw + b);
+        const int4 d0 = src[0], d1 = src[1];
+        const int at = atomicAdd(&s_off[d1.x < kPfBuckets ? d1.x : kPfBuckets - 1], 1);
+        int4* dst = reinterpret_cast<int4*>(tiles + at);
+        dst[0] = d0;
+        dst[1] = d1;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        if (s_bad) set_error(ctrl, kErrBadPos);
+        ctrl->n_items = s_bad ? 0 : n_tiles;
+        ctrl->kv_heads = a.kv_heads;
+        ctrl->group = a.heads / a.kv_heads;
+        ctrl->head_dim = a.head_dim;
+        ctrl->magic = kPlanMagic;
+    }
+}
+
+template <typename T>
+__device__ void rope_write_token(const PrefillPrepArgs& a, int i) {
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(a.ws + a.L.ctrl);
+    const int D = a.head_dim, Hq = a.heads, Hk = a.kv_heads;
+    const int pos = __ldg(a.positions + i);
+    const bool rope = a.rope_cos != nullptr;
+    if (pos < 0 || pos >= a.pages_per_row * kPageSize || (rope && pos >= a.rope_len)) {
+        if (threadIdx.x == 0) set_error(ctrl, kErrBadPos);
+        return;
+    }
+    const int slot = __ldg(a.slots + i);
+    const int page = slot >= 0 ? slot / kPageSize : -1;
+    const bool page_ok = page >= 0 && page < a.num_pages;
+    if (!page_ok && threadIdx.x == 0) set_error(ctrl, kErrBadPage);
+    rope_write_vectors<T>(static_cast<const T*>(a.q) + (size_t)i * Hq * D,
+                          reinterpret_cast<T*>(a.ws + a.L.q_rot) + (size_t)i * Hq * D,
+                          static_cast<const T*>(a.k_new) + (size_t)i * Hk * D,
+                          static_cast<const T*>(a.v_new) + (size_t)i * Hk * D, static_cast<T*>(a.k_pool),
+                          static_cast<T*>(a.v_pool),
+                          rope ? static_cast<const T*>(a.rope_cos) + (size_t)pos * D : nullptr,
+                          rope ? static_cast<const T*>(a.rope_sin) + (size_t)pos * D : nullptr, Hq, Hk, D,
+                          page_ok, page, slot >= 0 ? slot % kPageSize : 0);
+}
+
+// Block 0 builds the tile list; block 1 + i rotates and writes token i.
+template <typename T>
+__global__ void __launch_bounds__(512) prefill_prep_kernel(const __grid_constant__ PrefillPrepArgs a) {
+    griddep_launch_dependents();
+    if (blockIdx.x == 0) {
+        build_prefill_plan(a);
+        return;
+    }
+    rope_write_token<T>(a, blockIdx.x - 1);
+}
+
+// ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
 cudaError_t launch_rope_tables(float theta, int D, int S, int dtype, void* cos_out, void* sin_out,
@@ -451,6 +634,15 @@ cudaError_t launch_prep(const PrepArgs& a, int dtype, cudaStream_t stream) {
         prep_kernel<__nv_bfloat16><<<blocks, 512, 0, stream>>>(a);
     else
         prep_kernel<float><<<blocks, 512, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_prep(const PrefillPrepArgs& a, int dtype, cudaStream_t stream) {
+    if (a.n_tokens <= 0) return cudaSuccess;
+    if (dtype == 0)
+        prefill_prep_kernel<__nv_bfloat16><<<a.n_tokens + 1, 512, 0, stream>>>(a);
+    else
+        prefill_prep_kernel<float><<<a.n_tokens + 1, 512, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -256,3 +256,13 @@ def generate_prefill(w: PrefillWorkload, device="cpu", seed: Optional[int] = Non
     return dict(q=normal(P, Hq, D), k_new=normal(P, Hk, D), v_new=normal(P, Hk, D), positions=i32(positions),
                 rows=i32(rows), slots=i32(slots), table=table.to(device),
                 k_pool=normal(num_pages, Hk, PAGE_SIZE, D), v_pool=normal(num_pages, Hk, PAGE_SIZE, D))
+
+
+# Llama-3.1-8B attention shape, chunked prefill: 8 rows, 1024 new tokens each
+# on cached prefixes of 0, 1024, ..., 7168 positions (8192 tokens in all,
+# contexts 1 .. 8192).
+PREFILL_LLAMA = PrefillWorkload("llama8b_prefill", prefix=tuple(range(0, 8192, 1024)), chunk=(1024,) * 8,
+                                heads=32, kv_heads=8, head_dim=128, pages_per_row=128, rope_theta=500000.0,
+                                seed=1005)
+
+PREFILL_WORKLOADS = {w.name: w for w in (PREFILL_LLAMA,)}

@@ -139,3 +139,21 @@ def test_workspace_layout_bound_covers_every_plan():
         items = sum(Hk * math.ceil(x / C) for x in n)
         bound = max(items_per_cta * grid + R * Hk, R * Hk * math.ceil(Pg / chunk_max))
         assert items <= bound
+
+
+def test_prefill_host_validation(lib):
+    import torch
+    null = ctypes.c_void_p(0)
+    f = lib.lib.pdattn_prefill_paged
+    p = _p(lib, dtype=torch.float32)
+    assert f(ctypes.byref(p), 4, *([null] * 11), 0, null) == 2        # tensor-core path: bf16 only
+    p = _p(lib)
+    assert f(ctypes.byref(p), -1, *([null] * 11), 0, null) == 1
+    assert f(ctypes.byref(p), 0, *([null] * 11), 0, null) == 0         # no tokens: nothing launched
+    assert lib.lib.pdattn_last_launch_count() == 0
+    assert f(ctypes.byref(p), 4, *([null] * 11), 0, null) == 1
+    assert b"NULL" in lib.lib.pdattn_last_error()
+    # workspace: control block, two tile lists and the rotated queries
+    n = lib.lib.pdattn_prefill_workspace_size(ctypes.byref(p), 1000)
+    assert n >= 256 + 2 * 32 * 1000 + 2 * 1000 * 8 * 64 and n % 256 == 0
+    assert lib.lib.pdattn_prefill_workspace_size(ctypes.byref(p), -1) == 0
