@@ -378,17 +378,18 @@ static pdattn_status prefill_impl(const pdattn_params* p, int32_t n_tokens, cons
     if (sms <= 0) return fail(PDATTN_ECUDA, "no CUDA device");
     char* ws = static_cast<char*>(workspace);
     const int g = p->heads / p->kv_heads;
-    const int tile_tokens = kPfRows / g;
+    const int tile_tokens = 2 * (kPfRows / g);   // two halves of 128 / g tokens
 
     // Rotated queries [n_tokens, heads, D] as a 3-D tensor (D, heads, tokens):
-    // one box = the g heads of a kv head for tile_tokens tokens, 64 columns wide.
+    // one box = the g heads of a kv head for one half tile (128 / g tokens),
+    // 64 columns wide.
     auto fn = encode_fn();
     if (!fn) return fail(PDATTN_ECUDA, "cuTensorMapEncodeTiled is not available");
     CUtensorMap qm, km, vm;
     {
         cuuint64_t dims[3] = {(cuuint64_t)p->head_dim, (cuuint64_t)p->heads, (cuuint64_t)n_tokens};
         cuuint64_t strides[2] = {(cuuint64_t)p->head_dim * 2, (cuuint64_t)p->heads * p->head_dim * 2};
-        cuuint32_t box[3] = {64, (cuuint32_t)g, (cuuint32_t)tile_tokens};
+        cuuint32_t box[3] = {64, (cuuint32_t)g, (cuuint32_t)(tile_tokens / 2)};
         cuuint32_t estr[3] = {1, 1, 1};
         CUresult r = fn(&qm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ws + L.q_rot, dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

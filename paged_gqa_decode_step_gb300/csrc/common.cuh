@@ -90,7 +90,7 @@ __host__ __device__ inline WsLayout ws_layout(int rows, int heads, int kv_heads,
 // ---------------------------------------------------------------------------
 // Paged prefill: tiles of consecutive tokens of one row and the workspace.
 // ---------------------------------------------------------------------------
-constexpr int kPfRows = 128;          // MMA rows of a prefill tile: tokens x query heads of a group
+constexpr int kPfRows = 128;          // MMA rows of half a prefill tile: tokens x query heads of a group
 
 // Tokens [t0, t0 + ntok) of table row `row`; they see pages
 // [first_page, first_page + npg) of the row, positions [lo_min, pos_max].

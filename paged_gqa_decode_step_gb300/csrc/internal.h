@@ -38,7 +38,7 @@ struct AttendArgs {
 
 struct PrefillPrepArgs {
     int n_tokens, rows, heads, kv_heads, head_dim, pages_per_row, num_pages, window, rope_len;
-    int tile_tokens;        // tokens per tile: 128 / (heads / kv_heads)
+    int tile_tokens;        // tokens per tile: two halves of 128 / (heads / kv_heads)
     const void* q;          // [n_tokens, heads, D]
     const void* k_new;      // [n_tokens, kv_heads, D]
     const void* v_new;

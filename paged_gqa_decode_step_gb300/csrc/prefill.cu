@@ -7,23 +7,25 @@
 // page table, lo = 0 or pos - window + 1 (gpt-oss-20b page, sliding window),
 // with optional per-head sinks (gpt-oss-20b page, SinkAttention).
 //
-// Work unit = one tile of up to 128 / g consecutive tokens of one row times
-// one kv head.  The tile's g query heads per token stack into the 128 rows of
-// the MMA (row m = token (m / g), head kvh * g + m % g), so one K/V page read
-// serves every query of the tile.  Per page of 64 keys:
+// Work unit = one tile of up to 256 / g consecutive tokens of one row times
+// one kv head, in two halves of 128 / g tokens.  Each half's g query heads
+// per token stack into the 128 rows of an MMA (row m = token m / g, head
+// kvh * g + m % g), so one K/V page read serves 256 query rows.  Per page of
+// 64 keys and per half:
 //   S  = Q K^T      tcgen05.mma M=128 N=64 K=D, fp32 accumulator in TMEM
 //   softmax         one thread per MMA row: mask, running max, exp2, sum
 //   P               bf16 in shared memory (128-byte swizzle, K-major)
 //   O += P V        tcgen05.mma M=128 N=D K=64, V page read MN-major
-// S is double-buffered in TMEM so that S of page j+1 runs under the softmax
-// of page j.  The running max is raised lazily: O is rescaled in TMEM only
-// when a row's max grows by more than 2^8, so that most pages need no
-// round trip through the accumulator.
+// The MMA issuer interleaves the halves (S_A(j) S_B(j) PV_A(j-1) PV_B(j-1))
+// so that each half's softmax runs while the tensor core works for the
+// other; S is double-buffered per half.  The running max is raised lazily:
+// O is rescaled in TMEM only when a row's max grows by more than 2^8.
 //
-// Warps: 0 = TMA producer (Q box, K and V pages), 1 = TMEM owner and MMA
-// issuer, 2..5 = softmax and epilogue (warp w reads TMEM lanes
-// 32 * (w % 4) .. + 31).  Every wait is bounded; on a timeout the kernel sets
-// the error flag, drains its own copies and MMAs, frees TMEM and returns.
+// Warps: 0 = TMA producer (Q boxes, K and V pages), 1 = TMEM owner and MMA
+// issuer, 2..5 = softmax and epilogue of half A, 6..9 of half B (warp w
+// reads TMEM lanes 32 * (w % 4) .. + 31).  Every wait is bounded; on a
+// timeout the kernel sets the error flag, drains its own copies and MMAs,
+// frees TMEM and returns.
 #include <climits>
 
 #include "internal.h"
@@ -31,25 +33,26 @@
 namespace pdattn {
 namespace {
 
-constexpr int kPfThreads = 192;
+constexpr int kPfThreads = 320;
 constexpr uint64_t kPfTimeoutNs = 2000000000ull;
 constexpr float kRescaleLog2 = 8.0f;    // lazy rescale threshold (log2 units)
 
 template <int D>
 struct PfCfg {
     static constexpr int kBoxes = D / 64;                 // 64-element column boxes
-    static constexpr int kQBytes = kBoxes * 16384;        // 128 rows x 128 B per box
+    static constexpr int kQBytes = kBoxes * 16384;        // one half: 128 rows x 128 B per box
     static constexpr int kKvBytes = kBoxes * 8192;        // one page of K (or V): 64 rows x 128 B per box
     static constexpr int kStageBytes = 2 * kKvBytes;
     static constexpr int kStages = D == 128 ? 4 : 8;
-    static constexpr int kPBytes = 16384;                 // 128 rows x 64 bf16
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffStage = kQBytes;
+    static constexpr int kPBytes = 16384;                 // 128 rows x 64 bf16, one per half
+    static constexpr int kOffQ = 0;                       // halves A, B
+    static constexpr int kOffStage = 2 * kQBytes;
     static constexpr int kOffP = kOffStage + kStages * kStageBytes;
     static constexpr int kSmem = kOffP + 2 * kPBytes + 1024;   // + alignment slack
-    static constexpr uint32_t kTmemCols = 256;            // S0 [0,64)  S1 [64,128)  O [128,128+D)
-    static constexpr uint32_t kColO = 128;
-    static_assert(kSmem <= 227 * 1024, "shared memory budget");
+    // TMEM: S of half h, buffer b at column 128 h + 64 b; O of half h at 256 + h D.
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kColO = 256;
+    static_assert(kSmem <= 227 * 1024 - 2048, "shared memory budget");
 };
 
 // --- tcgen05 / TMA wrappers ---------------------------------------------------
@@ -73,19 +76,42 @@ __host__ __device__ constexpr uint32_t instr_desc(int M, int N, int a_mn, int b_
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The issuing warps run their loops with all 32 lanes (warp-uniform control
+// flow and operands); each of these instructions is issued once, by the lane
+// elect.sync picks.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                           uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
-// The barrier arrives once every MMA issued so far by this thread is done.
+// The barrier arrives once every MMA issued so far by this warp is done.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+        ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void elect_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}"
+        ::"r"(bar), "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ void elect_tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];\n\t}"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -123,13 +149,37 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
-                                            uint32_t bar) {
+__device__ __forceinline__ void elect_tma_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                             uint32_t bar) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];"
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];\n\t}"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
+}
+
+// Warp-wide bounded wait: every lane polls, and the warp agrees on the result.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, Ctrl* ctrl);
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Max of 64 values as eight short independent chains.
+__device__ __forceinline__ float max64(const uint32_t (&s)[64]) {
+    float acc[8];
+    #pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float* v = reinterpret_cast<const float*>(&s[8 * k]);
+        float x = fmax3(v[0], v[1], v[2]);
+        x = fmax3(x, v[3], v[4]);
+        x = fmax3(x, v[5], v[6]);
+        acc[k] = fmaxf(x, v[7]);
+    }
+    return fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
 }
 
 // Bounded wait that also gives up once another role has aborted.
@@ -153,9 +203,179 @@ __device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, volatile 
     }
 }
 
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, Ctrl* ctrl) {
+    return __all_sync(0xffffffffu, pf_wait(bar, parity, abort, ctrl));
+}
+
+// Broadcast of lane 0's value: the loops of the issuing warps stay uniform.
+__device__ __forceinline__ int uni(int v) { return __shfl_sync(0xffffffffu, v, 0); }
+
 struct PfBars {
-    uint64_t q_full, q_empty, s_full[2], p_full[2], pv_done[2], mma_done;
+    uint64_t q_full, q_empty, mma_done;
+    uint64_t s_full[2][2];   // [half][S buffer]
+    uint64_t p_full[2];      // [half]: P written (128 arrivals)
+    uint64_t pv_done[2];     // [half]: O += P V finished
 };
+
+// Softmax and epilogue of one half (128 threads, one MMA row each).
+template <int D>
+__device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile* tiles, int n_units, int half,
+                                             int quarter, int lane, uint32_t tmem, uint32_t st_s, uint32_t p_s,
+                                             PfBars& bars, volatile int* abort, Ctrl* ctrl) {
+    using C = PfCfg<D>;
+    const int Hk = a.kv_heads, g = a.group, Tq = a.tile_tokens / 2;
+    const int m = quarter * 32 + lane;                    // MMA row = TMEM lane
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const uint32_t s_col = 128u * half, o_col = C::kColO + (uint32_t)(half * D);
+    const uint32_t pb = p_s + half * C::kPBytes;
+    const int tq = m / g, jh = m % g;
+    const float sl2 = a.scale_log2;
+    const __nv_bfloat16* sinks = static_cast<const __nv_bfloat16*>(a.sinks);
+    const uint32_t p_full = smem_u32(&bars.p_full[half]), pv_done = smem_u32(&bars.pv_done[half]);
+    uint32_t it = 0, ch = 0;     // pages of every unit / of units with this half
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const PfTile t = tiles[u / Hk];
+        const int kvh = u % Hk;
+        const bool present = half == 0 || t.ntok > Tq;
+        if (!present) {
+            it += t.npg;
+            continue;
+        }
+        const int tok = half * Tq + tq;                   // token of this row within the tile
+        const bool active = tq < Tq && tok < t.ntok;
+        int pos = -1, lo = 0;
+        if (active) {
+            pos = __ldg(a.positions + t.t0 + tok);
+            pos = pos < 0 ? 0 : pos;
+            lo = (a.window > 0 && pos - a.window + 1 > 0) ? pos - a.window + 1 : 0;
+        }
+        float m_run = -INFINITY, l = 0.f;
+        for (int k = 0; k < t.npg; ++k) {
+            const uint32_t j = ch + k;
+            const int pg = t.first_page + k;
+            ok = pf_wait(smem_u32(&bars.s_full[half][j & 1]), (j >> 1) & 1, abort, ctrl);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t s[64];
+            tmem_ld32(tmem + lane_base + s_col + (j & 1) * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+            tmem_ld32(tmem + lane_base + s_col + (j & 1) * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+            tmem_wait_ld();
+            // keys c of this page visible to the row: lo <= pg*64 + c <= pos
+            const int c_lo = lo - pg * kPageSize, c_hi = pos - pg * kPageSize;
+            if (!__all_sync(0xffffffffu, c_lo <= 0 && c_hi >= kPageSize - 1)) {
+                #pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (c < c_lo || c > c_hi) s[c] = __float_as_uint(-INFINITY);
+            }
+            const float mx = max64(s) * sl2;               // scale > 0: the max commutes with it
+            const bool need = mx > m_run + kRescaleLog2;
+            float alpha = 1.f;
+            if (need) {
+                alpha = exp2_approx(m_run - mx);           // 0 while m_run is -inf
+                m_run = mx;
+                l *= alpha;
+            }
+            const float neg_mu = m_run == -INFINITY ? 0.f : -m_run;
+            // The denominator sums the bf16 weights the PV MMA multiplies,
+            // so the normalised weights are an exact convex combination.
+            uint32_t pk[32];
+            float acc[8];
+            #pragma unroll
+            for (int c = 0; c < 64; c += 2) {
+                pk[c >> 1] = pack_bf16x2(exp2_approx(fmaf(__uint_as_float(s[c]), sl2, neg_mu)),
+                                         exp2_approx(fmaf(__uint_as_float(s[c + 1]), sl2, neg_mu)));
+                const float lo_w = __uint_as_float(pk[c >> 1] << 16), hi_w = __uint_as_float(pk[c >> 1] & 0xffff0000u);
+                const int k = (c >> 1) & 7;
+                acc[k] = c < 16 ? lo_w + hi_w : acc[k] + (lo_w + hi_w);
+            }
+            l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+            // PV of this half's previous page is done: O may be rescaled and
+            // the P buffer is free.
+            if (j > 0) {
+                ok = pf_wait(pv_done, (j - 1) & 1, abort, ctrl);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+            }
+            if (k > 0 && __any_sync(0xffffffffu, need && alpha != 1.f)) {
+                #pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tmem + lane_base + o_col + c0, o);
+                    tmem_wait_ld();
+                    #pragma unroll
+                    for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                    tmem_st32(tmem + lane_base + o_col + c0, o);
+                }
+                tmem_wait_st();
+            }
+            #pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8)
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                             ::"r"(swz128(pb, m, c8)), "r"(pk[4 * c8]), "r"(pk[4 * c8 + 1]), "r"(pk[4 * c8 + 2]),
+                               "r"(pk[4 * c8 + 3])
+                             : "memory");
+            // V rows outside every row's range hold no cached value of this
+            // tile (possibly stale or non-finite): half A zeroes them so that
+            // 0 * V stays 0 (the issuer runs PV_B after PV_A).
+            const int v_lo = t.lo_min - pg * kPageSize, v_hi = t.pos_max - pg * kPageSize;
+            if (half == 0 && (v_lo > 0 || v_hi < kPageSize - 1)) {
+                const uint32_t vb = st_s + ((it + k) % C::kStages) * C::kStageBytes + C::kKvBytes;
+                for (int i = m; i < kPageSize * C::kBoxes * 8; i += 128) {
+                    const int r = i / (C::kBoxes * 8), rest = i % (C::kBoxes * 8);
+                    if (r < v_lo || r > v_hi)
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};"
+                                     ::"r"(vb + (rest >> 3) * 8192 + r * 128 + (rest & 7) * 16), "r"(0)
+                                     : "memory");
+                }
+            }
+            fence_proxy_async_shared();
+            tc_fence_before();
+            mbar_arrive(p_full);
+        }
+        if (!ok) break;
+        // Epilogue: O / l (with the sink's share of the denominator).
+        const uint32_t jl = ch + t.npg - 1;
+        ok = pf_wait(pv_done, jl & 1, abort, ctrl);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const int h = kvh * g + jh;
+        float inv = l > 0.f ? 1.f / l : 0.f;
+        if (sinks != nullptr && active) {
+            const float sk = __bfloat162float(sinks[h]) * 1.4426950408889634f;
+            const float mu = m_run == -INFINITY ? sk : m_run;
+            const float Mp = fmaxf(mu, sk);
+            const float f = exp2_approx(mu - Mp);
+            inv = f / (l * f + exp2_approx(sk - Mp));
+        }
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + ((size_t)(t.t0 + tok) * a.heads + h) * D;
+        #pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_base + o_col + c0, o);
+            tmem_wait_ld();
+            if (active) {
+                #pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+                    w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+                    w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+                    w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+                    *reinterpret_cast<uint4*>(orow + c0 + 8 * v) = w;
+                }
+            }
+        }
+        // The next unit's first PV overwrites O only after this read (its
+        // p_full arrival follows in program order).
+        tc_fence_before();
+        ch += t.npg;
+        it += t.npg;
+    }
+}
 
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1)
@@ -176,8 +396,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(a.ws + a.L.ctrl);
     volatile int* abort = &s_abort;
 
-    // Rows of the Q tile that no token fills stay zero.
-    for (int i = tid; i < C::kQBytes / 16; i += kPfThreads)
+    // Rows of the Q tiles that no token fills stay zero.
+    for (int i = tid; i < 2 * C::kQBytes / 16; i += kPfThreads)
         reinterpret_cast<uint4*>(sm + C::kOffQ)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -186,12 +406,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         mbar_init(smem_u32(&bars.q_full), 1);
         mbar_init(smem_u32(&bars.q_empty), 1);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&bars.s_full[b]), 1);
-            mbar_init(smem_u32(&bars.p_full[b]), 128);
-            mbar_init(smem_u32(&bars.pv_done[b]), 1);
-        }
         mbar_init(smem_u32(&bars.mma_done), 1);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(smem_u32(&bars.s_full[h][0]), 1);
+            mbar_init(smem_u32(&bars.s_full[h][1]), 1);
+            mbar_init(smem_u32(&bars.p_full[h]), 128);
+            mbar_init(smem_u32(&bars.pv_done[h]), 1);
+        }
         s_abort = 0;
         fence_barrier_init();
         prefetch_tensormap(&q_map);
@@ -211,243 +432,123 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
     // Everything below reads what the prep kernel wrote.
     griddep_wait();
-    const int Hk = a.kv_heads, g = a.group, Tq = a.tile_tokens;
+    const int Hk = a.kv_heads, g = a.group, Tq = a.tile_tokens / 2;
     const int n_units = (ctrl->magic == kPlanMagic ? ctrl->n_items : 0) * Hk;
     const PfTile* tiles = reinterpret_cast<const PfTile*>(a.ws + a.L.tiles);
 
     if (warp == 0) {
-        // ---------------- TMA producer ----------------
-        if (lane == 0) {
-            uint32_t it = 0, ui = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ui) {
-                const PfTile t = tiles[u / Hk];
-                const int kvh = u % Hk;
-                ok = pf_wait(smem_u32(&bars.q_empty), (ui & 1) ^ 1, abort, ctrl);
-                if (!ok) break;
-                mbar_arrive_expect_tx(smem_u32(&bars.q_full), C::kBoxes * 128 * g * Tq);
-                for (int b = 0; b < C::kBoxes; ++b)
-                    tma_load_3d(q_s + b * 16384, &q_map, b * 64, kvh * g, t.t0, smem_u32(&bars.q_full));
-                const int* trow = a.table + (size_t)t.row * a.pages_per_row;
-                for (int k = 0; k < t.npg; ++k, ++it) {
-                    const int s = it % C::kStages;
-                    ok = pf_wait(smem_u32(&kv_empty[s]), ((it / C::kStages) & 1) ^ 1, abort, ctrl);
-                    if (!ok) break;
-                    int page = __ldg(trow + t.first_page + k);
-                    if (page < 0 || page >= a.num_pages) {
-                        set_error(ctrl, kErrBadPage);
-                        page = 0;
-                    }
-                    const int y = (page * Hk + kvh) * kPageSize;
-                    const uint32_t kb = st_s + s * C::kStageBytes, vb = kb + C::kKvBytes;
-                    mbar_arrive_expect_tx(smem_u32(&kv_full[s]), C::kStageBytes);
-                    for (int b = 0; b < C::kBoxes; ++b) {
-                        tma_load_2d(kb + b * 8192, &k_map, b * 64, y, smem_u32(&kv_full[s]));
-                        tma_load_2d(vb + b * 8192, &v_map, b * 64, y, smem_u32(&kv_full[s]));
-                    }
-                }
-            }
-            // Drain: the last load of each stage and of Q has landed before exit.
-            for (uint32_t k = 0; k < (uint32_t)C::kStages && k < it; ++k) {
-                const uint32_t j = it - 1 - k;
-                mbar_wait(smem_u32(&kv_full[j % C::kStages]), (j / C::kStages) & 1, kPfTimeoutNs);
-            }
-            if (ui > 0) mbar_wait(smem_u32(&bars.q_full), (ui - 1) & 1, kPfTimeoutNs);
-        }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = instr_desc(128, 64, 0, 0);
-            constexpr uint32_t idesc_o = instr_desc(128, D, 0, 1);
-            uint32_t it = 0, ui = 0;
-            bool ok = true;
-            // O += P_j V_j; the first page of a unit overwrites O.
-            auto pv = [&](uint32_t j, bool first) -> bool {
-                if (!pf_wait(smem_u32(&bars.p_full[j & 1]), (j >> 1) & 1, abort, ctrl)) return false;
-                tc_fence_after();
-                const uint32_t vb = st_s + (j % C::kStages) * C::kStageBytes + C::kKvBytes;
-                const uint32_t pb = p_s + (j & 1) * C::kPBytes;
-                #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    umma_bf16(tmem + C::kColO, smem_desc(pb + ks * 32, 16, 1024),
-                              smem_desc(vb + ks * 2048, 8192, 1024), idesc_o, (first && ks == 0) ? 0u : 1u);
-                umma_commit(smem_u32(&bars.pv_done[j & 1]));
-                umma_commit(smem_u32(&kv_empty[j % C::kStages]));
-                return true;
-            };
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ui) {
-                const PfTile t = tiles[u / Hk];
-                ok = pf_wait(smem_u32(&bars.q_full), ui & 1, abort, ctrl);
-                if (!ok) break;
-                tc_fence_after();
-                for (int k = 0; k < t.npg && ok; ++k) {
-                    const uint32_t j = it + k;
-                    const int s = j % C::kStages;
-                    ok = pf_wait(smem_u32(&kv_full[s]), (j / C::kStages) & 1, abort, ctrl);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t kb = st_s + s * C::kStageBytes;
-                    #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks)
-                        umma_bf16(tmem + (j & 1) * 64, smem_desc(q_s + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                                  smem_desc(kb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), idesc_s,
-                                  ks > 0 ? 1u : 0u);
-                    umma_commit(smem_u32(&bars.s_full[j & 1]));
-                    if (k > 0) ok = pv(j - 1, k == 1);
-                }
-                if (!ok) break;
-                umma_commit(smem_u32(&bars.q_empty));      // Q is free once every S of the unit is done
-                ok = pv(it + t.npg - 1, t.npg == 1);
-                it += t.npg;
-            }
-            // Drain: every MMA issued has finished before TMEM is freed.
-            if (ui > 0) {
-                umma_commit(smem_u32(&bars.mma_done));
-                mbar_wait(smem_u32(&bars.mma_done), 0, kPfTimeoutNs);
-            }
-        }
-    } else {
-        // ---------------- softmax + epilogue (warps 2..5) ----------------
-        const int quarter = warp & 3;
-        const int m = quarter * 32 + lane;           // MMA row = TMEM lane
-        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-        const int tq = m / g, jh = m % g;
-        const float sl2 = a.scale_log2;
-        const __nv_bfloat16* sinks = static_cast<const __nv_bfloat16*>(a.sinks);
-        uint32_t it = 0;
+        // ---------------- TMA producer (whole warp, one lane issues) ----------------
+        uint32_t it = 0, ui = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ui) {
             const PfTile t = tiles[u / Hk];
-            const int kvh = u % Hk;
-            const bool active = tq < Tq && tq < t.ntok;
-            int pos = -1, lo = 0;
-            if (active) {
-                pos = __ldg(a.positions + t.t0 + tq);
-                pos = pos < 0 ? 0 : pos;
-                lo = (a.window > 0 && pos - a.window + 1 > 0) ? pos - a.window + 1 : 0;
-            }
-            float m_run = -INFINITY, l = 0.f;
-            for (int k = 0; k < t.npg; ++k) {
-                const uint32_t j = it + k;
-                const int pg = t.first_page + k;
-                ok = pf_wait(smem_u32(&bars.s_full[j & 1]), (j >> 1) & 1, abort, ctrl);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                tc_fence_after();
-                uint32_t s[64];
-                tmem_ld32(tmem + lane_base + (j & 1) * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-                tmem_ld32(tmem + lane_base + (j & 1) * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-                tmem_wait_ld();
-                // keys c of this page visible to the row: lo <= pg*64 + c <= pos
-                const int c_lo = lo - pg * kPageSize, c_hi = pos - pg * kPageSize;
-                float x[64];
-                float mx = -INFINITY;
-                #pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    x[c] = (c >= c_lo && c <= c_hi) ? __uint_as_float(s[c]) * sl2 : -INFINITY;
-                    mx = fmaxf(mx, x[c]);
-                }
-                const bool need = mx > m_run + kRescaleLog2;
-                float alpha = 1.f;
-                if (need) {
-                    alpha = exp2_approx(m_run - mx);   // 0 while m_run is -inf
-                    m_run = mx;
-                    l *= alpha;
-                }
-                const float mu = m_run == -INFINITY ? 0.f : m_run;
-                uint32_t pk[32];
-                float sum = 0.f;
-                // The denominator sums the bf16 weights the PV MMA multiplies,
-                // so the normalised weights are an exact convex combination.
-                #pragma unroll
-                for (int c = 0; c < 64; c += 2) {
-                    pk[c >> 1] = pack_bf16x2(exp2_approx(x[c] - mu), exp2_approx(x[c + 1] - mu));
-                    const float2 r = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[c >> 1]));
-                    sum += r.x + r.y;
-                }
-                l += sum;
-                // PV of the previous page is done: O may be rescaled, P buffer j&1 is free.
-                if (j > 0) {
-                    ok = pf_wait(smem_u32(&bars.pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, abort, ctrl);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-                if (k > 0 && __any_sync(0xffffffffu, need && alpha != 1.f)) {
-                    #pragma unroll 1
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(tmem + lane_base + C::kColO + c0, o);
-                        tmem_wait_ld();
-                        #pragma unroll
-                        for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                        tmem_st32(tmem + lane_base + C::kColO + c0, o);
-                    }
-                    tmem_wait_st();
-                }
-                const uint32_t pb = p_s + (j & 1) * C::kPBytes;
-                #pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                                 ::"r"(swz128(pb, m, ch)), "r"(pk[4 * ch]), "r"(pk[4 * ch + 1]),
-                                   "r"(pk[4 * ch + 2]), "r"(pk[4 * ch + 3])
-                                 : "memory");
-                // V rows outside every row's range hold no cached value of this
-                // tile (possibly stale or non-finite): zero them so 0 * V stays 0.
-                const int v_lo = t.lo_min - pg * kPageSize, v_hi = t.pos_max - pg * kPageSize;
-                if (v_lo > 0 || v_hi < kPageSize - 1) {
-                    const uint32_t vb = st_s + (j % C::kStages) * C::kStageBytes + C::kKvBytes;
-                    for (int i = m; i < kPageSize * C::kBoxes * 8; i += 128) {
-                        const int r = i / (C::kBoxes * 8), rest = i % (C::kBoxes * 8);
-                        if (r < v_lo || r > v_hi)
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};"
-                                         ::"r"(vb + (rest >> 3) * 8192 + r * 128 + (rest & 7) * 16), "r"(0)
-                                         : "memory");
-                    }
-                }
-                fence_proxy_async_shared();
-                tc_fence_before();
-                mbar_arrive(smem_u32(&bars.p_full[j & 1]));
-            }
+            const int kvh = u % Hk, nh = uni(t.ntok > Tq ? 2 : 1), npg = uni(t.npg), t0 = uni(t.t0);
+            const int first = uni(t.first_page), row = uni(t.row);
+            ok = warp_wait(smem_u32(&bars.q_empty), (ui & 1) ^ 1, abort, ctrl);
             if (!ok) break;
-            // Epilogue: O / l (with the sink's share of the denominator).
-            const uint32_t jl = it + t.npg - 1;
-            ok = pf_wait(smem_u32(&bars.pv_done[jl & 1]), (jl >> 1) & 1, abort, ctrl);
-            ok = __all_sync(0xffffffffu, ok);
+            elect_arrive_expect_tx(smem_u32(&bars.q_full), nh * C::kBoxes * 128 * g * Tq);
+            for (int h = 0; h < nh; ++h)
+                for (int b = 0; b < C::kBoxes; ++b)
+                    elect_tma_3d(q_s + h * C::kQBytes + b * 16384, &q_map, b * 64, kvh * g, t0 + h * Tq,
+                                 smem_u32(&bars.q_full));
+            const int* trow = a.table + (size_t)row * a.pages_per_row + first;
+            for (int k = 0; k < npg; ++k, ++it) {
+                const int s = it % C::kStages;
+                ok = warp_wait(smem_u32(&kv_empty[s]), ((it / C::kStages) & 1) ^ 1, abort, ctrl);
+                if (!ok) break;
+                int page = uni(__ldg(trow + k));
+                if (page < 0 || page >= a.num_pages) {
+                    if (lane == 0) set_error(ctrl, kErrBadPage);
+                    page = 0;
+                }
+                const int y = (page * Hk + kvh) * kPageSize;
+                const uint32_t kb = st_s + s * C::kStageBytes, vb = kb + C::kKvBytes;
+                elect_arrive_expect_tx(smem_u32(&kv_full[s]), C::kStageBytes);
+                for (int b = 0; b < C::kBoxes; ++b) {
+                    elect_tma_2d(kb + b * 8192, &k_map, b * 64, y, smem_u32(&kv_full[s]));
+                    elect_tma_2d(vb + b * 8192, &v_map, b * 64, y, smem_u32(&kv_full[s]));
+                }
+            }
+        }
+        // Drain: the last load of each stage and of Q has landed before exit.
+        for (uint32_t k = 0; k < (uint32_t)C::kStages && k < it; ++k) {
+            const uint32_t j = it - 1 - k;
+            mbar_wait(smem_u32(&kv_full[j % C::kStages]), (j / C::kStages) & 1, kPfTimeoutNs);
+        }
+        if (ui > 0) mbar_wait(smem_u32(&bars.q_full), (ui - 1) & 1, kPfTimeoutNs);
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (whole warp, one lane issues) ----------------
+        constexpr uint32_t idesc_s = instr_desc(128, 64, 0, 0);
+        constexpr uint32_t idesc_o = instr_desc(128, D, 0, 1);
+        uint32_t it = 0, ui = 0, cnt0 = 0, cnt1 = 0;
+        bool ok = true;
+        // Descriptors are built once: the start-address field (bits 0..13,
+        // address >> 4) is linear, so every operand below is a base
+        // descriptor plus a constant.
+        const uint64_t dq = smem_desc(q_s, 16, 1024), dk = smem_desc(st_s, 16, 1024);
+        const uint64_t dp = smem_desc(p_s, 16, 1024), dv = smem_desc(st_s + C::kKvBytes, 8192, 1024);
+        // S_h(j) = Q_h K^T into S buffer j & 1 of half h (K of stage s).
+        auto qk = [&](int h, uint32_t j, int s) {
+            const uint64_t a0 = dq + (uint64_t)(h * (C::kQBytes >> 4));
+            const uint64_t b0 = dk + (uint64_t)(s * (C::kStageBytes >> 4));
+            const uint32_t d = tmem + 128u * h + (j & 1) * 64;
+            #pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                umma_bf16(d, a0 + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
+                          b0 + (uint64_t)((ks >> 2) * 512 + (ks & 3) * 2), idesc_s, ks > 0 ? 1u : 0u);
+            umma_commit(smem_u32(&bars.s_full[h][j & 1]));
+        };
+        // O_h += P_h V (V of stage s); the first page of a unit overwrites O_h.
+        auto pv = [&](int h, uint32_t j, int s, bool first) -> bool {
+            if (!warp_wait(smem_u32(&bars.p_full[h]), j & 1, abort, ctrl)) return false;
+            tc_fence_after();
+            const uint64_t a0 = dp + (uint64_t)(h * (C::kPBytes >> 4));
+            const uint64_t b0 = dv + (uint64_t)(s * (C::kStageBytes >> 4));
+            const uint32_t d = tmem + C::kColO + h * D;
+            #pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_bf16(d, a0 + (uint64_t)(ks * 2), b0 + (uint64_t)(ks * 128), idesc_o,
+                          (first && ks == 0) ? 0u : 1u);
+            umma_commit(smem_u32(&bars.pv_done[h]));
+            return true;
+        };
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ui) {
+            const PfTile t = tiles[u / Hk];
+            const int nh = uni(t.ntok > Tq ? 2 : 1), npg = uni(t.npg);
+            ok = warp_wait(smem_u32(&bars.q_full), ui & 1, abort, ctrl);
             if (!ok) break;
             tc_fence_after();
-            const int h = kvh * g + jh;
-            float inv = l > 0.f ? 1.f / l : 0.f;
-            if (sinks != nullptr && active) {
-                const float sk = __bfloat162float(sinks[h]) * 1.4426950408889634f;
-                const float mu = m_run == -INFINITY ? sk : m_run;
-                const float Mp = fmaxf(mu, sk);
-                const float f = exp2_approx(mu - Mp);
-                inv = f / (l * f + exp2_approx(sk - Mp));
-            }
-            __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + ((size_t)(t.t0 + tq) * a.heads + h) * D;
-            #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_base + C::kColO + c0, o);
-                tmem_wait_ld();
-                if (active) {
-                    #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-                        *reinterpret_cast<uint4*>(orow + c0 + 8 * v) = w;
-                    }
+            for (int k = 0; k <= npg && ok; ++k) {
+                const uint32_t j = it + k;
+                if (k < npg) {
+                    const int s = j % C::kStages;
+                    ok = warp_wait(smem_u32(&kv_full[s]), (j / C::kStages) & 1, abort, ctrl);
+                    if (!ok) break;
+                    tc_fence_after();
+                    qk(0, cnt0 + k, s);
+                    if (nh == 2) qk(1, cnt1 + k, s);
+                    if (k == npg - 1) umma_commit(smem_u32(&bars.q_empty));   // every S of the unit issued
+                }
+                if (k > 0) {
+                    const int sp = (j - 1) % C::kStages;
+                    ok = pv(0, cnt0 + k - 1, sp, k == 1);
+                    if (ok && nh == 2) ok = pv(1, cnt1 + k - 1, sp, k == 1);
+                    if (!ok) break;
+                    umma_commit(smem_u32(&kv_empty[sp]));
                 }
             }
-            // The next unit's first PV overwrites O only after this read
-            // (its p_full arrival follows in program order).
-            tc_fence_before();
-            it += t.npg;
+            it += npg;
+            cnt0 += npg;
+            if (nh == 2) cnt1 += npg;
         }
+        // Drain: every MMA issued has finished before TMEM is freed.
+        if (ui > 0) {
+            umma_commit(smem_u32(&bars.mma_done));
+            mbar_wait(smem_u32(&bars.mma_done), 0, kPfTimeoutNs);
+        }
+    } else {
+        // ---------------- softmax + epilogue: warps 2..5 half A, 6..9 half B ----------------
+        softmax_half<D>(a, tiles, n_units, (warp - 2) >> 2, warp & 3, lane, tmem, st_s, p_s, bars, abort, ctrl);
     }
 
     tc_fence_before();
