@@ -427,8 +427,8 @@ static pdattn_status prefill_impl(const pdattn_params* p, int32_t n_tokens, cons
         pa.ws = ws;
         pa.L = L;
         cudaError_t e = launch_prefill_prep(pa, p->dtype, (cudaStream_t)stream);
-        if (e != cudaSuccess) return cuda_fail(e, "prefill rope/write/tile launch");
-        ++launches;
+        if (e != cudaSuccess) return cuda_fail(e, "prefill tile/rope/write launch");
+        launches += 2;
     }
 
     PrefillArgs aa = {};

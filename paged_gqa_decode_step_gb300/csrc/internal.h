@@ -71,7 +71,8 @@ cudaError_t launch_prep(const PrepArgs& a, int dtype, cudaStream_t stream);
 cudaError_t launch_attend(const AttendArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
                           int dtype, int grid, bool programmatic, cudaStream_t stream);
 size_t attend_smem_bytes(int dtype, int head_dim);
-// Rope + write of every token at its slot; block 0 also builds the tile list.
+// The tile list (one block), then the rope + write of every token at its
+// slot (programmatic launch that ends after the tile list): two launches.
 cudaError_t launch_prefill_prep(const PrefillPrepArgs& a, int dtype, cudaStream_t stream);
 // Tensor-core attention of the tiles (bf16, head dim 64 or 128).
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,

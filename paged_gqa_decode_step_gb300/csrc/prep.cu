@@ -445,20 +445,22 @@ __global__ void __launch_bounds__(512) prep_kernel(const __grid_constant__ PrepA
 // ---------------------------------------------------------------------------
 constexpr int kPfBuckets = 1024;     // sort buckets of tile sizes (pages, capped)
 
-// Inclusive block scan (sum, or max with kMax) of one int per thread;
-// blockDim.x a multiple of 32.  *total gets the block's sum or max.
+// Exclusive block scan (sum, or max with kMax) of one int per thread, with
+// `identity` before the first thread; blockDim.x a multiple of 32.  *total
+// gets the block's sum or max.
 template <bool kMax>
-__device__ int block_scan(int v, int* s_warp, int* total) {
+__device__ int block_scan_excl(int v, int identity, int* s_warp, int* total) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
     #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, v, d);
-        if (lane >= d) v = kMax ? max(v, o) : v + o;
+        const int o = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x = kMax ? max(x, o) : x + o;
     }
-    if (lane == 31) s_warp[w] = v;
+    if (lane == 31) s_warp[w] = x;
     __syncthreads();
     if (w == 0) {
-        int t = lane < nw ? s_warp[lane] : (kMax ? INT_MIN : 0);
+        int t = lane < nw ? s_warp[lane] : identity;
         #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
             const int o = __shfl_up_sync(0xffffffffu, t, d);
@@ -467,11 +469,20 @@ __device__ int block_scan(int v, int* s_warp, int* total) {
         if (lane < nw) s_warp[lane] = t;
     }
     __syncthreads();
-    if (w > 0) v = kMax ? max(v, s_warp[w - 1]) : v + s_warp[w - 1];
+    int up = __shfl_up_sync(0xffffffffu, x, 1);
+    if (lane == 0) up = identity;
+    const int pre = w > 0 ? s_warp[w - 1] : identity;
+    const int ex = kMax ? max(pre, up) : pre + up;
     *total = s_warp[nw - 1];
     __syncthreads();
-    return v;
+    return ex;
 }
+
+// One block of kPrepThreads threads; each thread holds kPerThread
+// consecutive tokens in registers, so a pass over up to
+// kPrepThreads * kPerThread tokens costs one global round trip.
+constexpr int kPrepThreads = 256;
+constexpr int kPerThread = 32;
 
 __device__ void build_prefill_plan(const PrefillPrepArgs& a) {
     __shared__ int s_warp[32];
@@ -487,68 +498,109 @@ __device__ void build_prefill_plan(const PrefillPrepArgs& a) {
     __syncthreads();
 
     // 1. tile starts: a token starts a tile when it starts a run of its row
-    //    or lies a multiple of Tq tokens after its run's start.
-    int carry_run = 0, n_tiles = 0, bad = 0;
-    for (int base = 0; base < n; base += blockDim.x) {
-        const int i = base + tid;
-        const bool in = i < n;
-        const int r = in ? __ldg(a.row_of + i) : 0;
-        if (in) {
-            const int pos = __ldg(a.positions + i);
-            if (r < 0 || r >= a.rows || pos < 0 || pos >= max_pos || (a.rope_cos && pos >= a.rope_len))
-                bad = 1;
+    //    or lies a multiple of Tq tokens after its run's start; each tile's
+    //    visible positions [lo_min, pos_max] by atomics on its descriptor.
+    int carry_run = 0, n_tiles = 0;
+    bool bad = false;
+    for (int base = 0; base < n; base += kPrepThreads * kPerThread) {
+        const int i0 = base + tid * kPerThread;
+        int r[kPerThread], ps[kPerThread];
+        #pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+            const int i = i0 + k;
+            r[k] = i < n ? __ldg(a.row_of + i) : -1;
+            ps[k] = i < n ? __ldg(a.positions + i) : 0;
         }
-        const bool run_start = in && (i == 0 || __ldg(a.row_of + i - 1) != r);
-        int last_start;
-        const int rs = block_scan<true>(run_start ? i : carry_run, s_warp, &last_start);
-        const bool tile_start = in && (i - rs) % Tq == 0;
+        const int r_before = (i0 > 0 && i0 < n) ? __ldg(a.row_of + i0 - 1) : -1;
+        unsigned run_starts = 0;
+        int last_start = -1;
+        #pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+            const int i = i0 + k;
+            if (i >= n) continue;
+            if (r[k] < 0 || r[k] >= a.rows || ps[k] < 0 || ps[k] >= max_pos || (a.rope_cos && ps[k] >= a.rope_len))
+                bad = true;
+            if (i == 0 || r[k] != (k ? r[k - 1] : r_before)) {
+                run_starts |= 1u << k;
+                last_start = i;
+            }
+        }
+        int block_last;
+        int rs = block_scan_excl<true>(last_start, -1, s_warp, &block_last);
+        rs = max(rs, carry_run);
+        unsigned tile_starts = 0;
+        #pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+            const int i = i0 + k;
+            if (i >= n) continue;
+            if (run_starts >> k & 1) rs = i;
+            if ((i - rs) % Tq == 0) tile_starts |= 1u << k;
+        }
         int chunk_tiles;
-        const int at = block_scan<false>(tile_start ? 1 : 0, s_warp, &chunk_tiles);
-        if (tile_start) raw[n_tiles + at - 1].t0 = i;
-        carry_run = last_start;
+        const int first_id = n_tiles + block_scan_excl<false>(__popc(tile_starts), 0, s_warp, &chunk_tiles);
+        int id = first_id;
+        #pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+            if (tile_starts >> k & 1) {
+                int4* dst = reinterpret_cast<int4*>(raw + id);
+                dst[0] = make_int4(i0 + k, 0, r[k], 0);
+                dst[1] = make_int4(0, INT_MAX, -1, 0);
+                ++id;
+            }
+        }
+        __syncthreads();   // descriptors initialised before the atomics below
+        int cur = first_id - 1, lmin = INT_MAX, pmax = -1;
+        #pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+            const int i = i0 + k;
+            if (i >= n) continue;
+            if (tile_starts >> k & 1) {
+                if (cur >= 0 && pmax >= 0) {
+                    atomicMin(&raw[cur].lo_min, lmin);
+                    atomicMax(&raw[cur].pos_max, pmax);
+                }
+                ++cur;
+                lmin = INT_MAX;
+                pmax = -1;
+            }
+            const int pos = ps[k] < 0 ? 0 : (ps[k] >= max_pos ? max_pos - 1 : ps[k]);
+            lmin = min(lmin, row_lo(pos, a.window));
+            pmax = max(pmax, pos);
+        }
+        if (cur >= 0 && pmax >= 0) {
+            atomicMin(&raw[cur].lo_min, lmin);
+            atomicMax(&raw[cur].pos_max, pmax);
+        }
+        carry_run = max(carry_run, block_last);
         n_tiles += chunk_tiles;
     }
     if (bad) atomicOr(&s_bad, 1);
-    __syncthreads();   // raw[].t0 visible to the block
+    __syncthreads();   // every descriptor complete and visible to the block
 
-    // 2. each tile's tokens, row and visible pages; histogram of sizes
-    for (int base = 0; base < n_tiles; base += blockDim.x) {
-        const int b = base + tid;
-        int t0 = 0, t1 = 0;
-        if (b < n_tiles) {
-            t0 = raw[b].t0;
-            t1 = b + 1 < n_tiles ? raw[b + 1].t0 : n;
-        }
-        __syncthreads();   // every t0 read before any descriptor is rewritten
-        if (b < n_tiles) {
-            int lo_min = INT_MAX, pos_max = -1;
-            for (int t = t0; t < t1; ++t) {
-                int pos = __ldg(a.positions + t);
-                pos = pos < 0 ? 0 : (pos >= max_pos ? max_pos - 1 : pos);
-                lo_min = min(lo_min, row_lo(pos, a.window));
-                pos_max = max(pos_max, pos);
-            }
-            const int first = lo_min / kPageSize, npg = pos_max / kPageSize - first + 1;
-            int4* dst = reinterpret_cast<int4*>(raw + b);
-            dst[0] = make_int4(t0, t1 - t0, __ldg(a.row_of + t0), first);
-            dst[1] = make_int4(npg, lo_min, pos_max, 0);
-            atomicAdd(&s_off[npg < kPfBuckets ? npg : kPfBuckets - 1], 1);
-        }
+    // 2. each tile's token count and pages; histogram of sizes
+    for (int b = tid; b < n_tiles; b += blockDim.x) {
+        const int t0 = raw[b].t0, t1 = b + 1 < n_tiles ? raw[b + 1].t0 : n;
+        const int first = raw[b].lo_min / kPageSize, npg = raw[b].pos_max / kPageSize - first + 1;
+        raw[b].ntok = t1 - t0;
+        raw[b].first_page = first;
+        raw[b].npg = npg;
+        atomicAdd(&s_off[npg < kPfBuckets ? npg : kPfBuckets - 1], 1);
     }
     __syncthreads();
 
     // 3. counting sort, largest first: bucket kPfBuckets-1 first
     {
-        const int per = kPfBuckets / (int)blockDim.x;   // buckets per thread (blockDim divides 1024)
-        int h[kPfBuckets / 256];
+        constexpr int per = kPfBuckets / kPrepThreads;   // buckets per thread
+        int h[per];
         int sum = 0;
+        #pragma unroll
         for (int k = 0; k < per; ++k) {
             h[k] = s_off[kPfBuckets - 1 - (tid * per + k)];
             sum += h[k];
         }
         int total;
-        const int inc = block_scan<false>(sum, s_warp, &total);
-        int off = inc - sum;
+        int off = block_scan_excl<false>(sum, 0, s_warp, &total);
+        #pragma unroll
         for (int k = 0; k < per; ++k) {
             s_off[kPfBuckets - 1 - (tid * per + k)] = off;
             off += h[k];
@@ -598,15 +650,23 @@ __device__ void rope_write_token(const PrefillPrepArgs& a, int i) {
                           page_ok, page, slot >= 0 ? slot % kPageSize : 0);
 }
 
-// Block 0 builds the tile list; block 1 + i rotates and writes token i.
-template <typename T>
-__global__ void __launch_bounds__(512) prefill_prep_kernel(const __grid_constant__ PrefillPrepArgs a) {
+// The tile list: one block.  Lets the rope kernel launched after it start
+// at once.
+__global__ void __launch_bounds__(kPrepThreads) prefill_plan_kernel(const __grid_constant__ PrefillPrepArgs a) {
     griddep_launch_dependents();
-    if (blockIdx.x == 0) {
-        build_prefill_plan(a);
-        return;
-    }
-    rope_write_token<T>(a, blockIdx.x - 1);
+    build_prefill_plan(a);
+}
+
+// Block i rotates and writes token i.  It waits for the planner before it
+// exits, so that the completion of this grid (all the attention kernel
+// waits for) also covers the tile list.
+constexpr int kRopeThreads = 128;
+
+template <typename T>
+__global__ void __launch_bounds__(kRopeThreads) prefill_rope_kernel(const __grid_constant__ PrefillPrepArgs a) {
+    griddep_launch_dependents();
+    rope_write_token<T>(a, blockIdx.x);
+    griddep_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -639,11 +699,20 @@ cudaError_t launch_prep(const PrepArgs& a, int dtype, cudaStream_t stream) {
 
 cudaError_t launch_prefill_prep(const PrefillPrepArgs& a, int dtype, cudaStream_t stream) {
     if (a.n_tokens <= 0) return cudaSuccess;
-    if (dtype == 0)
-        prefill_prep_kernel<__nv_bfloat16><<<a.n_tokens + 1, 512, 0, stream>>>(a);
-    else
-        prefill_prep_kernel<float><<<a.n_tokens + 1, 512, 0, stream>>>(a);
-    return cudaGetLastError();
+    prefill_plan_kernel<<<1, kPrepThreads, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.n_tokens);
+    cfg.blockDim = dim3(kRopeThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (dtype == 0) return cudaLaunchKernelEx(&cfg, prefill_rope_kernel<__nv_bfloat16>, a);
+    return cudaLaunchKernelEx(&cfg, prefill_rope_kernel<float>, a);
 }
 
 }  // namespace pdattn
