@@ -21,6 +21,9 @@ Functions and the passages they follow (page title, section):
   prefill_paged   packed prompt tokens: rope, write at their pool slots, then
                   each token's causal attention over its row (the
                   llama-3.1-8b-instruct page's ``prefill_paged`` signature)
+  packed          Llama example page, ``src/attention.linnet`` (``packed``):
+                  sequences packed into one row, mask ``own[i, j] =
+                  segments[i] == segments[j] && positions[j] <= positions[i]``
 
 Every function is pinned by tests under ``tests/test_oracle_*.py`` against
 closed forms, brute force and invariants; the rotation direction of RoPE is
@@ -62,10 +65,11 @@ def lib():
         L.oracle_decode_sinks.argtypes = [ctypes.POINTER(Shape)] + [vp] * 8
         L.oracle_step.argtypes = [ctypes.POINTER(Shape)] + [vp] * 10
         L.oracle_prefill_paged.argtypes = [ctypes.POINTER(Shape), ctypes.c_int] + [vp] * 13
+        L.oracle_packed.argtypes = [ctypes.POINTER(Shape), ctypes.c_int] + [vp] * 10
         L.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
         L.oracle_f32_to_bf16.restype = ctypes.c_uint16
         for f in (L.oracle_rope_tables, L.oracle_rope_write_kv, L.oracle_decode, L.oracle_decode_sinks,
-                  L.oracle_step, L.oracle_prefill_paged):
+                  L.oracle_step, L.oracle_prefill_paged, L.oracle_packed):
             f.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -137,6 +141,16 @@ def prefill_paged(shape, q, k_new, v_new, positions, rows, slots, table, k_pool,
                                     _ptr(positions), _ptr(rows), _ptr(slots), _ptr(table), _ptr(k_pool),
                                     _ptr(v_pool), _ptr(sinks), _ptr(q_rot), _ptr(out), _ptr(out64))
     return q_rot, out, out64, rc
+
+
+def packed(shape, q, k, v, positions, segments, sinks=None):
+    """Packed attention; returns (q_rot, k_rot, out, out64, status)."""
+    q_rot, k_rot = np.empty_like(q), np.empty_like(k)
+    out = np.zeros(q.shape, dtype=q.dtype)
+    out64 = np.zeros(q.shape, dtype=np.float64)
+    rc = lib().oracle_packed(ctypes.byref(shape), int(q.shape[0]), _ptr(q), _ptr(k), _ptr(v), _ptr(positions),
+                             _ptr(segments), _ptr(sinks), _ptr(q_rot), _ptr(k_rot), _ptr(out), _ptr(out64))
+    return q_rot, k_rot, out, out64, rc
 
 
 def f32_to_bf16_bits(x: float) -> int:

@@ -22,6 +22,11 @@
  *   oracle_prefill_paged rope + write of packed prompt tokens at their slots,
  *                        then each token's causal attention over its row
  *                        (llama-3.1-8b-instruct page, `prefill_paged`).
+ *   oracle_packed        Llama example page, "src/attention.linnet"
+ *                        (`packed`): sequences packed into one row, rope at
+ *                        each token's own position, mask own[i, j] =
+ *                        segments[i] == segments[j] && positions[j] <=
+ *                        positions[i], no cache.
  *   oracle_decode(_sinks) Llama example page, "src/attention.linnet"
  *                        (`decode`): mask seen[s] = s <= pos, scale
  *                        rsqrt(f32(head dim)), grouped attention where query
@@ -346,4 +351,80 @@ int oracle_prefill_paged(const oracle_shape* p, int n_tokens, const void* q, con
 }
 
 /* Exposed for pins on the rounding helper itself. */
+/*
+ * Packed attention (Llama example page, "src/attention.linnet", `packed`):
+ * n tokens of several sequences packed into one row; token p sits at
+ * positions[p] of sequence segments[p].  q [n, Hq, D] and k [n, Hk, D] are
+ * rotated at each token's own position into q_rot and k_rot (caller
+ * buffers of the same shapes); v [n, Hk, D] is used as given.  Token i
+ * attends to every token j of the pack with segments[j] == segments[i] and
+ * positions[j] <= positions[i] (the pages' mask `own`), and with a window
+ * W > 0 also positions[j] > positions[i] - W (the gpt-oss-20b page's
+ * windowed variants), scale rsqrt(f32(D)), optional sinks as in decode.
+ * Uses heads, kv_heads, head_dim, dtype, window and rope_theta of the shape.
+ * Written out directly from the definition: it shares no code with decode.
+ */
+int oracle_packed(const oracle_shape* p, int n, const void* q, const void* k, const void* v,
+                  const int32_t* positions, const int32_t* segments, const void* sinks,
+                  void* q_rot, void* k_rot, void* out, double* out64) {
+    if (!p || n < 0 || p->heads <= 0 || p->kv_heads <= 0 || p->heads % p->kv_heads != 0 ||
+        p->head_dim <= 0 || p->head_dim % 2 != 0 || (p->dtype != 0 && p->dtype != 1))
+        return ORACLE_EINVAL;
+    const int D = p->head_dim, Hq = p->heads, Hk = p->kv_heads, group = Hq / Hk;
+    for (int i = 0; i < n; ++i) {
+        if (positions[i] < 0) return ORACLE_EINVAL;
+        for (int h = 0; h < Hq; ++h) {
+            size_t o = ((size_t)i * Hq + h) * D;
+            if (p->rope_theta > 0.0f) rope_vector(q, o, q_rot, o, D, positions[i], p->rope_theta, p->dtype);
+            else for (int d = 0; d < D; ++d) copy_t(q_rot, o + d, q, o + d, p->dtype);
+        }
+        for (int h = 0; h < Hk; ++h) {
+            size_t o = ((size_t)i * Hk + h) * D;
+            if (p->rope_theta > 0.0f) rope_vector(k, o, k_rot, o, D, positions[i], p->rope_theta, p->dtype);
+            else for (int d = 0; d < D; ++d) copy_t(k_rot, o + d, k, o + d, p->dtype);
+        }
+    }
+    const double scale = (double)(float)(1.0 / sqrt((double)D)); /* rsqrt(f32(D)) */
+    double* w = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    double* acc = (double*)malloc(sizeof(double) * (size_t)D);
+    if (!w || !acc) { free(w); free(acc); return ORACLE_EINVAL; }
+    for (int i = 0; i < n; ++i) {
+        for (int h = 0; h < Hq; ++h) {
+            const int kvh = h / group;
+            const size_t qo = ((size_t)i * Hq + h) * D;
+            /* scores of the keys the mask lets through, max-subtracted softmax */
+            double m = sinks ? (double)load_t(sinks, (size_t)h, p->dtype) : -INFINITY;
+            for (int j = 0; j < n; ++j) {
+                int own = segments[j] == segments[i] && positions[j] <= positions[i];
+                if (own && p->window > 0) own = positions[j] > positions[i] - p->window;
+                if (!own) { w[j] = -INFINITY; continue; }
+                const size_t ko = ((size_t)j * Hk + kvh) * D;
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d)
+                    dot += (double)load_t(q_rot, qo + d, p->dtype) * (double)load_t(k_rot, ko + d, p->dtype);
+                w[j] = scale * dot;
+                if (w[j] > m) m = w[j];
+            }
+            double l = sinks ? exp((double)load_t(sinks, (size_t)h, p->dtype) - m) : 0.0;
+            for (int j = 0; j < n; ++j) {
+                w[j] = w[j] == -INFINITY ? 0.0 : exp(w[j] - m);
+                l += w[j];
+            }
+            for (int d = 0; d < D; ++d) acc[d] = 0.0;
+            for (int j = 0; j < n; ++j) {
+                if (w[j] == 0.0) continue;
+                const size_t vo = ((size_t)j * Hk + kvh) * D;
+                for (int d = 0; d < D; ++d) acc[d] += (w[j] / l) * (double)load_t(v, vo + d, p->dtype);
+            }
+            for (int d = 0; d < D; ++d) {
+                if (out64) out64[qo + d] = acc[d];
+                store_t(out, qo + d, (float)acc[d], p->dtype);
+            }
+        }
+    }
+    free(w);
+    free(acc);
+    return ORACLE_OK;
+}
+
 uint16_t oracle_f32_to_bf16(float f) { return float_to_bf16_bits(f); }

@@ -266,3 +266,61 @@ PREFILL_LLAMA = PrefillWorkload("llama8b_prefill", prefix=tuple(range(0, 8192, 1
                                 seed=1005)
 
 PREFILL_WORKLOADS = {w.name: w for w in (PREFILL_LLAMA,)}
+
+
+@dataclass(frozen=True)
+class PackedWorkload:
+    """Sequences of the given lengths packed into one row: sequence s holds
+    positions 0 .. lengths[s] - 1; its segment id is s, or a shuffled id."""
+    name: str
+    lengths: Sequence[int]
+    heads: int
+    kv_heads: int
+    head_dim: int
+    dtype: str = "bf16"
+    rope_theta: float = 10000.0
+    window: int = 0
+    shuffle_ids: bool = False
+    seed: int = 0
+
+    @property
+    def tokens(self) -> int:
+        return int(sum(self.lengths))
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    @property
+    def max_seq(self) -> int:
+        return int(max(self.lengths))
+
+
+def generate_packed(w: PackedWorkload, device="cpu", seed: Optional[int] = None):
+    """q [P, Hq, D], k / v [P, Hk, D], positions / segments [P] i32.
+    Draw order: segment ids (if shuffled) -> q -> k -> v."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed if seed is None else seed)
+    n_seq = len(w.lengths)
+    ids = torch.randperm(n_seq, generator=gen, device=device).cpu().tolist() if w.shuffle_ids else list(range(n_seq))
+    positions, segments = [], []
+    for s, L in enumerate(w.lengths):
+        positions += list(range(L))
+        segments += [ids[s] * 7 + 3] * L          # arbitrary, non-contiguous id values
+    P, Hq, Hk, D = w.tokens, w.heads, w.kv_heads, w.head_dim
+
+    def normal(*shape):
+        return torch.randn(*shape, generator=gen, device=device, dtype=torch.float32).to(w.torch_dtype)
+
+    i32 = lambda x: torch.tensor(x, dtype=torch.int32, device=device)
+    return dict(q=normal(P, Hq, D), k=normal(P, Hk, D), v=normal(P, Hk, D), positions=i32(positions),
+                segments=i32(segments))
+
+
+# Llama-3.1-8B attention shape, packed training row: 8192 tokens in sequences
+# of mixed lengths (the pages' packed entries take several sequences per row).
+PACKED_LLAMA = PackedWorkload("llama8b_packed", lengths=(3000, 1500, 1200, 900, 700, 400, 300, 192), heads=32,
+                              kv_heads=8, head_dim=128, rope_theta=500000.0, seed=1006)
+
+PACKED_WORKLOADS = {w.name: w for w in (PACKED_LLAMA,)}
