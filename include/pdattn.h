@@ -224,6 +224,35 @@ pdattn_status pdattn_prefill_attend(const pdattn_params* p, int32_t n_tokens, co
                                     pdattn_stream stream);
 
 /*
+ * Bytes of workspace pdattn_packed needs for n_tokens packed tokens (0 if the
+ * parameters are invalid).
+ */
+size_t pdattn_packed_workspace_size(const pdattn_params* p, int32_t n_tokens);
+
+/*
+ * Packed sequences, no cache: `packed(x, positions, segments)` of the Llama
+ * example page ("src/attention.linnet").  Several sequences lie in one row
+ * of n_tokens tokens; token i sits at positions[i] of sequence segments[i].
+ * q_rot[i] = rope(q[i], positions[i]) and k_rot[i] = rope(k[i],
+ * positions[i]) (kept in the workspace); then
+ *   out[i, h] = sum_j softmax_j(scale * q_rot[i, h] . k_rot[j, h / g]) v[j, h / g]
+ * over the tokens j with segments[j] == segments[i] and positions[j] <=
+ * positions[i] (the pages' mask `own`), and with a window W > 0 also
+ * positions[j] > positions[i] - W; sinks as in pdattn_attend.
+ * Layouts: q, out [n_tokens, heads, head_dim]; k, v [n_tokens, kv_heads,
+ * head_dim]; positions, segments [n_tokens] int32.  Of p only heads,
+ * kv_heads, head_dim, dtype (bf16), window, scale, the rope tables and
+ * sinks are read.  Fast when every sequence is one run of consecutive
+ * tokens with strictly increasing positions (as packing lays them out);
+ * any other layout is handled exactly but visits the whole pack per tile.
+ * A negative position or one past the rope table is recorded as
+ * PDATTN_EBADPOS and no output is written.
+ */
+pdattn_status pdattn_packed(const pdattn_params* p, int32_t n_tokens, const void* q, const void* k,
+                            const void* v, const int32_t* positions, const int32_t* segments,
+                            void* out, void* workspace, size_t workspace_bytes, pdattn_stream stream);
+
+/*
  * Synchronises `stream`, reads the workspace's device status word, clears
  * it and returns the first error it recorded (PDATTN_OK if none).
  */

@@ -54,6 +54,8 @@ def _load():
         "pdattn_prefill_workspace_size": (sz, [P, i32]),
         "pdattn_prefill_paged": (i32, [P, i32] + [vp] * 11 + [sz, vp]),
         "pdattn_prefill_attend": (i32, [P, i32] + [vp] * 6 + [sz, vp]),
+        "pdattn_packed_workspace_size": (sz, [P, i32]),
+        "pdattn_packed": (i32, [P, i32] + [vp] * 7 + [sz, vp]),
         "pdattn_check_status": (i32, [vp, vp]),
         "pdattn_last_error": (ctypes.c_char_p, []),
         "pdattn_last_launch_count": (i32, []),
@@ -243,6 +245,26 @@ def prefill_attend(p, positions, table, k_pool, v_pool, out, ws, stream=None):
     w, nb = _ws(ws)
     _check(lib.pdattn_prefill_attend(ctypes.byref(p), n, _ptr(positions), _ptr(table), _ptr(k_pool), _ptr(v_pool),
                                      _ptr(out), w, nb, _stream(stream)))
+
+
+def new_packed_workspace(p, n_tokens, device="cuda"):
+    n = lib.pdattn_packed_workspace_size(ctypes.byref(p), n_tokens)
+    if n == 0:
+        raise PdattnError(EINVAL, lib.pdattn_last_error().decode() or "invalid parameters")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def packed(p, q, k, v, positions, segments, out, ws, stream=None):
+    """Sequences packed into one row: q / out [n, heads, D], k / v [n, kv_heads, D],
+    positions / segments [n] int32."""
+    n = q.shape[0] if isinstance(q, torch.Tensor) else -1
+    for name, t in (("positions", positions), ("segments", segments)):
+        _expect(name, t, (n,), torch.int32)
+    for name, t, h in (("q", q, p.heads), ("k", k, p.kv_heads), ("v", v, p.kv_heads), ("out", out, p.heads)):
+        _expect(name, t, (n, h, p.head_dim), _dt(p))
+    w, nb = _ws(ws)
+    _check(lib.pdattn_packed(ctypes.byref(p), n, _ptr(q), _ptr(k), _ptr(v), _ptr(positions), _ptr(segments),
+                             _ptr(out), w, nb, _stream(stream)))
 
 
 def check_status(ws, stream=None):

@@ -472,6 +472,114 @@ pdattn_status pdattn_prefill_attend(const pdattn_params* p, int32_t n_tokens, co
                         stream, false);
 }
 
+static pdattn_status check_packed_params(const pdattn_params* p) {
+    if (!p) return fail(PDATTN_EINVAL, "params is NULL");
+    if (p->heads <= 0 || p->kv_heads <= 0 || p->heads % p->kv_heads != 0)
+        return fail(PDATTN_EINVAL, "heads (%d) must be a positive multiple of kv_heads (%d)", p->heads, p->kv_heads);
+    if (p->head_dim <= 0 || p->head_dim % 2 != 0) return fail(PDATTN_EINVAL, "head_dim must be even and positive");
+    if (p->dtype != PDATTN_BF16 && p->dtype != PDATTN_F32) return fail(PDATTN_EINVAL, "unknown dtype %d", p->dtype);
+    if ((p->rope_cos == nullptr) != (p->rope_sin == nullptr))
+        return fail(PDATTN_EINVAL, "rope_cos and rope_sin must be both set or both NULL");
+    if (p->rope_cos && p->rope_len <= 0) return fail(PDATTN_EINVAL, "rope_len must be > 0 with rope tables");
+    if (p->rope_cos && (!aligned16(p->rope_cos) || !aligned16(p->rope_sin)))
+        return fail(PDATTN_EINVAL, "rope tables must be 16-byte aligned");
+    if (!(p->scale >= 0.f)) return fail(PDATTN_EINVAL, "scale must be >= 0 (0 selects rsqrt(head_dim))");
+    if (p->dtype != PDATTN_BF16) return fail(PDATTN_EUNSUPPORTED, "packed attention runs on the tensor cores: dtype must be bf16");
+    if (p->head_dim != 64 && p->head_dim != 128) return fail(PDATTN_EUNSUPPORTED, "head_dim must be 64 or 128");
+    if (p->heads / p->kv_heads > kMaxGroup) return fail(PDATTN_EUNSUPPORTED, "heads / kv_heads must be <= 8");
+    return PDATTN_OK;
+}
+
+size_t pdattn_packed_workspace_size(const pdattn_params* p, int32_t n_tokens) {
+    if (check_packed_params(p) != PDATTN_OK || n_tokens < 0) return 0;
+    return pk_layout(n_tokens, p->heads, p->kv_heads, p->head_dim, 2).total;
+}
+
+pdattn_status pdattn_packed(const pdattn_params* p, int32_t n_tokens, const void* q, const void* k, const void* v,
+                            const int32_t* positions, const int32_t* segments, void* out, void* workspace,
+                            size_t workspace_bytes, pdattn_stream stream) {
+    g_launches = 0;
+    pdattn_status s = check_packed_params(p);
+    if (s != PDATTN_OK) return s;
+    if (n_tokens < 0) return fail(PDATTN_EINVAL, "n_tokens < 0");
+    if (n_tokens == 0) return PDATTN_OK;
+    if (!q || !k || !v || !positions || !segments || !out) return fail(PDATTN_EINVAL, "NULL data pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return fail(PDATTN_EINVAL, "q, k, v and out must be 16-byte aligned");
+    if (!workspace) return fail(PDATTN_EINVAL, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+        return fail(PDATTN_EINVAL, "workspace must be 256-byte aligned");
+    const PfLayout L = pk_layout(n_tokens, p->heads, p->kv_heads, p->head_dim, 2);
+    if (workspace_bytes < L.total)
+        return fail(PDATTN_EINVAL, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, L.total);
+    const int sms = sm_count();
+    if (sms <= 0) return fail(PDATTN_ECUDA, "no CUDA device");
+    char* ws = static_cast<char*>(workspace);
+    const int g = p->heads / p->kv_heads, tile_tokens = 2 * (kPfRows / g), D = p->head_dim;
+
+    auto fn = encode_fn();
+    if (!fn) return fail(PDATTN_ECUDA, "cuTensorMapEncodeTiled is not available");
+    // queries (D, heads, tokens), boxes of g heads x half a tile; keys and
+    // values (D, kv_heads, tokens), boxes of one kv head x 64 tokens
+    auto map3 = [&](CUtensorMap* m, const void* base, int heads, int box_h, int box_t) -> pdattn_status {
+        cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)n_tokens};
+        cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
+        cuuint32_t box[3] = {64, (cuuint32_t)box_h, (cuuint32_t)box_t};
+        cuuint32_t estr[3] = {1, 1, 1};
+        CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(PDATTN_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+        return PDATTN_OK;
+    };
+    CUtensorMap qm, km, vm;
+    if ((s = map3(&qm, ws + L.q_rot, p->heads, g, tile_tokens / 2)) != PDATTN_OK) return s;
+    if ((s = map3(&km, ws + L.k_rot, p->kv_heads, 1, kPageSize)) != PDATTN_OK) return s;
+    if ((s = map3(&vm, v, p->kv_heads, 1, kPageSize)) != PDATTN_OK) return s;
+
+    PrefillPrepArgs pa = {};
+    pa.n_tokens = n_tokens;
+    pa.rows = 0;
+    pa.heads = p->heads;
+    pa.kv_heads = p->kv_heads;
+    pa.head_dim = D;
+    pa.window = p->window;
+    pa.rope_len = p->rope_len;
+    pa.tile_tokens = tile_tokens;
+    pa.q = q;
+    pa.k_new = k;
+    pa.v_new = v;
+    pa.positions = positions;
+    pa.row_of = segments;
+    pa.rope_cos = p->rope_cos;
+    pa.rope_sin = p->rope_sin;
+    pa.ws = ws;
+    pa.L = L;
+    cudaError_t e = launch_packed_prep(pa, p->dtype, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "packed plan/rope launch");
+
+    PrefillArgs aa = {};
+    aa.n_tokens = n_tokens;
+    aa.heads = p->heads;
+    aa.kv_heads = p->kv_heads;
+    aa.group = g;
+    aa.tile_tokens = tile_tokens;
+    aa.head_dim = D;
+    aa.window = p->window;
+    aa.packed = 1;
+    aa.scale_log2 = scale_log2(p);
+    aa.positions = positions;
+    aa.sinks = p->sinks;
+    aa.out = out;
+    aa.ws = ws;
+    aa.L = L;
+    const long long units = (long long)n_tokens * p->kv_heads;
+    e = launch_packed(aa, qm, km, vm, (int)(units < sms ? units : sms), (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "packed attention launch");
+    g_launches = 3;
+    return PDATTN_OK;
+}
+
 pdattn_status pdattn_check_status(void* workspace, pdattn_stream stream) {
     if (!workspace) return fail(PDATTN_EINVAL, "workspace is NULL");
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);

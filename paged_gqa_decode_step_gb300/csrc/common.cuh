@@ -102,6 +102,10 @@ static_assert(sizeof(PfTile) == 32, "prefill tile descriptor is 32 bytes");
 
 struct PfLayout {
     size_t ctrl, tiles_raw, tiles, q_rot, total;
+    // packed attention only (0 otherwise): rotated keys [n, kv_heads, D],
+    // segment ids and positions padded to whole 64-token blocks, and one
+    // int4 summary per block {all one segment, segment, min pos, max pos}
+    size_t k_rot, seg_pad, pos_pad, blk;
 };
 
 // Tiles never outnumber tokens.
@@ -112,6 +116,19 @@ __host__ __device__ inline PfLayout pf_layout(int n_tokens, int heads, int head_
     L.tiles_raw = off; off = align256(off + sizeof(PfTile) * (size_t)n_tokens);
     L.tiles = off; off = align256(off + sizeof(PfTile) * (size_t)n_tokens);
     L.q_rot = off; off = align256(off + (size_t)elem_bytes * n_tokens * heads * head_dim);
+    L.total = off;
+    L.k_rot = L.seg_pad = L.pos_pad = L.blk = 0;
+    return L;
+}
+
+__host__ __device__ inline PfLayout pk_layout(int n_tokens, int heads, int kv_heads, int head_dim, int elem_bytes) {
+    PfLayout L = pf_layout(n_tokens, heads, head_dim, elem_bytes);
+    const size_t blocks = ((size_t)n_tokens + kPageSize - 1) / kPageSize;
+    size_t off = L.total;
+    L.k_rot = off; off = align256(off + (size_t)elem_bytes * n_tokens * kv_heads * head_dim);
+    L.seg_pad = off; off = align256(off + sizeof(int) * blocks * kPageSize);
+    L.pos_pad = off; off = align256(off + sizeof(int) * blocks * kPageSize);
+    L.blk = off; off = align256(off + sizeof(int4) * blocks);
     L.total = off;
     return L;
 }

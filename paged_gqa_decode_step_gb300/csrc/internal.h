@@ -43,8 +43,8 @@ struct PrefillPrepArgs {
     const void* k_new;      // [n_tokens, kv_heads, D]
     const void* v_new;
     const int* positions;   // [n_tokens]
-    const int* row_of;      // [n_tokens] table row of each token
-    const int* slots;       // [n_tokens] page * 64 + offset
+    const int* row_of;      // [n_tokens] table row of each token (packed: segment id)
+    const int* slots;       // [n_tokens] page * 64 + offset (packed: unused)
     const void* rope_cos;   // nullptr: copy without rotation
     const void* rope_sin;
     void* k_pool;
@@ -55,6 +55,7 @@ struct PrefillPrepArgs {
 
 struct PrefillArgs {
     int n_tokens, heads, kv_heads, group, tile_tokens, head_dim, pages_per_row, num_pages, window;
+    int packed;             // 1: packed sequences (keys are the pack's 64-token blocks)
     float scale_log2;
     const int* positions;
     const int* table;
@@ -78,5 +79,12 @@ cudaError_t launch_prefill_prep(const PrefillPrepArgs& a, int dtype, cudaStream_
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
                            const CUtensorMap& v_map, int grid, cudaStream_t stream);
 size_t prefill_smem_bytes(int head_dim);
+// Packed sequences: tile list and block summaries (one block), then rope of
+// q and k into the workspace (programmatic launch ending after the plan).
+cudaError_t launch_packed_prep(const PrefillPrepArgs& a, int dtype, cudaStream_t stream);
+// Tensor-core attention of the packed tiles: k_map over the rotated keys and
+// v_map over v, both [n, kv_heads, D] as 3-D tensors.
+cudaError_t launch_packed(const PrefillArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
+                          const CUtensorMap& v_map, int grid, cudaStream_t stream);
 
 }  // namespace pdattn

@@ -21,6 +21,13 @@
 // other; S is double-buffered per half.  The running max is raised lazily:
 // O is rescaled in TMEM only when a row's max grows by more than 2^8.
 //
+// Packed sequences (Llama example page, `packed`) run the same kernel: the
+// pack is a contiguous cache of 64-token key blocks, K and V come by 3-D TMA
+// from the rotated keys and the values [n, kv_heads, D], and the mask is
+// per key (same segment id, position <= the query's, inside the window),
+// from segment ids and positions copied into shared memory with each block;
+// blocks wholly of the row's sequence and before its position skip the test.
+//
 // Warps: 0 = TMA producer (Q boxes, K and V pages), 1 = TMEM owner and MMA
 // issuer, 2..5 = softmax and epilogue of half A, 6..9 of half B (warp w
 // reads TMEM lanes 32 * (w % 4) .. + 31).  Every wait is bounded; on a
@@ -37,13 +44,16 @@ constexpr int kPfThreads = 320;
 constexpr uint64_t kPfTimeoutNs = 2000000000ull;
 constexpr float kRescaleLog2 = 8.0f;    // lazy rescale threshold (log2 units)
 
-template <int D>
+template <int D, bool kPacked = false>
 struct PfCfg {
     static constexpr int kBoxes = D / 64;                 // 64-element column boxes
     static constexpr int kQBytes = kBoxes * 16384;        // one half: 128 rows x 128 B per box
     static constexpr int kKvBytes = kBoxes * 8192;        // one page of K (or V): 64 rows x 128 B per box
     static constexpr int kStageBytes = 2 * kKvBytes;
-    static constexpr int kStages = D == 128 ? 4 : 8;
+    // packed mode keeps each stage's segment ids and positions (512 B) in
+    // static shared memory, which costs D = 128 one stage
+    static constexpr int kStages = D == 128 ? (kPacked ? 3 : 4) : 8;
+    static constexpr int kMaskStages = kPacked ? kStages : 1;
     static constexpr int kPBytes = 16384;                 // 128 rows x 64 bf16, one per half
     static constexpr int kOffQ = 0;                       // halves A, B
     static constexpr int kOffStage = 2 * kQBytes;
@@ -52,7 +62,7 @@ struct PfCfg {
     // TMEM: S of half h, buffer b at column 128 h + 64 b; O of half h at 256 + h D.
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColO = 256;
-    static_assert(kSmem <= 227 * 1024 - 2048, "shared memory budget");
+    static_assert(kSmem + kMaskStages * 512 <= 227 * 1024 - 1536, "shared memory budget");
 };
 
 // --- tcgen05 / TMA wrappers ---------------------------------------------------
@@ -159,6 +169,14 @@ __device__ __forceinline__ void elect_tma_3d(uint32_t dst, const CUtensorMap* ma
         : "memory");
 }
 
+__device__ __forceinline__ void elect_bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 // Warp-wide bounded wait: every lane polls, and the warp agrees on the result.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, Ctrl* ctrl);
 
@@ -218,11 +236,15 @@ struct PfBars {
 };
 
 // Softmax and epilogue of one half (128 threads, one MMA row each).
-template <int D>
+template <int D, bool kPacked>
 __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile* tiles, int n_units, int half,
                                              int quarter, int lane, uint32_t tmem, uint32_t st_s, uint32_t p_s,
-                                             PfBars& bars, volatile int* abort, Ctrl* ctrl) {
-    using C = PfCfg<D>;
+                                             PfBars& bars, const int (*s_mask)[128], uint64_t* kv_full,
+                                             volatile int* abort, Ctrl* ctrl) {
+    using C = PfCfg<D, kPacked>;
+    const int* seg_pad = reinterpret_cast<const int*>(a.ws + a.L.seg_pad);
+    const int4* blk = reinterpret_cast<const int4*>(a.ws + a.L.blk);
+    const int W = a.window;
     const int Hk = a.kv_heads, g = a.group, Tq = a.tile_tokens / 2;
     const int m = quarter * 32 + lane;                    // MMA row = TMEM lane
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -244,11 +266,12 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
         }
         const int tok = half * Tq + tq;                   // token of this row within the tile
         const bool active = tq < Tq && tok < t.ntok;
-        int pos = -1, lo = 0;
+        int pos = -1, lo = 0, seg = 0;
         if (active) {
             pos = __ldg(a.positions + t.t0 + tok);
             pos = pos < 0 ? 0 : pos;
-            lo = (a.window > 0 && pos - a.window + 1 > 0) ? pos - a.window + 1 : 0;
+            lo = (W > 0 && pos - W + 1 > 0) ? pos - W + 1 : 0;
+            if (kPacked) seg = seg_pad[t.t0 + tok];
         }
         float m_run = -INFINITY, l = 0.f;
         for (int k = 0; k < t.npg; ++k) {
@@ -262,12 +285,37 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
             tmem_ld32(tmem + lane_base + s_col + (j & 1) * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
             tmem_ld32(tmem + lane_base + s_col + (j & 1) * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
             tmem_wait_ld();
-            // keys c of this page visible to the row: lo <= pg*64 + c <= pos
-            const int c_lo = lo - pg * kPageSize, c_hi = pos - pg * kPageSize;
-            if (!__all_sync(0xffffffffu, c_lo <= 0 && c_hi >= kPageSize - 1)) {
-                #pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (c < c_lo || c > c_hi) s[c] = __float_as_uint(-INFINITY);
+            if (!kPacked) {
+                // keys c of this page visible to the row: lo <= pg*64 + c <= pos
+                const int c_lo = lo - pg * kPageSize, c_hi = pos - pg * kPageSize;
+                if (!__all_sync(0xffffffffu, c_lo <= 0 && c_hi >= kPageSize - 1)) {
+                    #pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (c < c_lo || c > c_hi) s[c] = __float_as_uint(-INFINITY);
+                }
+            } else {
+                // key c of block pg is visible when it belongs to the row's
+                // sequence at a position <= pos (and inside the window); a
+                // block wholly of that sequence and before pos skips the test
+                const int4 bi = blk[pg];
+                const bool full = active && bi.x && bi.y == seg && bi.w <= pos && (W <= 0 || bi.z > pos - W);
+                if (!__all_sync(0xffffffffu, full)) {
+                    const int st = (it + k) % C::kStages;
+                    // the stage's ids and positions came by bulk copy on kv_full
+                    mbar_wait(smem_u32(&kv_full[st]), ((it + k) / C::kStages) & 1, kPfTimeoutNs);
+                    const int4* sg = reinterpret_cast<const int4*>(s_mask[st]);
+                    const int4* sp = reinterpret_cast<const int4*>(s_mask[st] + 64);
+                    #pragma unroll
+                    for (int c4 = 0; c4 < 16; ++c4) {
+                        const int4 g4 = sg[c4], p4 = sp[c4];
+                        const int gs[4] = {g4.x, g4.y, g4.z, g4.w}, pp[4] = {p4.x, p4.y, p4.z, p4.w};
+                        #pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const bool vis = active && gs[e] == seg && pp[e] <= pos && (W <= 0 || pp[e] > pos - W);
+                            if (!vis) s[4 * c4 + e] = __float_as_uint(-INFINITY);
+                        }
+                    }
+                }
             }
             const float mx = max64(s) * sl2;               // scale > 0: the max commutes with it
             const bool need = mx > m_run + kRescaleLog2;
@@ -377,15 +425,16 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
     }
 }
 
-template <int D>
+template <int D, bool kPacked>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                    const __grid_constant__ CUtensorMap v_map, const __grid_constant__ PrefillArgs a) {
-    using C = PfCfg<D>;
+    using C = PfCfg<D, kPacked>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t kv_full[C::kStages];
     __shared__ __align__(8) uint64_t kv_empty[C::kStages];
     __shared__ __align__(8) PfBars bars;
+    __shared__ __align__(16) int s_mask[C::kMaskStages][128];   // packed: segment ids [0,64), positions [64,128)
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -451,22 +500,37 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 for (int b = 0; b < C::kBoxes; ++b)
                     elect_tma_3d(q_s + h * C::kQBytes + b * 16384, &q_map, b * 64, kvh * g, t0 + h * Tq,
                                  smem_u32(&bars.q_full));
-            const int* trow = a.table + (size_t)row * a.pages_per_row + first;
+            const int* trow = kPacked ? nullptr : a.table + (size_t)row * a.pages_per_row + first;
             for (int k = 0; k < npg; ++k, ++it) {
                 const int s = it % C::kStages;
                 ok = warp_wait(smem_u32(&kv_empty[s]), ((it / C::kStages) & 1) ^ 1, abort, ctrl);
                 if (!ok) break;
-                int page = uni(__ldg(trow + k));
-                if (page < 0 || page >= a.num_pages) {
-                    if (lane == 0) set_error(ctrl, kErrBadPage);
-                    page = 0;
-                }
-                const int y = (page * Hk + kvh) * kPageSize;
                 const uint32_t kb = st_s + s * C::kStageBytes, vb = kb + C::kKvBytes;
-                elect_arrive_expect_tx(smem_u32(&kv_full[s]), C::kStageBytes);
-                for (int b = 0; b < C::kBoxes; ++b) {
-                    elect_tma_2d(kb + b * 8192, &k_map, b * 64, y, smem_u32(&kv_full[s]));
-                    elect_tma_2d(vb + b * 8192, &v_map, b * 64, y, smem_u32(&kv_full[s]));
+                if (kPacked) {
+                    // key block first + k of the pack: tokens [64 blk, 64 blk + 64)
+                    const int blk0 = (first + k) * kPageSize;
+                    elect_arrive_expect_tx(smem_u32(&kv_full[s]), C::kStageBytes + 512);
+                    for (int b = 0; b < C::kBoxes; ++b) {
+                        elect_tma_3d(kb + b * 8192, &k_map, b * 64, kvh, blk0, smem_u32(&kv_full[s]));
+                        elect_tma_3d(vb + b * 8192, &v_map, b * 64, kvh, blk0, smem_u32(&kv_full[s]));
+                    }
+                    const uint32_t mb = smem_u32(&s_mask[kPacked ? s : 0][0]);
+                    elect_bulk_load(mb, reinterpret_cast<const int*>(a.ws + a.L.seg_pad) + blk0, 256,
+                                    smem_u32(&kv_full[s]));
+                    elect_bulk_load(mb + 256, reinterpret_cast<const int*>(a.ws + a.L.pos_pad) + blk0, 256,
+                                    smem_u32(&kv_full[s]));
+                } else {
+                    int page = uni(__ldg(trow + k));
+                    if (page < 0 || page >= a.num_pages) {
+                        if (lane == 0) set_error(ctrl, kErrBadPage);
+                        page = 0;
+                    }
+                    const int y = (page * Hk + kvh) * kPageSize;
+                    elect_arrive_expect_tx(smem_u32(&kv_full[s]), C::kStageBytes);
+                    for (int b = 0; b < C::kBoxes; ++b) {
+                        elect_tma_2d(kb + b * 8192, &k_map, b * 64, y, smem_u32(&kv_full[s]));
+                        elect_tma_2d(vb + b * 8192, &v_map, b * 64, y, smem_u32(&kv_full[s]));
+                    }
                 }
             }
         }
@@ -548,7 +612,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
     } else {
         // ---------------- softmax + epilogue: warps 2..5 half A, 6..9 half B ----------------
-        softmax_half<D>(a, tiles, n_units, (warp - 2) >> 2, warp & 3, lane, tmem, st_s, p_s, bars, abort, ctrl);
+        softmax_half<D, kPacked>(a, tiles, n_units, (warp - 2) >> 2, warp & 3, lane, tmem, st_s, p_s, bars, s_mask,
+                                 kv_full, abort, ctrl);
     }
 
     tc_fence_before();
@@ -561,23 +626,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
 }
 
-template <int D>
+template <int D, bool kPacked>
 cudaError_t launch_d(const PrefillArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
                      const CUtensorMap& v_map, int grid, cudaStream_t stream) {
-    auto kern = prefill_kernel<D>;
+    using C = PfCfg<D, kPacked>;
+    auto kern = prefill_kernel<D, kPacked>;
     static int configured_mask = 0;   // bit per device id < 31
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 31 || !(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PfCfg<D>::kSmem);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
         if (e != cudaSuccess) return e;
         if (dev < 31) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_ACQ_REL);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kPfThreads);
-    cfg.dynamicSmemBytes = PfCfg<D>::kSmem;
+    cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -591,13 +657,20 @@ cudaError_t launch_d(const PrefillArgs& a, const CUtensorMap& q_map, const CUten
 
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
                            const CUtensorMap& v_map, int grid, cudaStream_t stream) {
-    if (a.head_dim == 128) return launch_d<128>(a, q_map, k_map, v_map, grid, stream);
-    if (a.head_dim == 64) return launch_d<64>(a, q_map, k_map, v_map, grid, stream);
+    if (a.head_dim == 128) return launch_d<128, false>(a, q_map, k_map, v_map, grid, stream);
+    if (a.head_dim == 64) return launch_d<64, false>(a, q_map, k_map, v_map, grid, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_packed(const PrefillArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
+                          const CUtensorMap& v_map, int grid, cudaStream_t stream) {
+    if (a.head_dim == 128) return launch_d<128, true>(a, q_map, k_map, v_map, grid, stream);
+    if (a.head_dim == 64) return launch_d<64, true>(a, q_map, k_map, v_map, grid, stream);
     return cudaErrorInvalidValue;
 }
 
 size_t prefill_smem_bytes(int head_dim) {
-    return head_dim == 128 ? PfCfg<128>::kSmem : PfCfg<64>::kSmem;
+    return head_dim == 128 ? PfCfg<128, false>::kSmem : PfCfg<64, false>::kSmem;
 }
 
 }  // namespace pdattn

@@ -120,17 +120,18 @@ __device__ __forceinline__ void rope_pair(const T* x, T* y, const T* cos_row, co
 // last block (if plan) builds the split plan.
 // ---------------------------------------------------------------------------
 // Rotates the Hq query vectors q into q_out and the Hk key vectors kn into
-// pool slot (page, off), and copies the value vectors vn there; with
-// page_ok false only the queries.  cos_row == nullptr: plain copies.
+// k_dst (head h at k_dst + h * head_stride), and copies the value vectors vn
+// to v_dst the same way; with write_kv false only the queries, and with
+// v_dst == nullptr no values.  cos_row == nullptr: plain copies.
 template <typename T>
-__device__ __forceinline__ void rope_write_vectors(const T* q, T* q_out, const T* kn, const T* vn, T* kp, T* vp,
-                                                   const T* cos_row, const T* sin_row, int Hq, int Hk, int D,
-                                                   bool page_ok, int page, int off) {
+__device__ __forceinline__ void rope_write_vectors(const T* q, T* q_out, const T* kn, const T* vn, T* k_dst, T* v_dst,
+                                                   size_t head_stride, const T* cos_row, const T* sin_row, int Hq,
+                                                   int Hk, int D, bool write_kv) {
     constexpr int N = Vec16<T>::N;
     const bool rope = cos_row != nullptr;
     const int half = D / 2;
     const int per_head = rope ? half / N : D / N;  // work units per head vector
-    const int uq = Hq * per_head, uk = Hk * per_head, uv = Hk * (D / N);
+    const int uq = Hq * per_head, uk = Hk * per_head, uv = v_dst ? Hk * (D / N) : 0;
     for (int u = threadIdx.x; u < uq + uk + uv; u += blockDim.x) {
         if (u < uq) {
             const int h = u / per_head, e0 = (u % per_head) * N;
@@ -140,11 +141,11 @@ __device__ __forceinline__ void rope_write_vectors(const T* q, T* q_out, const T
                 *reinterpret_cast<uint4*>(q_out + (size_t)h * D + e0) =
                     *reinterpret_cast<const uint4*>(q + (size_t)h * D + e0);
             }
-        } else if (!page_ok) {
+        } else if (!write_kv) {
             break;
         } else if (u < uq + uk) {
             const int v = u - uq, h = v / per_head, e0 = (v % per_head) * N;
-            T* slot = kp + (((size_t)page * Hk + h) * kPageSize + off) * D;
+            T* slot = k_dst + h * head_stride;
             if (rope) {
                 rope_pair<T>(kn + (size_t)h * D, slot, cos_row, sin_row, half, e0);
             } else {
@@ -153,11 +154,17 @@ __device__ __forceinline__ void rope_write_vectors(const T* q, T* q_out, const T
             }
         } else {
             const int v = u - uq - uk, h = v / (D / N), e0 = (v % (D / N)) * N;
-            T* slot = vp + (((size_t)page * Hk + h) * kPageSize + off) * D;
+            T* slot = v_dst + h * head_stride;
             *reinterpret_cast<uint4*>(slot + e0) =
                 __ldg(reinterpret_cast<const uint4*>(vn + (size_t)h * D + e0));
         }
     }
+}
+
+// Pool slot (page, off) of kv head 0; kv head h is kPageSize * D further.
+template <typename T>
+__device__ __forceinline__ T* pool_slot(void* pool, int page, int Hk, int off, int D) {
+    return static_cast<T*>(pool) + (((size_t)page * Hk) * kPageSize + off) * D;
 }
 
 template <typename T>
@@ -173,14 +180,14 @@ __device__ void rope_write_row(const PrepArgs& a, int row) {
     const int page = __ldg(a.table + (size_t)row * a.pages_per_row + pos / kPageSize);
     const bool page_ok = page >= 0 && page < a.num_pages;
     if (!page_ok && threadIdx.x == 0) set_error(ctrl, kErrBadPage);
+    const int off = pos % kPageSize, pg = page_ok ? page : 0;
     rope_write_vectors<T>(static_cast<const T*>(a.q) + (size_t)row * Hq * D,
                           static_cast<T*>(a.q_out) + (size_t)row * Hq * D,
                           static_cast<const T*>(a.k_new) + (size_t)row * Hk * D,
-                          static_cast<const T*>(a.v_new) + (size_t)row * Hk * D, static_cast<T*>(a.k_pool),
-                          static_cast<T*>(a.v_pool),
+                          static_cast<const T*>(a.v_new) + (size_t)row * Hk * D, pool_slot<T>(a.k_pool, pg, Hk, off, D),
+                          pool_slot<T>(a.v_pool, pg, Hk, off, D), (size_t)kPageSize * D,
                           rope ? static_cast<const T*>(a.rope_cos) + (size_t)pos * D : nullptr,
-                          rope ? static_cast<const T*>(a.rope_sin) + (size_t)pos * D : nullptr, Hq, Hk, D,
-                          page_ok, page, pos % kPageSize);
+                          rope ? static_cast<const T*>(a.rope_sin) + (size_t)pos * D : nullptr, Hq, Hk, D, page_ok);
 }
 
 // Visible positions of a row: [lo, pos] with lo = 0 or pos - window + 1.
@@ -640,14 +647,224 @@ __device__ void rope_write_token(const PrefillPrepArgs& a, int i) {
     const int page = slot >= 0 ? slot / kPageSize : -1;
     const bool page_ok = page >= 0 && page < a.num_pages;
     if (!page_ok && threadIdx.x == 0) set_error(ctrl, kErrBadPage);
+    const int off = slot >= 0 ? slot % kPageSize : 0, pg = page_ok ? page : 0;
     rope_write_vectors<T>(static_cast<const T*>(a.q) + (size_t)i * Hq * D,
                           reinterpret_cast<T*>(a.ws + a.L.q_rot) + (size_t)i * Hq * D,
                           static_cast<const T*>(a.k_new) + (size_t)i * Hk * D,
-                          static_cast<const T*>(a.v_new) + (size_t)i * Hk * D, static_cast<T*>(a.k_pool),
-                          static_cast<T*>(a.v_pool),
+                          static_cast<const T*>(a.v_new) + (size_t)i * Hk * D, pool_slot<T>(a.k_pool, pg, Hk, off, D),
+                          pool_slot<T>(a.v_pool, pg, Hk, off, D), (size_t)kPageSize * D,
                           rope ? static_cast<const T*>(a.rope_cos) + (size_t)pos * D : nullptr,
-                          rope ? static_cast<const T*>(a.rope_sin) + (size_t)pos * D : nullptr, Hq, Hk, D,
-                          page_ok, page, slot >= 0 ? slot % kPageSize : 0);
+                          rope ? static_cast<const T*>(a.rope_sin) + (size_t)pos * D : nullptr, Hq, Hk, D, page_ok);
+}
+
+// ---------------------------------------------------------------------------
+// Packed sequences (Llama example page, `packed`): the pack is read as a
+// contiguous cache of 64-token key blocks.  Tiles are runs of one segment id
+// cut into tile_tokens.  When the pack is canonical (every segment id forms a
+// single run, positions strictly increase along it) a tile visits the blocks
+// from its run's start (or its window) to its own last token; otherwise every
+// tile visits the whole pack, and the per-key mask alone decides.
+// ---------------------------------------------------------------------------
+constexpr int kPkHash = 2048;        // segment ids of runs, open addressing
+constexpr int kPkRunsCap = kPkHash / 2;
+
+__device__ __forceinline__ void pk_hash_insert(unsigned long long* tab, int id, int* noncanon) {
+    const unsigned long long key = (1ull << 32) | (unsigned)id;
+    unsigned h = ((unsigned)id * 2654435761u) & (kPkHash - 1);
+    for (int probe = 0; probe < kPkHash; ++probe) {
+        const unsigned long long prev = atomicCAS(&tab[h], 0ull, key);
+        if (prev == 0ull) return;
+        if (prev == key) {          // a second run of the same sequence
+            *noncanon = 1;
+            return;
+        }
+        h = (h + 1) & (kPkHash - 1);
+    }
+    *noncanon = 1;
+}
+
+__device__ void build_packed_plan(const PrefillPrepArgs& a) {
+    __shared__ int s_warp[32];
+    __shared__ int s_off[kPfBuckets];
+    __shared__ int s_bad, s_noncanon, s_runs;
+    __shared__ unsigned long long s_ids[kPkHash];
+    const int tid = threadIdx.x, n = a.n_tokens, Tq = a.tile_tokens, W = a.window;
+    const int n64 = (n + kPageSize - 1) / kPageSize * kPageSize;
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(a.ws + a.L.ctrl);
+    PfTile* raw = reinterpret_cast<PfTile*>(a.ws + a.L.tiles_raw);
+    PfTile* tiles = reinterpret_cast<PfTile*>(a.ws + a.L.tiles);
+    int* seg_pad = reinterpret_cast<int*>(a.ws + a.L.seg_pad);
+    int* pos_pad = reinterpret_cast<int*>(a.ws + a.L.pos_pad);
+    int4* blk = reinterpret_cast<int4*>(a.ws + a.L.blk);
+    for (int b = tid; b < kPfBuckets; b += blockDim.x) s_off[b] = 0;
+    for (int b = tid; b < kPkHash; b += blockDim.x) s_ids[b] = 0ull;
+    if (tid == 0) { s_bad = 0; s_noncanon = 0; s_runs = 0; }
+    __syncthreads();
+
+    int carry_run = 0, n_tiles = 0;
+    bool bad = false;
+    static_assert(kPageSize % kPerThread == 0 || kPerThread % kPageSize == 0, "block summaries pair threads");
+    for (int base = 0; base < n64; base += kPrepThreads * kPerThread) {
+        const int i0 = base + tid * kPerThread;
+        int r[kPerThread], ps[kPerThread];
+        #pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+            const int i = i0 + k;
+            r[k] = i < n ? __ldg(a.row_of + i) : 0;
+            ps[k] = i < n ? __ldg(a.positions + i) : INT_MAX;
+            if (i < n64) {
+                seg_pad[i] = r[k];
+                pos_pad[i] = ps[k];
+            }
+        }
+        const int r_before = (i0 > 0 && i0 < n) ? __ldg(a.row_of + i0 - 1) : 0;
+        const int p_before = (i0 > 0 && i0 < n) ? __ldg(a.positions + i0 - 1) : 0;
+        unsigned run_starts = 0;
+        int last_start = -1;
+        bool uniform = i0 + kPerThread <= n, noncanon = false;
+        int pmin = INT_MAX, pmax = INT_MIN;
+        #pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+            const int i = i0 + k;
+            if (i >= n) continue;
+            if (ps[k] < 0 || (a.rope_cos && ps[k] >= a.rope_len)) bad = true;
+            const bool start = i == 0 || r[k] != (k ? r[k - 1] : r_before);
+            if (start) {
+                run_starts |= 1u << k;
+                last_start = i;
+                if (atomicAdd(&s_runs, 1) >= kPkRunsCap) noncanon = true;
+                else pk_hash_insert(s_ids, r[k], &s_noncanon);
+            } else if (ps[k] <= (k ? ps[k - 1] : p_before)) {
+                noncanon = true;
+            }
+            if (r[k] != r[0]) uniform = false;
+            pmin = min(pmin, ps[k]);
+            pmax = max(pmax, ps[k]);
+        }
+        if (noncanon) atomicOr(&s_noncanon, 1);
+        // summaries of 64-token blocks: threads 2b and 2b + 1 of a pass share one
+        {
+            const int o_seg = __shfl_xor_sync(0xffffffffu, r[0], 1);
+            const int o_uni = __shfl_xor_sync(0xffffffffu, uniform ? 1 : 0, 1);
+            const int o_min = __shfl_xor_sync(0xffffffffu, pmin, 1);
+            const int o_max = __shfl_xor_sync(0xffffffffu, pmax, 1);
+            if ((tid & 1) == 0 && i0 < n) {
+                const int u = uniform && o_uni && o_seg == r[0];
+                blk[i0 / kPageSize] = make_int4(u, r[0], min(pmin, o_min), max(pmax, o_max));
+            }
+        }
+        int block_last;
+        int rs = block_scan_excl<true>(last_start, -1, s_warp, &block_last);
+        rs = max(rs, carry_run);
+        unsigned tile_starts = 0;
+        int tile_run[kPerThread / 8 > 0 ? 1 : 1];
+        (void)tile_run;
+        int starts_rs[kPerThread];
+        #pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+            const int i = i0 + k;
+            starts_rs[k] = rs;
+            if (i >= n) continue;
+            if (run_starts >> k & 1) rs = i;
+            starts_rs[k] = rs;
+            if ((i - rs) % Tq == 0) tile_starts |= 1u << k;
+        }
+        int chunk_tiles;
+        int id = n_tiles + block_scan_excl<false>(__popc(tile_starts), 0, s_warp, &chunk_tiles);
+        #pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+            if (tile_starts >> k & 1) {
+                int4* dst = reinterpret_cast<int4*>(raw + id);
+                dst[0] = make_int4(i0 + k, 0, r[k], 0);
+                dst[1] = make_int4(0, 0, 0, starts_rs[k]);   // .pad = start of the tile's run
+                ++id;
+            }
+        }
+        carry_run = max(carry_run, block_last);
+        n_tiles += chunk_tiles;
+    }
+    if (bad) atomicOr(&s_bad, 1);
+    __syncthreads();
+    const bool canonical = s_noncanon == 0;
+
+    // key blocks of each tile; histogram of sizes
+    for (int b = tid; b < n_tiles; b += blockDim.x) {
+        const int t0 = raw[b].t0, t1 = b + 1 < n_tiles ? raw[b + 1].t0 : n, run0 = raw[b].pad;
+        int kf = 0, kl = n - 1;
+        if (canonical) {
+            kl = t1 - 1;
+            kf = W > 0 ? max(run0, t0 - W + 1) : run0;
+        }
+        const int first = kf / kPageSize, npg = kl / kPageSize - first + 1;
+        raw[b].ntok = t1 - t0;
+        raw[b].first_page = first;
+        raw[b].npg = npg;
+        raw[b].lo_min = kf;
+        raw[b].pos_max = kl;
+        atomicAdd(&s_off[npg < kPfBuckets ? npg : kPfBuckets - 1], 1);
+    }
+    __syncthreads();
+    {
+        constexpr int per = kPfBuckets / kPrepThreads;
+        int h[per];
+        int sum = 0;
+        #pragma unroll
+        for (int k = 0; k < per; ++k) {
+            h[k] = s_off[kPfBuckets - 1 - (tid * per + k)];
+            sum += h[k];
+        }
+        int total;
+        int off = block_scan_excl<false>(sum, 0, s_warp, &total);
+        #pragma unroll
+        for (int k = 0; k < per; ++k) {
+            s_off[kPfBuckets - 1 - (tid * per + k)] = off;
+            off += h[k];
+        }
+    }
+    __syncthreads();
+    for (int b = tid; b < n_tiles; b += blockDim.x) {
+        const int4* src = reinterpret_cast<const int4*>(raw + b);
+        const int4 d0 = src[0], d1 = src[1];
+        const int at = atomicAdd(&s_off[d1.x < kPfBuckets ? d1.x : kPfBuckets - 1], 1);
+        int4* dst = reinterpret_cast<int4*>(tiles + at);
+        dst[0] = d0;
+        dst[1] = d1;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        if (s_bad) set_error(ctrl, kErrBadPos);
+        ctrl->n_items = s_bad ? 0 : n_tiles;
+        ctrl->kv_heads = a.kv_heads;
+        ctrl->group = a.heads / a.kv_heads;
+        ctrl->head_dim = a.head_dim;
+        ctrl->rows = canonical ? 1 : 0;    // recorded for inspection
+        ctrl->magic = kPlanMagic;
+    }
+}
+
+__global__ void __launch_bounds__(kPrepThreads) packed_plan_kernel(const __grid_constant__ PrefillPrepArgs a) {
+    griddep_launch_dependents();
+    build_packed_plan(a);
+}
+
+// Block i rotates q and k of packed token i into the workspace.
+template <typename T>
+__global__ void __launch_bounds__(128) packed_rope_kernel(const __grid_constant__ PrefillPrepArgs a) {
+    griddep_launch_dependents();
+    const int i = blockIdx.x, D = a.head_dim, Hq = a.heads, Hk = a.kv_heads;
+    const int pos = __ldg(a.positions + i);
+    const bool rope = a.rope_cos != nullptr;
+    if (pos < 0 || (rope && pos >= a.rope_len)) {
+        if (threadIdx.x == 0) set_error(reinterpret_cast<Ctrl*>(a.ws + a.L.ctrl), kErrBadPos);
+    } else {
+        rope_write_vectors<T>(static_cast<const T*>(a.q) + (size_t)i * Hq * D,
+                              reinterpret_cast<T*>(a.ws + a.L.q_rot) + (size_t)i * Hq * D,
+                              static_cast<const T*>(a.k_new) + (size_t)i * Hk * D, nullptr,
+                              reinterpret_cast<T*>(a.ws + a.L.k_rot) + (size_t)i * Hk * D, nullptr, (size_t)D,
+                              rope ? static_cast<const T*>(a.rope_cos) + (size_t)pos * D : nullptr,
+                              rope ? static_cast<const T*>(a.rope_sin) + (size_t)pos * D : nullptr, Hq, Hk, D, true);
+    }
+    griddep_wait();
 }
 
 // The tile list: one block.  Lets the rope kernel launched after it start
@@ -713,6 +930,23 @@ cudaError_t launch_prefill_prep(const PrefillPrepArgs& a, int dtype, cudaStream_
     cfg.numAttrs = 1;
     if (dtype == 0) return cudaLaunchKernelEx(&cfg, prefill_rope_kernel<__nv_bfloat16>, a);
     return cudaLaunchKernelEx(&cfg, prefill_rope_kernel<float>, a);
+}
+
+cudaError_t launch_packed_prep(const PrefillPrepArgs& a, int dtype, cudaStream_t stream) {
+    if (a.n_tokens <= 0 || dtype != 0) return a.n_tokens <= 0 ? cudaSuccess : cudaErrorInvalidValue;
+    packed_plan_kernel<<<1, kPrepThreads, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.n_tokens);
+    cfg.blockDim = dim3(128);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, packed_rope_kernel<__nv_bfloat16>, a);
 }
 
 }  // namespace pdattn

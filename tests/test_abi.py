@@ -157,3 +157,20 @@ def test_prefill_host_validation(lib):
     n = lib.lib.pdattn_prefill_workspace_size(ctypes.byref(p), 1000)
     assert n >= 256 + 2 * 32 * 1000 + 2 * 1000 * 8 * 64 and n % 256 == 0
     assert lib.lib.pdattn_prefill_workspace_size(ctypes.byref(p), -1) == 0
+
+
+def test_packed_host_validation(lib):
+    import torch
+    null = ctypes.c_void_p(0)
+    f = lib.lib.pdattn_packed
+    p = _p(lib, dtype=torch.float32)
+    assert f(ctypes.byref(p), 4, *([null] * 7), 0, null) == 2         # tensor-core path: bf16 only
+    p = _p(lib, pages_per_row=0, num_pages=0)                           # cache fields are not read
+    assert f(ctypes.byref(p), -1, *([null] * 7), 0, null) == 1
+    assert f(ctypes.byref(p), 0, *([null] * 7), 0, null) == 0
+    assert lib.lib.pdattn_last_launch_count() == 0
+    assert f(ctypes.byref(p), 4, *([null] * 7), 0, null) == 1
+    assert b"NULL" in lib.lib.pdattn_last_error()
+    n = lib.lib.pdattn_packed_workspace_size(ctypes.byref(p), 1000)
+    # control, two tile lists, rotated q and k, padded ids and positions, block summaries
+    assert n >= 256 + 2 * 32 * 1000 + 2 * 1000 * (8 + 2) * 64 + 2 * 4 * 1024 + 16 * 16 and n % 256 == 0
