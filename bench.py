@@ -21,7 +21,9 @@ Default workload: the Llama-3.1-8B serving batch (256 rows, 32 query heads,
 --workload llama8b_prefill measures the paged prefill instead (8 rows x 1024
 new tokens on cached prefixes 0 .. 7168, Llama-3.1-8B attention shape): value
 = attention TFLOP/s of whole prefill calls (4 * D * heads * visible keys per
-token), roofline against the measured bf16 tensor peak.
+token), roofline against the measured bf16 tensor peak.  --workload
+llama8b_packed measures packed sequences the same way (one 8192-token row of
+eight sequences, no cache).
 """
 import argparse
 import glob
@@ -670,6 +672,177 @@ def run_prefill_reference(args, w, world, rank):
     }
 
 
+# ----------------------------------------------------------------- packed --
+PACKED_METRIC = "packed-sequence attention TFLOP/s (% of GB300 bf16 tensor peak)"
+
+
+def packed_flops(w, positions):
+    """4 * D * heads per visible (query, key) pair; sequences start at position 0."""
+    return sum(4 * w.head_dim * w.heads * (min(int(p) + 1, w.window) if w.window > 0 else int(p) + 1)
+               for p in positions)
+
+
+def cpu_oracle_packed_rate(w, host, budget_s, max_seqs=None):
+    """The oracle's packed attention on whole sequences of the row, shortest
+    first, for about budget_s; returns (TFLOP/s, seconds, description, sequences)."""
+    import numpy as np
+    import oracle
+    shape = oracle.make_shape(0, w.heads, w.kv_heads, w.head_dim, 1, 1, oracle.BF16, window=w.window,
+                              rope_theta=w.rope_theta)
+    starts = np.concatenate([[0], np.cumsum(w.lengths)])
+    flops, spent, done = 0, 0.0, 0
+    for s in np.argsort(w.lengths):
+        lo, hi = starts[s], starts[s + 1]
+        sub = {k: np.ascontiguousarray(host[k][lo:hi]) for k in ("q", "k", "v", "positions", "segments")}
+        t0 = time.perf_counter()
+        _, _, _, _, rc = oracle.packed(shape, sub["q"], sub["k"], sub["v"], sub["positions"], sub["segments"])
+        spent += time.perf_counter() - t0
+        assert rc == 0
+        flops += packed_flops(w, sub["positions"])
+        done += 1
+        if (max_seqs and done >= max_seqs) or (not max_seqs and spent >= budget_s):
+            break
+    desc = f"oracle packed attention of the {done} shortest of {len(w.lengths)} sequences, single thread"
+    return flops / spent / 1e12, spent, desc, done
+
+
+def run_packed(args, w, world, rank, local):
+    from paged_gqa_decode_step_gb300 import build
+    build.build()
+    from paged_gqa_decode_step_gb300 import binding as b
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    t = wl.generate_packed(w, dev, seed=rank_seed(w, rank))
+    P = w.tokens
+    pos_list = t["positions"].cpu().tolist()
+    cos, sin = b.rope_tables(w.rope_theta, w.head_dim, w.max_seq, torch.bfloat16)
+    p = b.make_params(1, w.heads, w.kv_heads, w.head_dim, 1, 1, torch.bfloat16, window=w.window, rope_cos=cos,
+                      rope_sin=sin)
+    ws = b.new_packed_workspace(p, P)
+    out = torch.empty_like(t["q"])
+    flops = packed_flops(w, pos_list)
+    flush = torch.empty(4 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+    names = ("q", "k", "v", "positions", "segments")
+
+    def step():
+        b.packed(p, *(t[k] for k in names), out, ws)
+
+    for _ in range(args.warmup):
+        step()
+    b.check_status(ws)
+    launches_per_step = b.last_launch_count()
+
+    def timed(fn, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize()
+        for e0, e1 in evs:
+            flush.fill_(1)
+            e0.record()
+            fn()
+            e1.record()
+        torch.cuda.synchronize()
+        return sum(e0.elapsed_time(e1) for e0, e1 in evs) / n
+
+    with ClockSampler(dev) as clocks:
+        barrier(world)
+        ms = timed(step, args.steps)
+        barrier(world)
+    clk = clocks.summary()
+    b.check_status(ws)
+    if args.quick:
+        if rank == 0:
+            print(json.dumps({"quick": True, "workload": w.name, "ms_per_step": ms,
+                              "tflops": flops / (ms * 1e-3) / 1e12}), flush=True)
+        return None
+    ms = max_over_ranks(ms, world)
+    all_flops = sum_over_ranks(flops, world)
+    value = all_flops / (ms * 1e-3) / 1e12
+
+    att_ms = timed(lambda: b.packed_attend(p, t["v"], t["positions"], out, ws), max(20, min(args.steps, 200)))
+    b.check_status(ws)
+    peak, peak_kind = measured_tensor_peak()
+    achieved = flops / (att_ms * 1e-3) / 1e12
+
+    host_in = {k: t[k].cpu().pin_memory() for k in names}
+    dev_in = {k: torch.empty_like(t[k]) for k in host_in}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    stream = torch.cuda.current_stream()
+
+    def e2e_step():
+        for k in host_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        b.packed(p, *(dev_in[k] for k in names), out, ws)
+        host_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    n_e2e = max(10, min(args.steps, 100))
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        e2e_step()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, world)
+    b.check_status(ws)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = {k: wl.to_numpy(v) for k, v in t.items()}
+        rate, spent, desc, _ = cpu_oracle_packed_rate(w, host, args.cpu_baseline_seconds)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": desc,
+               "seconds": round(spent, 2), "cpu": cpu_model()}
+    if rank != 0:
+        return None
+    return {
+        "metric": PACKED_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) q/k/v)",
+        "config": {
+            "workload": w.name, "tokens_per_gpu": P, "lengths": list(w.lengths), "heads": w.heads,
+            "kv_heads": w.kv_heads, "head_dim": w.head_dim, "window": w.window, "rope_theta": w.rope_theta,
+            "flops_per_step_per_gpu": flops,
+            "l2": "L2 flushed (512 MB write) between timed steps, outside the events",
+            "parallelism": f"replicas x{world} (rows sharded across ranks, no exchange)",
+        },
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": f"prefill_kernel<{w.head_dim},packed>",
+                     "flops_per_launch": flops, "launch_us": att_ms * 1e3, "peak_kind": peak_kind},
+        "cpu_baseline": cpu,
+        "e2e": {"value": all_flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+
+
+def run_packed_reference(args, w, world, rank):
+    if rank != 0:
+        return None
+    t = wl.generate_packed(w, "cpu", seed=rank_seed(w, 0))
+    host = {k: wl.to_numpy(v) for k, v in t.items()}
+    del t
+    rates, spent_all, seqs = [], 0.0, 0
+    for _ in range(max(1, args.steps)):
+        r, spent, desc, n = cpu_oracle_packed_rate(w, host, 0, max_seqs=2)
+        rates.append(r)
+        spent_all += spent
+        seqs += n
+    rate = sum(rates) / len(rates)
+    return {
+        "metric": PACKED_METRIC, "value": rate, "unit": "TFLOP/s", "n_gpus": world, "steps": len(rates),
+        "warmup": args.warmup, "ms_per_step": spent_all / len(rates) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name, "sequences_per_step": 2, "tokens": w.tokens},
+        "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": desc, "value": rate, "unit": "TFLOP/s",
+                         "cpu": cpu_model()},
+        "e2e": {"value": rate, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -677,7 +850,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_serving",
-                    choices=sorted(wl.WORKLOADS) + sorted(wl.PREFILL_WORKLOADS))
+                    choices=sorted(wl.WORKLOADS) + sorted(wl.PREFILL_WORKLOADS) + sorted(wl.PACKED_WORKLOADS))
     ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--chunk-pages", type=int, default=0,
@@ -688,12 +861,17 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_setup()
-    if args.workload in wl.PREFILL_WORKLOADS:
-        w = wl.PREFILL_WORKLOADS[args.workload]
-        if args.impl == "reference":
-            line = run_prefill_reference(args, w, world, rank)
+    if args.workload in wl.PREFILL_WORKLOADS or args.workload in wl.PACKED_WORKLOADS:
+        if args.workload in wl.PREFILL_WORKLOADS:
+            w = wl.PREFILL_WORKLOADS[args.workload]
+            ref, ours = run_prefill_reference, run_prefill
         else:
-            line = run_prefill(args, w, world, rank, local)
+            w = wl.PACKED_WORKLOADS[args.workload]
+            ref, ours = run_packed_reference, run_packed
+        if args.impl == "reference":
+            line = ref(args, w, world, rank)
+        else:
+            line = ours(args, w, world, rank, local)
         if line is not None:
             print(json.dumps(line), flush=True)
         if world > 1:

@@ -253,6 +253,16 @@ pdattn_status pdattn_packed(const pdattn_params* p, int32_t n_tokens, const void
                             void* out, void* workspace, size_t workspace_bytes, pdattn_stream stream);
 
 /*
+ * The attention half of pdattn_packed alone: re-runs it over the rotated q
+ * and k and the tile list that the last pdattn_packed call on this
+ * workspace left there, with the same parameters, n_tokens, v and
+ * positions (for timing the attention, or attending again).
+ */
+pdattn_status pdattn_packed_attend(const pdattn_params* p, int32_t n_tokens, const void* v,
+                                   const int32_t* positions, void* out, void* workspace,
+                                   size_t workspace_bytes, pdattn_stream stream);
+
+/*
  * Synchronises `stream`, reads the workspace's device status word, clears
  * it and returns the first error it recorded (PDATTN_OK if none).
  */

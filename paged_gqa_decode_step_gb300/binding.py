@@ -56,6 +56,7 @@ def _load():
         "pdattn_prefill_attend": (i32, [P, i32] + [vp] * 6 + [sz, vp]),
         "pdattn_packed_workspace_size": (sz, [P, i32]),
         "pdattn_packed": (i32, [P, i32] + [vp] * 7 + [sz, vp]),
+        "pdattn_packed_attend": (i32, [P, i32] + [vp] * 4 + [sz, vp]),
         "pdattn_check_status": (i32, [vp, vp]),
         "pdattn_last_error": (ctypes.c_char_p, []),
         "pdattn_last_launch_count": (i32, []),
@@ -265,6 +266,16 @@ def packed(p, q, k, v, positions, segments, out, ws, stream=None):
     w, nb = _ws(ws)
     _check(lib.pdattn_packed(ctypes.byref(p), n, _ptr(q), _ptr(k), _ptr(v), _ptr(positions), _ptr(segments),
                              _ptr(out), w, nb, _stream(stream)))
+
+
+def packed_attend(p, v, positions, out, ws, stream=None):
+    """Attention half of packed, over what its last call left in ws."""
+    n = out.shape[0] if isinstance(out, torch.Tensor) else -1
+    _expect("positions", positions, (n,), torch.int32)
+    _expect("v", v, (n, p.kv_heads, p.head_dim), _dt(p))
+    _expect("out", out, (n, p.heads, p.head_dim), _dt(p))
+    w, nb = _ws(ws)
+    _check(lib.pdattn_packed_attend(ctypes.byref(p), n, _ptr(v), _ptr(positions), _ptr(out), w, nb, _stream(stream)))
 
 
 def check_status(ws, stream=None):

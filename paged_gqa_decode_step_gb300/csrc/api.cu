@@ -495,16 +495,19 @@ size_t pdattn_packed_workspace_size(const pdattn_params* p, int32_t n_tokens) {
     return pk_layout(n_tokens, p->heads, p->kv_heads, p->head_dim, 2).total;
 }
 
-pdattn_status pdattn_packed(const pdattn_params* p, int32_t n_tokens, const void* q, const void* k, const void* v,
-                            const int32_t* positions, const int32_t* segments, void* out, void* workspace,
-                            size_t workspace_bytes, pdattn_stream stream) {
+// Shared body of the packed entry points; with_prep false re-runs the
+// attention only, over the tile list and rotated q and k in the workspace.
+static pdattn_status packed_impl(const pdattn_params* p, int32_t n_tokens, const void* q, const void* k,
+                                 const void* v, const int32_t* positions, const int32_t* segments, void* out,
+                                 void* workspace, size_t workspace_bytes, pdattn_stream stream, bool with_prep) {
     g_launches = 0;
     pdattn_status s = check_packed_params(p);
     if (s != PDATTN_OK) return s;
     if (n_tokens < 0) return fail(PDATTN_EINVAL, "n_tokens < 0");
     if (n_tokens == 0) return PDATTN_OK;
-    if (!q || !k || !v || !positions || !segments || !out) return fail(PDATTN_EINVAL, "NULL data pointer");
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    if (!v || !positions || !out || (with_prep && (!q || !k || !segments)))
+        return fail(PDATTN_EINVAL, "NULL data pointer");
+    if (!aligned16(v) || !aligned16(out) || (with_prep && (!aligned16(q) || !aligned16(k))))
         return fail(PDATTN_EINVAL, "q, k, v and out must be 16-byte aligned");
     if (!workspace) return fail(PDATTN_EINVAL, "workspace is NULL");
     if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
@@ -555,8 +558,11 @@ pdattn_status pdattn_packed(const pdattn_params* p, int32_t n_tokens, const void
     pa.rope_sin = p->rope_sin;
     pa.ws = ws;
     pa.L = L;
-    cudaError_t e = launch_packed_prep(pa, p->dtype, (cudaStream_t)stream);
-    if (e != cudaSuccess) return cuda_fail(e, "packed plan/rope launch");
+    cudaError_t e = cudaSuccess;
+    if (with_prep) {
+        e = launch_packed_prep(pa, p->dtype, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "packed plan/rope launch");
+    }
 
     PrefillArgs aa = {};
     aa.n_tokens = n_tokens;
@@ -576,8 +582,20 @@ pdattn_status pdattn_packed(const pdattn_params* p, int32_t n_tokens, const void
     const long long units = (long long)n_tokens * p->kv_heads;
     e = launch_packed(aa, qm, km, vm, (int)(units < sms ? units : sms), (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "packed attention launch");
-    g_launches = 3;
+    g_launches = with_prep ? 3 : 1;
     return PDATTN_OK;
+}
+
+pdattn_status pdattn_packed(const pdattn_params* p, int32_t n_tokens, const void* q, const void* k, const void* v,
+                            const int32_t* positions, const int32_t* segments, void* out, void* workspace,
+                            size_t workspace_bytes, pdattn_stream stream) {
+    return packed_impl(p, n_tokens, q, k, v, positions, segments, out, workspace, workspace_bytes, stream, true);
+}
+
+pdattn_status pdattn_packed_attend(const pdattn_params* p, int32_t n_tokens, const void* v, const int32_t* positions,
+                                   void* out, void* workspace, size_t workspace_bytes, pdattn_stream stream) {
+    return packed_impl(p, n_tokens, nullptr, nullptr, v, positions, nullptr, out, workspace, workspace_bytes, stream,
+                       false);
 }
 
 pdattn_status pdattn_check_status(void* workspace, pdattn_stream stream) {

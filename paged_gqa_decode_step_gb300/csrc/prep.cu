@@ -485,16 +485,64 @@ __device__ int block_scan_excl(int v, int identity, int* s_warp, int* total) {
     return ex;
 }
 
-// One block of kPrepThreads threads; each thread holds kPerThread
-// consecutive tokens in registers, so a pass over up to
-// kPrepThreads * kPerThread tokens costs one global round trip.
-constexpr int kPrepThreads = 256;
-constexpr int kPerThread = 32;
+// The planners run as one block of kPrepThreads threads over chunks of
+// kChunk tokens.  A chunk's row (or segment) ids and positions are staged in
+// shared memory with coalesced loads, padded by one word every 32 so that
+// each thread then reads its kPerThread consecutive tokens without bank
+// conflicts.
+constexpr int kPrepThreads = 512;
+constexpr int kPerThread = 8;
+constexpr int kChunk = kPrepThreads * kPerThread;
+constexpr int kChunkPad = kChunk + kChunk / 32;
+
+__device__ __forceinline__ int pad_idx(int i) { return i + (i >> 5); }
+
+// Stages ids[base .. base + kChunk) and pos[...] (fill values past n).
+__device__ __forceinline__ void stage_chunk(const int* __restrict__ ids, const int* __restrict__ pos, int base, int n,
+                                            int id_fill, int pos_fill, int* s_id, int* s_pos) {
+    for (int idx = threadIdx.x; idx < kChunk; idx += blockDim.x) {
+        const int i = base + idx;
+        s_id[pad_idx(idx)] = i < n ? __ldg(ids + i) : id_fill;
+        s_pos[pad_idx(idx)] = i < n ? __ldg(pos + i) : pos_fill;
+    }
+}
+
+// Counting sort of the tile descriptors by pages, largest first (bucket
+// kPfBuckets - 1 first); s_off holds the histogram on entry.
+__device__ void sort_tiles(const PfTile* raw, PfTile* tiles, int n_tiles, int* s_off, int* s_warp) {
+    const int tid = threadIdx.x;
+    constexpr int per = kPfBuckets / kPrepThreads;   // buckets per thread
+    int h[per];
+    int sum = 0;
+    #pragma unroll
+    for (int k = 0; k < per; ++k) {
+        h[k] = s_off[kPfBuckets - 1 - (tid * per + k)];
+        sum += h[k];
+    }
+    int total;
+    int off = block_scan_excl<false>(sum, 0, s_warp, &total);
+    #pragma unroll
+    for (int k = 0; k < per; ++k) {
+        s_off[kPfBuckets - 1 - (tid * per + k)] = off;
+        off += h[k];
+    }
+    __syncthreads();
+    for (int b = tid; b < n_tiles; b += blockDim.x) {
+        const int4* src = reinterpret_cast<const int4*>(raw + b);
+        const int4 d0 = src[0], d1 = src[1];
+        const int at = atomicAdd(&s_off[d1.x < kPfBuckets ? d1.x : kPfBuckets - 1], 1);
+        int4* dst = reinterpret_cast<int4*>(tiles + at);
+        dst[0] = d0;
+        dst[1] = d1;
+    }
+    __syncthreads();
+}
 
 __device__ void build_prefill_plan(const PrefillPrepArgs& a) {
     __shared__ int s_warp[32];
     __shared__ int s_off[kPfBuckets];
     __shared__ int s_bad;
+    __shared__ int s_id[kChunkPad], s_pos[kChunkPad];
     const int tid = threadIdx.x, n = a.n_tokens, Tq = a.tile_tokens;
     const int max_pos = a.pages_per_row * kPageSize;
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(a.ws + a.L.ctrl);
@@ -502,23 +550,23 @@ __device__ void build_prefill_plan(const PrefillPrepArgs& a) {
     PfTile* tiles = reinterpret_cast<PfTile*>(a.ws + a.L.tiles);
     for (int b = tid; b < kPfBuckets; b += blockDim.x) s_off[b] = 0;
     if (tid == 0) s_bad = 0;
-    __syncthreads();
 
     // 1. tile starts: a token starts a tile when it starts a run of its row
     //    or lies a multiple of Tq tokens after its run's start; each tile's
     //    visible positions [lo_min, pos_max] by atomics on its descriptor.
-    int carry_run = 0, n_tiles = 0;
+    int carry_run = 0, n_tiles = 0, id_before = -1;
     bool bad = false;
-    for (int base = 0; base < n; base += kPrepThreads * kPerThread) {
+    for (int base = 0; base < n; base += kChunk) {
+        stage_chunk(a.row_of, a.positions, base, n, -1, 0, s_id, s_pos);
+        __syncthreads();
         const int i0 = base + tid * kPerThread;
         int r[kPerThread], ps[kPerThread];
         #pragma unroll
         for (int k = 0; k < kPerThread; ++k) {
-            const int i = i0 + k;
-            r[k] = i < n ? __ldg(a.row_of + i) : -1;
-            ps[k] = i < n ? __ldg(a.positions + i) : 0;
+            r[k] = s_id[pad_idx(tid * kPerThread + k)];
+            ps[k] = s_pos[pad_idx(tid * kPerThread + k)];
         }
-        const int r_before = (i0 > 0 && i0 < n) ? __ldg(a.row_of + i0 - 1) : -1;
+        const int r_before = tid > 0 ? s_id[pad_idx(tid * kPerThread - 1)] : id_before;
         unsigned run_starts = 0;
         int last_start = -1;
         #pragma unroll
@@ -555,7 +603,8 @@ __device__ void build_prefill_plan(const PrefillPrepArgs& a) {
                 ++id;
             }
         }
-        __syncthreads();   // descriptors initialised before the atomics below
+        id_before = s_id[pad_idx(kChunk - 1)];
+        __syncthreads();   // descriptors initialised before the atomics below; staging free
         int cur = first_id - 1, lmin = INT_MAX, pmax = -1;
         #pragma unroll
         for (int k = 0; k < kPerThread; ++k) {
@@ -594,35 +643,7 @@ __device__ void build_prefill_plan(const PrefillPrepArgs& a) {
         atomicAdd(&s_off[npg < kPfBuckets ? npg : kPfBuckets - 1], 1);
     }
     __syncthreads();
-
-    // 3. counting sort, largest first: bucket kPfBuckets-1 first
-    {
-        constexpr int per = kPfBuckets / kPrepThreads;   // buckets per thread
-        int h[per];
-        int sum = 0;
-        #pragma unroll
-        for (int k = 0; k < per; ++k) {
-            h[k] = s_off[kPfBuckets - 1 - (tid * per + k)];
-            sum += h[k];
-        }
-        int total;
-        int off = block_scan_excl<false>(sum, 0, s_warp, &total);
-        #pragma unroll
-        for (int k = 0; k < per; ++k) {
-            s_off[kPfBuckets - 1 - (tid * per + k)] = off;
-            off += h[k];
-        }
-    }
-    __syncthreads();
-    for (int b = tid; b < n_tiles; b += blockDim.x) {
-        const int4* src = reinterpret_cast<const int4*>(raw + b);
-        const int4 d0 = src[0], d1 = src[1];
-        const int at = atomicAdd(&s_off[d1.x < kPfBuckets ? d1.x : kPfBuckets - 1], 1);
-        int4* dst = reinterpret_cast<int4*>(tiles + at);
-        dst[0] = d0;
-        dst[1] = d1;
-    }
-    __syncthreads();
+    sort_tiles(raw, tiles, n_tiles, s_off, s_warp);
     if (tid == 0) {
         if (s_bad) set_error(ctrl, kErrBadPos);
         ctrl->n_items = s_bad ? 0 : n_tiles;
@@ -665,7 +686,7 @@ __device__ void rope_write_token(const PrefillPrepArgs& a, int i) {
 // from its run's start (or its window) to its own last token; otherwise every
 // tile visits the whole pack, and the per-key mask alone decides.
 // ---------------------------------------------------------------------------
-constexpr int kPkHash = 2048;        // segment ids of runs, open addressing
+constexpr int kPkHash = 1024;        // segment ids of runs, open addressing
 constexpr int kPkRunsCap = kPkHash / 2;
 
 __device__ __forceinline__ void pk_hash_insert(unsigned long long* tab, int id, int* noncanon) {
@@ -688,6 +709,7 @@ __device__ void build_packed_plan(const PrefillPrepArgs& a) {
     __shared__ int s_off[kPfBuckets];
     __shared__ int s_bad, s_noncanon, s_runs;
     __shared__ unsigned long long s_ids[kPkHash];
+    __shared__ int s_id[kChunkPad], s_pos[kChunkPad];
     const int tid = threadIdx.x, n = a.n_tokens, Tq = a.tile_tokens, W = a.window;
     const int n64 = (n + kPageSize - 1) / kPageSize * kPageSize;
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(a.ws + a.L.ctrl);
@@ -699,29 +721,31 @@ __device__ void build_packed_plan(const PrefillPrepArgs& a) {
     for (int b = tid; b < kPfBuckets; b += blockDim.x) s_off[b] = 0;
     for (int b = tid; b < kPkHash; b += blockDim.x) s_ids[b] = 0ull;
     if (tid == 0) { s_bad = 0; s_noncanon = 0; s_runs = 0; }
-    __syncthreads();
 
-    int carry_run = 0, n_tiles = 0;
-    bool bad = false;
-    static_assert(kPageSize % kPerThread == 0 || kPerThread % kPageSize == 0, "block summaries pair threads");
-    for (int base = 0; base < n64; base += kPrepThreads * kPerThread) {
+    int carry_run = 0, n_tiles = 0, id_before = 0, pos_before = 0;
+    bool bad = false, noncanon = false;
+    static_assert(kPageSize % kPerThread == 0 && kPageSize / kPerThread <= 32, "a block's summary is one warp's");
+    constexpr int kLanesPerBlock = kPageSize / kPerThread;
+    for (int base = 0; base < n64; base += kChunk) {
+        stage_chunk(a.row_of, a.positions, base, n, 0, INT_MAX, s_id, s_pos);
+        __syncthreads();
+        // the padded copies read by the attention kernel, coalesced
+        for (int idx = tid; idx < kChunk && base + idx < n64; idx += blockDim.x) {
+            seg_pad[base + idx] = s_id[pad_idx(idx)];
+            pos_pad[base + idx] = s_pos[pad_idx(idx)];
+        }
         const int i0 = base + tid * kPerThread;
         int r[kPerThread], ps[kPerThread];
         #pragma unroll
         for (int k = 0; k < kPerThread; ++k) {
-            const int i = i0 + k;
-            r[k] = i < n ? __ldg(a.row_of + i) : 0;
-            ps[k] = i < n ? __ldg(a.positions + i) : INT_MAX;
-            if (i < n64) {
-                seg_pad[i] = r[k];
-                pos_pad[i] = ps[k];
-            }
+            r[k] = s_id[pad_idx(tid * kPerThread + k)];
+            ps[k] = s_pos[pad_idx(tid * kPerThread + k)];
         }
-        const int r_before = (i0 > 0 && i0 < n) ? __ldg(a.row_of + i0 - 1) : 0;
-        const int p_before = (i0 > 0 && i0 < n) ? __ldg(a.positions + i0 - 1) : 0;
+        const int r_before = tid > 0 ? s_id[pad_idx(tid * kPerThread - 1)] : id_before;
+        const int p_before = tid > 0 ? s_pos[pad_idx(tid * kPerThread - 1)] : pos_before;
         unsigned run_starts = 0;
         int last_start = -1;
-        bool uniform = i0 + kPerThread <= n, noncanon = false;
+        bool uniform = i0 + kPerThread <= n;
         int pmin = INT_MAX, pmax = INT_MIN;
         #pragma unroll
         for (int k = 0; k < kPerThread; ++k) {
@@ -741,33 +765,30 @@ __device__ void build_packed_plan(const PrefillPrepArgs& a) {
             pmin = min(pmin, ps[k]);
             pmax = max(pmax, ps[k]);
         }
-        if (noncanon) atomicOr(&s_noncanon, 1);
-        // summaries of 64-token blocks: threads 2b and 2b + 1 of a pass share one
+        // summary of each 64-token block from its kLanesPerBlock threads
         {
-            const int o_seg = __shfl_xor_sync(0xffffffffu, r[0], 1);
-            const int o_uni = __shfl_xor_sync(0xffffffffu, uniform ? 1 : 0, 1);
-            const int o_min = __shfl_xor_sync(0xffffffffu, pmin, 1);
-            const int o_max = __shfl_xor_sync(0xffffffffu, pmax, 1);
-            if ((tid & 1) == 0 && i0 < n) {
-                const int u = uniform && o_uni && o_seg == r[0];
-                blk[i0 / kPageSize] = make_int4(u, r[0], min(pmin, o_min), max(pmax, o_max));
+            int seg0 = r[0], uni_all = uniform ? 1 : 0, mn = pmin, mx = pmax;
+            const int lead = __shfl_sync(0xffffffffu, seg0, (tid & 31) & ~(kLanesPerBlock - 1));
+            uni_all = uni_all && seg0 == lead;
+            #pragma unroll
+            for (int d = 1; d < kLanesPerBlock; d <<= 1) {
+                uni_all &= __shfl_xor_sync(0xffffffffu, uni_all, d);
+                mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, d));
+                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, d));
             }
+            if ((tid & (kLanesPerBlock - 1)) == 0 && i0 < n) blk[i0 / kPageSize] = make_int4(uni_all, seg0, mn, mx);
         }
         int block_last;
         int rs = block_scan_excl<true>(last_start, -1, s_warp, &block_last);
         rs = max(rs, carry_run);
         unsigned tile_starts = 0;
-        int tile_run[kPerThread / 8 > 0 ? 1 : 1];
-        (void)tile_run;
         int starts_rs[kPerThread];
         #pragma unroll
         for (int k = 0; k < kPerThread; ++k) {
             const int i = i0 + k;
+            if (i < n && (run_starts >> k & 1)) rs = i;
             starts_rs[k] = rs;
-            if (i >= n) continue;
-            if (run_starts >> k & 1) rs = i;
-            starts_rs[k] = rs;
-            if ((i - rs) % Tq == 0) tile_starts |= 1u << k;
+            if (i < n && (i - rs) % Tq == 0) tile_starts |= 1u << k;
         }
         int chunk_tiles;
         int id = n_tiles + block_scan_excl<false>(__popc(tile_starts), 0, s_warp, &chunk_tiles);
@@ -780,10 +801,14 @@ __device__ void build_packed_plan(const PrefillPrepArgs& a) {
                 ++id;
             }
         }
+        id_before = s_id[pad_idx(kChunk - 1)];
+        pos_before = s_pos[pad_idx(kChunk - 1)];
         carry_run = max(carry_run, block_last);
         n_tiles += chunk_tiles;
+        __syncthreads();   // staging free for the next chunk
     }
     if (bad) atomicOr(&s_bad, 1);
+    if (noncanon) atomicOr(&s_noncanon, 1);
     __syncthreads();
     const bool canonical = s_noncanon == 0;
 
@@ -804,33 +829,7 @@ __device__ void build_packed_plan(const PrefillPrepArgs& a) {
         atomicAdd(&s_off[npg < kPfBuckets ? npg : kPfBuckets - 1], 1);
     }
     __syncthreads();
-    {
-        constexpr int per = kPfBuckets / kPrepThreads;
-        int h[per];
-        int sum = 0;
-        #pragma unroll
-        for (int k = 0; k < per; ++k) {
-            h[k] = s_off[kPfBuckets - 1 - (tid * per + k)];
-            sum += h[k];
-        }
-        int total;
-        int off = block_scan_excl<false>(sum, 0, s_warp, &total);
-        #pragma unroll
-        for (int k = 0; k < per; ++k) {
-            s_off[kPfBuckets - 1 - (tid * per + k)] = off;
-            off += h[k];
-        }
-    }
-    __syncthreads();
-    for (int b = tid; b < n_tiles; b += blockDim.x) {
-        const int4* src = reinterpret_cast<const int4*>(raw + b);
-        const int4 d0 = src[0], d1 = src[1];
-        const int at = atomicAdd(&s_off[d1.x < kPfBuckets ? d1.x : kPfBuckets - 1], 1);
-        int4* dst = reinterpret_cast<int4*>(tiles + at);
-        dst[0] = d0;
-        dst[1] = d1;
-    }
-    __syncthreads();
+    sort_tiles(raw, tiles, n_tiles, s_off, s_warp);
     if (tid == 0) {
         if (s_bad) set_error(ctrl, kErrBadPos);
         ctrl->n_items = s_bad ? 0 : n_tiles;
