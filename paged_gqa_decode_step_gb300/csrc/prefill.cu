@@ -14,8 +14,9 @@
 // 64 keys and per half:
 //   S  = Q K^T      tcgen05.mma M=128 N=64 K=D, fp32 accumulator in TMEM
 //   softmax         one thread per MMA row: mask, running max, exp2, sum
-//   P               bf16 in shared memory (128-byte swizzle, K-major)
-//   O += P V        tcgen05.mma M=128 N=D K=64, V page read MN-major
+//   P               bf16, written back into the S columns it came from
+//   O += P V        tcgen05.mma M=128 N=D K=64, P read from tensor memory,
+//                   V page read from shared memory MN-major
 // The MMA issuer interleaves the halves (S_A(j) S_B(j) PV_A(j-1) PV_B(j-1))
 // so that each half's softmax runs while the tensor core works for the
 // other; S is double-buffered per half.  The running max is raised lazily:
@@ -52,14 +53,13 @@ struct PfCfg {
     static constexpr int kStageBytes = 2 * kKvBytes;
     // packed mode keeps each stage's segment ids and positions (512 B) in
     // static shared memory, which costs D = 128 one stage
-    static constexpr int kStages = D == 128 ? (kPacked ? 3 : 4) : 8;
+    static constexpr int kStages = D == 128 ? (kPacked ? 4 : 5) : 10;
     static constexpr int kMaskStages = kPacked ? kStages : 1;
-    static constexpr int kPBytes = 16384;                 // 128 rows x 64 bf16, one per half
     static constexpr int kOffQ = 0;                       // halves A, B
     static constexpr int kOffStage = 2 * kQBytes;
-    static constexpr int kOffP = kOffStage + kStages * kStageBytes;
-    static constexpr int kSmem = kOffP + 2 * kPBytes + 1024;   // + alignment slack
-    // TMEM: S of half h, buffer b at column 128 h + 64 b; O of half h at 256 + h D.
+    static constexpr int kSmem = kOffStage + kStages * kStageBytes + 1024;   // + alignment slack
+    // TMEM: S of half h, buffer b at column 128 h + 64 b (its first 32 columns
+    // then hold P as bf16 pairs); O of half h at 256 + h D.
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColO = 256;
     static_assert(kSmem + kMaskStages * 512 <= 227 * 1024 - 1536, "shared memory budget");
@@ -95,6 +95,16 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t 
         "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.u32 p, %4, 0;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Same with A in tensor memory (a_tmem: row m = lane m, two bf16 per column).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -238,7 +248,7 @@ struct PfBars {
 // Softmax and epilogue of one half (128 threads, one MMA row each).
 template <int D, bool kPacked>
 __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile* tiles, int n_units, int half,
-                                             int quarter, int lane, uint32_t tmem, uint32_t st_s, uint32_t p_s,
+                                             int quarter, int lane, uint32_t tmem, uint32_t st_s,
                                              PfBars& bars, const int (*s_mask)[128], uint64_t* kv_full,
                                              volatile int* abort, Ctrl* ctrl) {
     using C = PfCfg<D, kPacked>;
@@ -249,7 +259,6 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
     const int m = quarter * 32 + lane;                    // MMA row = TMEM lane
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const uint32_t s_col = 128u * half, o_col = C::kColO + (uint32_t)(half * D);
-    const uint32_t pb = p_s + half * C::kPBytes;
     const int tq = m / g, jh = m % g;
     const float sl2 = a.scale_log2;
     const __nv_bfloat16* sinks = static_cast<const __nv_bfloat16*>(a.sinks);
@@ -359,12 +368,8 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
                 }
                 tmem_wait_st();
             }
-            #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8)
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                             ::"r"(swz128(pb, m, c8)), "r"(pk[4 * c8]), "r"(pk[4 * c8 + 1]), "r"(pk[4 * c8 + 2]),
-                               "r"(pk[4 * c8 + 3])
-                             : "memory");
+            // P over the first 32 columns of its S buffer (S already read)
+            tmem_st32(tmem + lane_base + s_col + (j & 1) * 64, pk);
             // V rows outside every row's range hold no cached value of this
             // tile (possibly stale or non-finite): half A zeroes them so that
             // 0 * V stays 0 (the issuer runs PV_B after PV_A).
@@ -379,7 +384,8 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
                                      : "memory");
                 }
             }
-            fence_proxy_async_shared();
+            fence_proxy_async_shared();   // zeroed V rows, read by the MMA
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(p_full);
         }
@@ -441,7 +447,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
-    const uint32_t q_s = sb + C::kOffQ, st_s = sb + C::kOffStage, p_s = sb + C::kOffP;
+    const uint32_t q_s = sb + C::kOffQ, st_s = sb + C::kOffStage;
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(a.ws + a.L.ctrl);
     volatile int* abort = &s_abort;
 
@@ -550,7 +556,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // address >> 4) is linear, so every operand below is a base
         // descriptor plus a constant.
         const uint64_t dq = smem_desc(q_s, 16, 1024), dk = smem_desc(st_s, 16, 1024);
-        const uint64_t dp = smem_desc(p_s, 16, 1024), dv = smem_desc(st_s + C::kKvBytes, 8192, 1024);
+        const uint64_t dv = smem_desc(st_s + C::kKvBytes, 8192, 1024);
         // S_h(j) = Q_h K^T into S buffer j & 1 of half h (K of stage s).
         auto qk = [&](int h, uint32_t j, int s) {
             const uint64_t a0 = dq + (uint64_t)(h * (C::kQBytes >> 4));
@@ -566,13 +572,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         auto pv = [&](int h, uint32_t j, int s, bool first) -> bool {
             if (!warp_wait(smem_u32(&bars.p_full[h]), j & 1, abort, ctrl)) return false;
             tc_fence_after();
-            const uint64_t a0 = dp + (uint64_t)(h * (C::kPBytes >> 4));
+            // P of page j sits in S buffer j & 1 of the half (8 columns per 16 keys)
+            const uint32_t a0 = tmem + 128u * h + (j & 1) * 64;
             const uint64_t b0 = dv + (uint64_t)(s * (C::kStageBytes >> 4));
             const uint32_t d = tmem + C::kColO + h * D;
             #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                umma_bf16(d, a0 + (uint64_t)(ks * 2), b0 + (uint64_t)(ks * 128), idesc_o,
-                          (first && ks == 0) ? 0u : 1u);
+                umma_bf16_ts(d, a0 + ks * 8, b0 + (uint64_t)(ks * 128), idesc_o, (first && ks == 0) ? 0u : 1u);
             umma_commit(smem_u32(&bars.pv_done[h]));
             return true;
         };
@@ -612,7 +618,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
     } else {
         // ---------------- softmax + epilogue: warps 2..5 half A, 6..9 half B ----------------
-        softmax_half<D, kPacked>(a, tiles, n_units, (warp - 2) >> 2, warp & 3, lane, tmem, st_s, p_s, bars, s_mask,
+        softmax_half<D, kPacked>(a, tiles, n_units, (warp - 2) >> 2, warp & 3, lane, tmem, st_s, bars, s_mask,
                                  kv_full, abort, ctrl);
     }
 
