@@ -241,8 +241,12 @@ __device__ __forceinline__ int uni(int v) { return __shfl_sync(0xffffffffu, v, 0
 struct PfBars {
     uint64_t q_full, q_empty, mma_done;
     uint64_t s_full[2][2];   // [half][S buffer]
-    uint64_t p_full[2];      // [half]: P written (128 arrivals)
-    uint64_t pv_done[2];     // [half]: O += P V finished
+    // [half][S buffer]: P of a page written into its S buffer (128 arrivals),
+    // and its O += P V finished.  One pair per buffer: the softmax runs up to
+    // a page ahead of the PV, and a buffer's next phase needs the PV that
+    // consumed its previous one.
+    uint64_t p_full[2][2];
+    uint64_t pv_done[2][2];
 };
 
 // Softmax and epilogue of one half (128 threads, one MMA row each).
@@ -262,7 +266,9 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
     const int tq = m / g, jh = m % g;
     const float sl2 = a.scale_log2;
     const __nv_bfloat16* sinks = static_cast<const __nv_bfloat16*>(a.sinks);
-    const uint32_t p_full = smem_u32(&bars.p_full[half]), pv_done = smem_u32(&bars.pv_done[half]);
+    auto pv_wait = [&](uint32_t j) -> bool {     // O += P V of this half's page j done
+        return warp_wait(smem_u32(&bars.pv_done[half][j & 1]), (j >> 1) & 1, abort, ctrl);
+    };
     uint32_t it = 0, ch = 0;     // pages of every unit / of units with this half
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -348,15 +354,15 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
                 acc[k] = c < 16 ? lo_w + hi_w : acc[k] + (lo_w + hi_w);
             }
             l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-            // PV of this half's previous page is done: O may be rescaled and
-            // the P buffer is free.
-            if (j > 0) {
-                ok = pf_wait(pv_done, (j - 1) & 1, abort, ctrl);
-                ok = __all_sync(0xffffffffu, ok);
+            // O is rescaled (rarely: lazy threshold) only after the PV of the
+            // previous page; otherwise the softmax does not wait for the PV.
+            const bool rescale = k > 0 && __any_sync(0xffffffffu, need && alpha != 1.f);
+            if (rescale) {
+                ok = pv_wait(j - 1);
                 if (!ok) break;
                 tc_fence_after();
             }
-            if (k > 0 && __any_sync(0xffffffffu, need && alpha != 1.f)) {
+            if (rescale) {
                 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t o[32];
@@ -387,13 +393,11 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
             fence_proxy_async_shared();   // zeroed V rows, read by the MMA
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(p_full);
+            mbar_arrive(smem_u32(&bars.p_full[half][j & 1]));
         }
         if (!ok) break;
         // Epilogue: O / l (with the sink's share of the denominator).
-        const uint32_t jl = ch + t.npg - 1;
-        ok = pf_wait(pv_done, jl & 1, abort, ctrl);
-        ok = __all_sync(0xffffffffu, ok);
+        ok = pv_wait(ch + t.npg - 1);
         if (!ok) break;
         tc_fence_after();
         const int h = kvh * g + jh;
@@ -465,8 +469,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int h = 0; h < 2; ++h) {
             mbar_init(smem_u32(&bars.s_full[h][0]), 1);
             mbar_init(smem_u32(&bars.s_full[h][1]), 1);
-            mbar_init(smem_u32(&bars.p_full[h]), 128);
-            mbar_init(smem_u32(&bars.pv_done[h]), 1);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(smem_u32(&bars.p_full[h][b]), 128);
+                mbar_init(smem_u32(&bars.pv_done[h][b]), 1);
+            }
         }
         s_abort = 0;
         fence_barrier_init();
@@ -570,7 +576,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         };
         // O_h += P_h V (V of stage s); the first page of a unit overwrites O_h.
         auto pv = [&](int h, uint32_t j, int s, bool first) -> bool {
-            if (!warp_wait(smem_u32(&bars.p_full[h]), j & 1, abort, ctrl)) return false;
+            if (!warp_wait(smem_u32(&bars.p_full[h][j & 1]), (j >> 1) & 1, abort, ctrl)) return false;
             tc_fence_after();
             // P of page j sits in S buffer j & 1 of the half (8 columns per 16 keys)
             const uint32_t a0 = tmem + 128u * h + (j & 1) * 64;
@@ -579,7 +585,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 umma_bf16_ts(d, a0 + ks * 8, b0 + (uint64_t)(ks * 128), idesc_o, (first && ks == 0) ? 0u : 1u);
-            umma_commit(smem_u32(&bars.pv_done[h]));
+            umma_commit(smem_u32(&bars.pv_done[h][j & 1]));
             return true;
         };
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ui) {
