@@ -26,7 +26,6 @@ llama8b_packed measures packed sequences the same way (one 8192-token row of
 eight sequences, no cache).
 """
 import argparse
-import glob
 import hashlib
 import json
 import math
@@ -87,9 +86,10 @@ def measured_hbm_peak():
 
 
 def kernel_source_hash():
+    """Hash of the sources that define the decode attention kernel."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "paged_gqa_decode_step_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
+    for name in ("attend.cu", "common.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "paged_gqa_decode_step_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
