@@ -135,7 +135,10 @@ def test_workspace_layout_bound_covers_every_plan():
             lo = max(0, p - window + 1) if window > 0 else 0
             n.append(p // 64 - lo // 64 + 1)
         W = sum(n) * Hk
-        C = min(max(math.ceil(W / (items_per_cta * grid)), 1), chunk_max)
+        if max(n) * grid <= 2 * W:
+            C = chunk_max                  # rows kept whole
+        else:
+            C = min(max(math.ceil(W / (items_per_cta * grid)), 1), chunk_max)
         items = sum(Hk * math.ceil(x / C) for x in n)
         bound = max(items_per_cta * grid + R * Hk, R * Hk * math.ceil(Pg / chunk_max))
         assert items <= bound
