@@ -66,6 +66,8 @@ def lib():
         L.oracle_step.argtypes = [ctypes.POINTER(Shape)] + [vp] * 10
         L.oracle_prefill_paged.argtypes = [ctypes.POINTER(Shape), ctypes.c_int] + [vp] * 13
         L.oracle_packed.argtypes = [ctypes.POINTER(Shape), ctypes.c_int] + [vp] * 10
+        L.oracle_set_threads.argtypes = [ctypes.c_int]
+        L.oracle_set_threads.restype = ctypes.c_int
         L.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
         L.oracle_f32_to_bf16.restype = ctypes.c_uint16
         for f in (L.oracle_rope_tables, L.oracle_rope_write_kv, L.oracle_decode, L.oracle_decode_sinks,
@@ -151,6 +153,11 @@ def packed(shape, q, k, v, positions, segments, sinks=None):
     rc = lib().oracle_packed(ctypes.byref(shape), int(q.shape[0]), _ptr(q), _ptr(k), _ptr(v), _ptr(positions),
                              _ptr(segments), _ptr(sinks), _ptr(q_rot), _ptr(k_rot), _ptr(out), _ptr(out64))
     return q_rot, k_rot, out, out64, rc
+
+
+def set_threads(n: int) -> int:
+    """Threads for the row loops (1 = serial); returns the count in use."""
+    return int(lib().oracle_set_threads(int(n)))
 
 
 def f32_to_bf16_bits(x: float) -> int:

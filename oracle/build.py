@@ -19,9 +19,12 @@ def build(force: bool = False) -> str:
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
-           SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
+    base = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+    # OpenMP only spreads independent rows over threads; without it the
+    # same code runs serially.
+    r = subprocess.run(base + ["-fopenmp", SRC, "-o", tmp, "-lm"], capture_output=True, text=True)
+    if r.returncode != 0:
+        subprocess.run(base + [SRC, "-o", tmp, "-lm"], check=True)
     os.replace(tmp, LIB)
     return LIB
 

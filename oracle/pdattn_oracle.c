@@ -55,6 +55,9 @@
  */
 #include <math.h>
 #include <stdint.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <stdlib.h>
 #include <string.h>
 
@@ -219,65 +222,105 @@ int oracle_rope_write_kv(const oracle_shape* p, const void* q, const void* k_new
  * as one more logit that carries no value, so it only enlarges the
  * denominator.
  */
+/* One row of oracle_decode_sinks; scores holds max_ctx doubles, acc D. */
+static int decode_row(const oracle_shape* p, int r, const void* q_rot, const int32_t* positions,
+                      const int32_t* table, const void* k_pool, const void* v_pool, const void* sinks,
+                      void* out, double* out64, double* scores, double* acc) {
+    const int D = p->head_dim, Hq = p->heads, Hk = p->kv_heads, PS = p->page_size;
+    const int group = Hq / Hk;
+    const double scale = (double)(float)(1.0 / sqrt((double)D)); /* rsqrt(f32(D)) */
+    const int max_ctx = p->pages_per_row * PS;
+    int pos = positions[r];
+    if (pos < 0 || pos >= max_ctx) return ORACLE_EINVAL;
+    int lo = 0;
+    if (p->window > 0 && pos - p->window + 1 > 0) lo = pos - p->window + 1;
+    for (int t = lo; t <= pos; ++t) {
+        int page = table[(size_t)r * p->pages_per_row + t / PS];
+        if (page < 0 || page >= p->num_pages) return ORACLE_EBADPAGE;
+    }
+    for (int h = 0; h < Hq; ++h) {
+        int kvh = h / group;
+        size_t qo = ((size_t)r * Hq + h) * D;
+        double m = -INFINITY;
+        const double sink = sinks ? (double)load_t(sinks, (size_t)h, p->dtype) : -INFINITY;
+        for (int t = lo; t <= pos; ++t) {
+            int page = table[(size_t)r * p->pages_per_row + t / PS];
+            size_t ko = pool_index(p, page, kvh, t % PS, 0);
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d)
+                dot += (double)load_t(q_rot, qo + d, p->dtype) * (double)load_t(k_pool, ko + d, p->dtype);
+            scores[t - lo] = scale * dot;
+            if (scores[t - lo] > m) m = scores[t - lo];
+        }
+        if (sink > m) m = sink;
+        double l = sinks ? exp(sink - m) : 0.0;
+        for (int t = lo; t <= pos; ++t) {
+            scores[t - lo] = exp(scores[t - lo] - m);
+            l += scores[t - lo];
+        }
+        for (int d = 0; d < D; ++d) acc[d] = 0.0;
+        for (int t = lo; t <= pos; ++t) {
+            int page = table[(size_t)r * p->pages_per_row + t / PS];
+            size_t vo = pool_index(p, page, kvh, t % PS, 0);
+            double w = scores[t - lo] / l;
+            for (int d = 0; d < D; ++d) acc[d] += w * (double)load_t(v_pool, vo + d, p->dtype);
+        }
+        for (int d = 0; d < D; ++d) {
+            if (out64) out64[qo + d] = acc[d];
+            store_t(out, qo + d, (float)acc[d], p->dtype);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Rows are independent; when the library is built with OpenMP they run on
+ * oracle_set_threads() threads (one row at a time per thread, the same
+ * arithmetic), and the status is that of the last failing row, as in order.
+ */
 int oracle_decode_sinks(const oracle_shape* p, const void* q_rot, const int32_t* positions,
                         const int32_t* table, const void* k_pool, const void* v_pool,
                         const void* sinks, void* out, double* out64) {
     if (!shape_ok(p)) return ORACLE_EINVAL;
-    const int D = p->head_dim, Hq = p->heads, Hk = p->kv_heads, PS = p->page_size;
-    const int group = Hq / Hk;
-    const double scale = (double)(float)(1.0 / sqrt((double)D)); /* rsqrt(f32(D)) */
-    int max_ctx = p->pages_per_row * PS;
-    double* scores = (double*)malloc(sizeof(double) * (size_t)max_ctx);
-    double* acc = (double*)malloc(sizeof(double) * (size_t)D);
-    if (!scores || !acc) { free(scores); free(acc); return ORACLE_EINVAL; }
-    int status = ORACLE_OK;
-    for (int r = 0; r < p->rows; ++r) {
-        int pos = positions[r];
-        if (pos < 0 || pos >= max_ctx) { status = ORACLE_EINVAL; continue; }
-        int lo = 0;
-        if (p->window > 0 && pos - p->window + 1 > 0) lo = pos - p->window + 1;
-        int bad = 0;
-        for (int t = lo; t <= pos; ++t) {
-            int page = table[(size_t)r * p->pages_per_row + t / PS];
-            if (page < 0 || page >= p->num_pages) bad = 1;
+    const int max_ctx = p->pages_per_row * p->page_size;
+    int* row_status = (int*)calloc((size_t)(p->rows > 0 ? p->rows : 1), sizeof(int));
+    if (!row_status) return ORACLE_EINVAL;
+    int oom = 0;
+#ifdef _OPENMP
+#pragma omp parallel
+#endif
+    {
+        double* scores = (double*)malloc(sizeof(double) * (size_t)max_ctx);
+        double* acc = (double*)malloc(sizeof(double) * (size_t)p->head_dim);
+        if (!scores || !acc) {
+            oom = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+            for (int r = 0; r < p->rows; ++r)
+                row_status[r] = decode_row(p, r, q_rot, positions, table, k_pool, v_pool, sinks, out, out64,
+                                           scores, acc);
         }
-        if (bad) { status = ORACLE_EBADPAGE; continue; }
-        for (int h = 0; h < Hq; ++h) {
-            int kvh = h / group;
-            size_t qo = ((size_t)r * Hq + h) * D;
-            double m = -INFINITY;
-            const double sink = sinks ? (double)load_t(sinks, (size_t)h, p->dtype) : -INFINITY;
-            for (int t = lo; t <= pos; ++t) {
-                int page = table[(size_t)r * p->pages_per_row + t / PS];
-                size_t ko = pool_index(p, page, kvh, t % PS, 0);
-                double dot = 0.0;
-                for (int d = 0; d < D; ++d)
-                    dot += (double)load_t(q_rot, qo + d, p->dtype) * (double)load_t(k_pool, ko + d, p->dtype);
-                scores[t - lo] = scale * dot;
-                if (scores[t - lo] > m) m = scores[t - lo];
-            }
-            if (sink > m) m = sink;
-            double l = sinks ? exp(sink - m) : 0.0;
-            for (int t = lo; t <= pos; ++t) {
-                scores[t - lo] = exp(scores[t - lo] - m);
-                l += scores[t - lo];
-            }
-            for (int d = 0; d < D; ++d) acc[d] = 0.0;
-            for (int t = lo; t <= pos; ++t) {
-                int page = table[(size_t)r * p->pages_per_row + t / PS];
-                size_t vo = pool_index(p, page, kvh, t % PS, 0);
-                double w = scores[t - lo] / l;
-                for (int d = 0; d < D; ++d) acc[d] += w * (double)load_t(v_pool, vo + d, p->dtype);
-            }
-            for (int d = 0; d < D; ++d) {
-                if (out64) out64[qo + d] = acc[d];
-                store_t(out, qo + d, (float)acc[d], p->dtype);
-            }
-        }
+        free(scores);
+        free(acc);
     }
-    free(scores);
-    free(acc);
+    int status = oom ? ORACLE_EINVAL : ORACLE_OK;
+    for (int r = 0; r < p->rows; ++r)
+        if (row_status[r] != ORACLE_OK) status = row_status[r];
+    free(row_status);
     return status;
+}
+
+/* Threads for the row loop (no effect without OpenMP); returns the count in use. */
+int oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
 }
 
 int oracle_decode(const oracle_shape* p, const void* q_rot, const int32_t* positions,
