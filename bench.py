@@ -13,7 +13,9 @@ Default workload: the Llama-3.1-8B serving batch (256 rows, 32 query heads,
   launch; achieved = its algorithmic bytes per launch / mean launch time,
   against the measured HBM copy bandwidth.
 * e2e: the same metric through the public call with pinned host buffers:
-  each step copies that step's inputs host->device and the output back.
+  each step copies that step's inputs host->device and its output back; as
+  in a serving loop the next step's copy overlaps the current step
+  (double-buffered, copy stream) and the host waits for each output.
 * cpu_baseline: the CPU oracle on the host (single thread), timed on whole
   steps of the same workload.
 * --impl reference: the CPU oracle alone, each step a bounded sample of rows.
@@ -166,6 +168,69 @@ class ClockSampler:
         sm = sorted(r[0] for r in rows)
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
                 "samples": len(rows)}
+
+
+# ------------------------------------------------------------- end to end --
+def e2e_pipelined(dev_tensors, names, run, out, n_steps, world):
+    """End-to-end seconds per step through the public call.  Every step copies
+    its own inputs (`names`) from pinned host memory and reads its output back
+    into pinned host memory.  As in a serving loop, inputs and outputs are
+    double-buffered, the copies run on their own streams (host to device
+    ahead of the step, device to host after it) under the neighbouring steps'
+    compute, and the host waits for step i - 1's output while step i runs.
+    `run(inputs, out)` issues the library call on the current stream.
+    Returns (seconds per step, H2D bytes per step, D2H bytes per step)."""
+    host = [{k: dev_tensors[k].cpu().pin_memory() for k in names} for _ in range(2)]
+    dev = [{k: torch.empty_like(dev_tensors[k]) for k in names} for _ in range(2)]
+    outs = [torch.empty_like(out) for _ in range(2)]
+    host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    compute = torch.cuda.current_stream()
+    h2d_done = [torch.cuda.Event() for _ in range(2)]
+    inputs_free = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    out_ready = [torch.cuda.Event() for _ in range(2)]
+    for e in inputs_free + out_ready:
+        e.record(compute)
+
+    def h2d(i):
+        b = i % 2
+        h2d_stream.wait_event(inputs_free[b])           # the step two back is done with this buffer
+        with torch.cuda.stream(h2d_stream):
+            for k in names:
+                dev[b][k].copy_(host[b][k], non_blocking=True)
+        h2d_done[b].record(h2d_stream)
+
+    def step(i):
+        b = i % 2
+        compute.wait_event(h2d_done[b])
+        compute.wait_event(out_ready[b])                # the step two back has read its output out
+        run(dev[b], outs[b])
+        inputs_free[b].record(compute)
+        computed[b].record(compute)
+        d2h_stream.wait_event(computed[b])
+        with torch.cuda.stream(d2h_stream):
+            host_out[b].copy_(outs[b], non_blocking=True)
+        out_ready[b].record(d2h_stream)
+
+    def loop(n):
+        torch.cuda.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        h2d(0)
+        for i in range(n):
+            if i + 1 < n:
+                h2d(i + 1)
+            step(i)
+            if i >= 1:
+                out_ready[(i - 1) % 2].synchronize()    # step i - 1's output is on the host
+        out_ready[(n - 1) % 2].synchronize()
+        return time.perf_counter() - t0
+
+    loop(3)
+    secs = loop(n_steps) / n_steps
+    h2d_bytes = sum(v.numel() * v.element_size() for v in host[0].values())
+    return secs, h2d_bytes, host_out[0].numel() * host_out[0].element_size()
 
 
 # -------------------------------------------------------------- distributed --
@@ -362,30 +427,11 @@ def run_ours(args, w, world, rank, local):
     traffic = profiled_traffic(w.name)
 
     # ---- end to end: pinned host inputs in, output back, every step
-    host_in = {k: t[k].cpu().pin_memory() for k in ("q", "k_new", "v_new", "positions", "table")}
-    dev_in = {k: torch.empty_like(t[k]) for k in host_in}
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = host_out.numel() * host_out.element_size()
     n_e2e = max(10, min(args.steps, 500))
-    stream = torch.cuda.current_stream()
-
-    def e2e_step():
-        for k in host_in:
-            dev_in[k].copy_(host_in[k], non_blocking=True)
-        b.decode_fused(p, dev_in["q"], dev_in["k_new"], dev_in["v_new"], dev_in["positions"], dev_in["table"],
-                       t["k_pool"], t["v_pool"], out, ws)
-        host_out.copy_(out, non_blocking=True)
-        stream.synchronize()
-
-    for _ in range(3):
-        e2e_step()
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(n_e2e):
-        e2e_step()
-    e2e_s = (time.perf_counter() - t0) / n_e2e
+    e2e_s, h2d, d2h = e2e_pipelined(
+        t, ("q", "k_new", "v_new", "positions", "table"),
+        lambda d, o: b.decode_fused(p, d["q"], d["k_new"], d["v_new"], d["positions"], d["table"], t["k_pool"],
+                                    t["v_pool"], o, ws), out, n_e2e, world)
     e2e_s = max_over_ranks(e2e_s, world)
     b.check_status(ws)
     e2e_value = all_kv / e2e_s / 1e9
@@ -597,30 +643,12 @@ def run_prefill(args, w, world, rank, local):
     achieved = flops / (att_ms * 1e-3) / 1e12
 
     # end to end: pinned host inputs in, output back, every call
-    host_in = {k: t[k].cpu().pin_memory() for k in ("q", "k_new", "v_new", "positions", "rows", "slots", "table")}
-    dev_in = {k: torch.empty_like(t[k]) for k in host_in}
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = host_out.numel() * host_out.element_size()
-    stream = torch.cuda.current_stream()
-
-    def e2e_step():
-        for k in host_in:
-            dev_in[k].copy_(host_in[k], non_blocking=True)
-        b.prefill_paged(p, dev_in["q"], dev_in["k_new"], dev_in["v_new"], dev_in["positions"], dev_in["rows"],
-                        dev_in["slots"], dev_in["table"], t["k_pool"], t["v_pool"], out, ws)
-        host_out.copy_(out, non_blocking=True)
-        stream.synchronize()
-
-    for _ in range(3):
-        e2e_step()
-    n_e2e = max(10, min(args.steps, 100))
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(n_e2e):
-        e2e_step()
-    e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, world)
+    e2e_s, h2d, d2h = e2e_pipelined(
+        t, ("q", "k_new", "v_new", "positions", "rows", "slots", "table"),
+        lambda d, o: b.prefill_paged(p, d["q"], d["k_new"], d["v_new"], d["positions"], d["rows"], d["slots"],
+                                     d["table"], t["k_pool"], t["v_pool"], o, ws),
+        out, max(10, min(args.steps, 100)), world)
+    e2e_s = max_over_ranks(e2e_s, world)
     b.check_status(ws)
 
     cpu = None
@@ -775,29 +803,9 @@ def run_packed(args, w, world, rank, local):
     peak, peak_kind = measured_tensor_peak()
     achieved = flops / (att_ms * 1e-3) / 1e12
 
-    host_in = {k: t[k].cpu().pin_memory() for k in names}
-    dev_in = {k: torch.empty_like(t[k]) for k in host_in}
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in host_in.values())
-    d2h = host_out.numel() * host_out.element_size()
-    stream = torch.cuda.current_stream()
-
-    def e2e_step():
-        for k in host_in:
-            dev_in[k].copy_(host_in[k], non_blocking=True)
-        b.packed(p, *(dev_in[k] for k in names), out, ws)
-        host_out.copy_(out, non_blocking=True)
-        stream.synchronize()
-
-    for _ in range(3):
-        e2e_step()
-    n_e2e = max(10, min(args.steps, 100))
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(n_e2e):
-        e2e_step()
-    e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, world)
+    e2e_s, h2d, d2h = e2e_pipelined(t, names, lambda d, o: b.packed(p, *(d[k] for k in names), o, ws), out,
+                                    max(10, min(args.steps, 100)), world)
+    e2e_s = max_over_ranks(e2e_s, world)
     b.check_status(ws)
 
     cpu = None
