@@ -259,6 +259,7 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
     const int* seg_pad = reinterpret_cast<const int*>(a.ws + a.L.seg_pad);
     const int4* blk = reinterpret_cast<const int4*>(a.ws + a.L.blk);
     const int W = a.window;
+    const bool canonical_no_window = kPacked && W <= 0 && ctrl->rows == 1;
     const int Hk = a.kv_heads, g = a.group, Tq = a.tile_tokens / 2;
     const int m = quarter * 32 + lane;                    // MMA row = TMEM lane
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -288,6 +289,10 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
             lo = (W > 0 && pos - W + 1 > 0) ? pos - W + 1 : 0;
             if (kPacked) seg = seg_pad[t.t0 + tok];
         }
+        // A canonical pack (every sequence one run, positions rising) without
+        // a window sees exactly the tokens [run start, own index] of the pack.
+        const bool by_index = !kPacked || canonical_no_window;
+        const int key_lo = kPacked ? t.pad : lo, key_hi = kPacked ? (active ? t.t0 + tok : -1) : pos;
         float m_run = -INFINITY, l = 0.f;
         for (int k = 0; k < t.npg; ++k) {
             const uint32_t j = ch + k;
@@ -300,9 +305,10 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
             tmem_ld32(tmem + lane_base + s_col + (j & 1) * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
             tmem_ld32(tmem + lane_base + s_col + (j & 1) * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
             tmem_wait_ld();
-            if (!kPacked) {
-                // keys c of this page visible to the row: lo <= pg*64 + c <= pos
-                const int c_lo = lo - pg * kPageSize, c_hi = pos - pg * kPageSize;
+            if (by_index) {
+                // keys c of this page visible to the row: key_lo <= pg*64 + c <= key_hi
+                // (cache positions, or indices of a canonical pack)
+                const int c_lo = key_lo - pg * kPageSize, c_hi = key_hi - pg * kPageSize;
                 if (!__all_sync(0xffffffffu, c_lo <= 0 && c_hi >= kPageSize - 1)) {
                     #pragma unroll
                     for (int c = 0; c < 64; ++c)

@@ -857,7 +857,7 @@ __device__ void build_packed_plan(const PrefillPrepArgs& a) {
         ctrl->kv_heads = a.kv_heads;
         ctrl->group = a.heads / a.kv_heads;
         ctrl->head_dim = a.head_dim;
-        ctrl->rows = canonical ? 1 : 0;    // recorded for inspection
+        ctrl->rows = canonical ? 1 : 0;    // read by the attention kernel: index-range masks
         ctrl->magic = kPlanMagic;
     }
 }
