@@ -17,9 +17,10 @@
 //   P               bf16, written back into the S columns it came from
 //   O += P V        tcgen05.mma M=128 N=D K=64, P read from tensor memory,
 //                   V page read from shared memory MN-major
-// The MMA issuer interleaves the halves (S_A(j) S_B(j) PV_A(j-1) PV_B(j-1))
+// The MMA issuer interleaves the halves (S_A(j) PV_A(j-1) S_B(j) PV_B(j-1))
 // so that each half's softmax runs while the tensor core works for the
-// other; S is double-buffered per half.  The running max is raised lazily:
+// other; S is double-buffered per half.  PV_A of a page precedes its PV_B:
+// half A zeroes the page's stale V rows before its P is marked ready.  The running max is raised lazily:
 // O is rescaled in TMEM only when a row's max grows by more than 2^8.
 //
 // Packed sequences (Llama example page, `packed`) run the same kernel: the
@@ -602,22 +603,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             tc_fence_after();
             for (int k = 0; k <= npg && ok; ++k) {
                 const uint32_t j = it + k;
+                const int s = j % C::kStages, sp = (j - 1) % C::kStages;
                 if (k < npg) {
-                    const int s = j % C::kStages;
                     ok = warp_wait(smem_u32(&kv_full[s]), (j / C::kStages) & 1, abort, ctrl);
                     if (!ok) break;
                     tc_fence_after();
                     qk(0, cnt0 + k, s);
-                    if (nh == 2) qk(1, cnt1 + k, s);
-                    if (k == npg - 1) umma_commit(smem_u32(&bars.q_empty));   // every S of the unit issued
                 }
-                if (k > 0) {
-                    const int sp = (j - 1) % C::kStages;
-                    ok = pv(0, cnt0 + k - 1, sp, k == 1);
-                    if (ok && nh == 2) ok = pv(1, cnt1 + k - 1, sp, k == 1);
+                if (k > 0) ok = pv(0, cnt0 + k - 1, sp, k == 1);
+                if (!ok) break;
+                if (nh == 2) {
+                    if (k < npg) qk(1, cnt1 + k, s);
+                    if (k > 0) ok = pv(1, cnt1 + k - 1, sp, k == 1);
                     if (!ok) break;
-                    umma_commit(smem_u32(&kv_empty[sp]));
                 }
+                if (k == npg - 1) umma_commit(smem_u32(&bars.q_empty));   // every S of the unit issued
+                if (k > 0) umma_commit(smem_u32(&kv_empty[sp]));
             }
             it += npg;
             cnt0 += npg;
