@@ -335,9 +335,14 @@ struct Consumer<float, D, G> {
                          bool partial, float sl2) {
         const int tok0 = warp * 16;
         const int tl = lane & 15, half = lane >> 4, t = tok0 + tl;
-        float acc[G];
+        // Independent partial sums per head (NA of them) keep the dot
+        // product's FMA chain short; they are added once at the end.
+        constexpr int NA = G == 1 ? 4 : (G == 2 ? 2 : 1);
+        float part[G][NA];
         #pragma unroll
-        for (int j = 0; j < G; ++j) acc[j] = 0.f;
+        for (int j = 0; j < G; ++j)
+            #pragma unroll
+            for (int a = 0; a < NA; ++a) part[j][a] = 0.f;
         // full unroll when the query sits in registers (its index must be static)
         #pragma unroll (G >= 4 ? 2 : D / 8)
         for (int c = 0; c < D / 8; ++c) {
@@ -349,12 +354,20 @@ struct Consumer<float, D, G> {
                     float4 qv;
                     if constexpr (kQRegs) qv = make_float4(qr[4 * c], qr[4 * c + 1], qr[4 * c + 2], qr[4 * c + 3]);
                     else qv = *reinterpret_cast<const float4*>(wq + j * D + col);
-                    acc[j] = fmaf(kv.x, qv.x, acc[j]);
-                    acc[j] = fmaf(kv.y, qv.y, acc[j]);
-                    acc[j] = fmaf(kv.z, qv.z, acc[j]);
-                    acc[j] = fmaf(kv.w, qv.w, acc[j]);
+                    float& pa = part[j][c % NA];
+                    pa = fmaf(kv.x, qv.x, pa);
+                    pa = fmaf(kv.y, qv.y, pa);
+                    pa = fmaf(kv.z, qv.z, pa);
+                    pa = fmaf(kv.w, qv.w, pa);
                 }
             }
+        }
+        float acc[G];
+        #pragma unroll
+        for (int j = 0; j < G; ++j) {
+            acc[j] = part[j][0];
+            #pragma unroll
+            for (int a = 1; a < NA; ++a) acc[j] += part[j][a];
         }
         const bool valid = t >= t_lo && t < t_hi;
         #pragma unroll
