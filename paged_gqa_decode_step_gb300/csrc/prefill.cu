@@ -396,8 +396,8 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
                                      ::"r"(vb + (rest >> 3) * 8192 + r * 128 + (rest & 7) * 16), "r"(0)
                                      : "memory");
                 }
+                fence_proxy_async_shared();   // zeroed V rows, read by the MMA
             }
-            fence_proxy_async_shared();   // zeroed V rows, read by the MMA
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(smem_u32(&bars.p_full[half][j & 1]));
