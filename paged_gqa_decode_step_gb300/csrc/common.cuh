@@ -26,7 +26,7 @@ constexpr int kErrBadPlan = 8;
 // Control block at the start of the workspace (256 bytes).
 struct Ctrl {
     int status;        // OR of kErr* bits; cleared by pdattn_check_status
-    int next_item;     // persistent-scheduler cursor (starts at `grid`)
+    int next_item;     // persistent-scheduler cursor (decode: starts at `grid`; prefill / packed: at 0)
     int done_ctas;     // CTAs that finished fetching work
     int n_items;       // work items in the plan
     int chunk_pages;   // pages per split chosen by the plan

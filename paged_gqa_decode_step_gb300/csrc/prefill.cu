@@ -10,31 +10,33 @@
 // Work unit = one tile of up to 256 / g consecutive tokens of one row times
 // one kv head, in two halves of 128 / g tokens.  Each half's g query heads
 // per token stack into the 128 rows of an MMA (row m = token m / g, head
-// kvh * g + m % g), so one K/V page read serves 256 query rows.  Per page of
-// 64 keys and per half:
-//   S  = Q K^T      tcgen05.mma M=128 N=64 K=D, fp32 accumulator in TMEM
+// kvh * g + m % g), so one K/V read serves 256 query rows.  Keys come in
+// blocks of 128 (two 64-token pages); per block and half:
+//   S  = Q K^T      tcgen05.mma M=128 N=128 K=D, fp32 accumulator in TMEM
 //   softmax         one thread per MMA row: mask, running max, exp2, sum
-//   P               bf16, written back into the S columns it came from
-//   O += P V        tcgen05.mma M=128 N=D K=64, P read from tensor memory,
-//                   V page read from shared memory MN-major
-// The MMA issuer interleaves the halves (S_A(j) PV_A(j-1) S_B(j) PV_B(j-1))
-// so that each half's softmax runs while the tensor core works for the
-// other; S is double-buffered per half.  PV_A of a page precedes its PV_B:
-// half A zeroes the page's stale V rows before its P is marked ready.  The running max is raised lazily:
-// O is rescaled in TMEM only when a row's max grows by more than 2^8.
+//   P               bf16, written back over the first 64 columns of S
+//   O += P V        tcgen05.mma M=128 N=D K=128, P read from tensor memory,
+//                   V read from shared memory MN-major
+// The issuer runs PV_A(j-1) S_A(j) PV_B(j-1) S_B(j): each half's S follows
+// its previous PV (P lives in S's columns), and each half's softmax runs
+// while the tensor core works for the other half.  The running max is
+// raised lazily: O is rescaled in TMEM only when a row's max grows by more
+// than 2^8 (S of a block done implies the PV before it is done).
 //
 // Packed sequences (Llama example page, `packed`) run the same kernel: the
-// pack is a contiguous cache of 64-token key blocks, K and V come by 3-D TMA
-// from the rotated keys and the values [n, kv_heads, D], and the mask is
-// per key (same segment id, position <= the query's, inside the window),
-// from segment ids and positions copied into shared memory with each block;
-// blocks wholly of the row's sequence and before its position skip the test.
+// pack is a contiguous cache of 64-token pages, K and V come by 3-D TMA from
+// the rotated keys and the values [n, kv_heads, D].  A canonical pack
+// without a window masks by pack index like a cache row; otherwise the mask
+// is per key (same segment id, position <= the query's, inside the window),
+// from segment ids and positions copied into shared memory with each block.
 //
-// Warps: 0 = TMA producer (Q boxes, K and V pages), 1 = TMEM owner and MMA
-// issuer, 2..5 = softmax and epilogue of half A, 6..9 of half B (warp w
-// reads TMEM lanes 32 * (w % 4) .. + 31).  Every wait is bounded; on a
-// timeout the kernel sets the error flag, drains its own copies and MMAs,
-// frees TMEM and returns.
+// Warpgroups: 0 = warp 0 TMA producer, warp 1 TMEM owner and MMA issuer
+// (warps 2 and 3 idle); 1 and 2 = softmax and epilogue of halves A and B
+// (warp w reads TMEM lanes 32 * (w % 4) .. + 31).  The issuing warpgroup
+// hands registers to the softmax warpgroups (setmaxnreg), which hold a
+// whole 128-key row of S.  Every wait is bounded; on a timeout the kernel
+// sets the error flag, drains its own copies and MMAs, frees TMEM and
+// returns.
 #include <climits>
 
 #include "internal.h"
@@ -42,7 +44,7 @@
 namespace pdattn {
 namespace {
 
-constexpr int kPfThreads = 320;
+constexpr int kPfThreads = 384;
 constexpr uint64_t kPfTimeoutNs = 2000000000ull;
 constexpr float kRescaleLog2 = 8.0f;    // lazy rescale threshold (log2 units)
 
@@ -50,21 +52,26 @@ template <int D, bool kPacked = false>
 struct PfCfg {
     static constexpr int kBoxes = D / 64;                 // 64-element column boxes
     static constexpr int kQBytes = kBoxes * 16384;        // one half: 128 rows x 128 B per box
-    static constexpr int kKvBytes = kBoxes * 8192;        // one page of K (or V): 64 rows x 128 B per box
-    static constexpr int kStageBytes = 2 * kKvBytes;
-    // packed mode keeps each stage's segment ids and positions (512 B) in
-    // static shared memory, which costs D = 128 one stage
-    static constexpr int kStages = D == 128 ? (kPacked ? 4 : 5) : 10;
+    static constexpr int kKBytes = kBoxes * 16384;        // K (or V) of a block: 128 keys x 128 B per box
+    static constexpr int kPageBytes = 8192;               // one page's 64 rows of a box
+    static constexpr int kStageBytes = 2 * kKBytes;       // K then V of one block
+    static constexpr int kStages = D == 128 ? 2 : 5;
     static constexpr int kMaskStages = kPacked ? kStages : 1;
     static constexpr int kOffQ = 0;                       // halves A, B
     static constexpr int kOffStage = 2 * kQBytes;
     static constexpr int kSmem = kOffStage + kStages * kStageBytes + 1024;   // + alignment slack
-    // TMEM: S of half h, buffer b at column 128 h + 64 b (its first 32 columns
-    // then hold P as bf16 pairs); O of half h at 256 + h D.
+    // TMEM: S of half h at column 128 h (128 columns; the first 64 then hold
+    // P as bf16 pairs); O of half h at 256 + h D.
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kColO = 256;
-    static_assert(kSmem + kMaskStages * 512 <= 227 * 1024 - 1536, "shared memory budget");
+    static_assert(kSmem + kMaskStages * 1024 <= 227 * 1024 - 1536, "shared memory budget");
 };
+
+// Registers per thread after the hand-over: the launch gives 384 threads 168
+// each (64512); the issuing warpgroup keeps 72, the softmax warpgroups 216
+// (128 x 72 + 256 x 216 = 64512).
+constexpr uint32_t kRegsIssue = 72, kRegsSoftmax = 216;
+static_assert(128 * kRegsIssue + 256 * kRegsSoftmax <= 384 * 168, "register hand-over exceeds the launch");
 
 // --- tcgen05 / TMA wrappers ---------------------------------------------------
 
@@ -211,6 +218,11 @@ __device__ __forceinline__ float max64(const uint32_t (&s)[64]) {
     return fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
 }
 
+__device__ __forceinline__ float max128(const uint32_t (&s)[128]) {
+    return fmaxf(max64(*reinterpret_cast<const uint32_t(*)[64]>(&s[0])),
+                 max64(*reinterpret_cast<const uint32_t(*)[64]>(&s[64])));
+}
+
 // Bounded wait that also gives up once another role has aborted.
 __device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, volatile int* abort, Ctrl* ctrl) {
     if (mbar_test_wait(bar, parity)) return true;
@@ -239,22 +251,37 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // Broadcast of lane 0's value: the loops of the issuing warps stay uniform.
 __device__ __forceinline__ int uni(int v) { return __shfl_sync(0xffffffffu, v, 0); }
 
+// Units reach a CTA through a small ring: the producer takes the next unit
+// of the descending-cost list (CTA b starts with unit b, later ones come
+// from a global cursor), so a CTA that finishes early takes more work.
+constexpr int kUnitSlots = 4;
+constexpr int kUnitReaders = 9;      // the issuing warp and the eight softmax warps
+
 struct PfBars {
     uint64_t q_full, q_empty, mma_done;
-    uint64_t s_full[2][2];   // [half][S buffer]
-    // [half][S buffer]: P of a page written into its S buffer (128 arrivals),
-    // and its O += P V finished.  One pair per buffer: the softmax runs up to
-    // a page ahead of the PV, and a buffer's next phase needs the PV that
-    // consumed its previous one.
-    uint64_t p_full[2][2];
-    uint64_t pv_done[2][2];
+    uint64_t unit_full[kUnitSlots], unit_empty[kUnitSlots];
+    uint64_t s_full[2];      // [half]: S of the block done (its previous PV too)
+    uint64_t p_full[2];      // [half]: P of the block written (128 arrivals)
+    uint64_t o_done[2];      // [half]: the unit's last PV done
 };
+
+// The next unit from the producer's ring (whole warp): -1 once there is no
+// more work, -2 on abort.
+__device__ __forceinline__ int take_unit(PfBars& bars, const int* s_unit, uint32_t k, int lane, volatile int* abort,
+                                         Ctrl* ctrl) {
+    const int slot = k % kUnitSlots;
+    if (!warp_wait(smem_u32(&bars.unit_full[slot]), (k / kUnitSlots) & 1, abort, ctrl)) return -2;
+    const int u = *reinterpret_cast<const volatile int*>(s_unit + slot);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&bars.unit_empty[slot]));
+    return u;
+}
 
 // Softmax and epilogue of one half (128 threads, one MMA row each).
 template <int D, bool kPacked>
 __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile* tiles, int n_units, int half,
-                                             int quarter, int lane, uint32_t tmem, uint32_t st_s,
-                                             PfBars& bars, const int (*s_mask)[128], uint64_t* kv_full,
+                                             int quarter, int lane, uint32_t tmem, uint32_t st_s, PfBars& bars,
+                                             const int (*s_mask)[256], uint64_t* v_full, const int* s_unit,
                                              volatile int* abort, Ctrl* ctrl) {
     using C = PfCfg<D, kPacked>;
     const int* seg_pad = reinterpret_cast<const int*>(a.ws + a.L.seg_pad);
@@ -264,21 +291,21 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
     const int Hk = a.kv_heads, g = a.group, Tq = a.tile_tokens / 2;
     const int m = quarter * 32 + lane;                    // MMA row = TMEM lane
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const uint32_t s_col = 128u * half, o_col = C::kColO + (uint32_t)(half * D);
+    const uint32_t s_addr = tmem + lane_base + 128u * half, o_addr = tmem + lane_base + C::kColO + half * D;
     const int tq = m / g, jh = m % g;
     const float sl2 = a.scale_log2;
     const __nv_bfloat16* sinks = static_cast<const __nv_bfloat16*>(a.sinks);
-    auto pv_wait = [&](uint32_t j) -> bool {     // O += P V of this half's page j done
-        return warp_wait(smem_u32(&bars.pv_done[half][j & 1]), (j >> 1) & 1, abort, ctrl);
-    };
-    uint32_t it = 0, ch = 0;     // pages of every unit / of units with this half
+    const uint32_t s_full = smem_u32(&bars.s_full[half]), p_full = smem_u32(&bars.p_full[half]);
+    uint32_t it = 0, ch = 0, uh = 0;     // blocks of every unit / of units with this half; units with it
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    for (uint32_t k = 0; ok; ++k) {
+        const int u = take_unit(bars, s_unit, k, lane, abort, ctrl);
+        if (u < 0) break;
         const PfTile t = tiles[u / Hk];
-        const int kvh = u % Hk;
+        const int kvh = u % Hk, nb = (t.npg + 1) / 2;
         const bool present = half == 0 || t.ntok > Tq;
         if (!present) {
-            it += t.npg;
+            it += nb;
             continue;
         }
         const int tok = half * Tq + tq;                   // token of this row within the tile
@@ -295,51 +322,58 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
         const bool by_index = !kPacked || canonical_no_window;
         const int key_lo = kPacked ? t.pad : lo, key_hi = kPacked ? (active ? t.t0 + tok : -1) : pos;
         float m_run = -INFINITY, l = 0.f;
-        for (int k = 0; k < t.npg; ++k) {
-            const uint32_t j = ch + k;
-            const int pg = t.first_page + k;
-            ok = pf_wait(smem_u32(&bars.s_full[half][j & 1]), (j >> 1) & 1, abort, ctrl);
+        for (int b = 0; b < nb; ++b) {
+            const uint32_t j = ch + b;
+            const int pg0 = t.first_page + 2 * b, npb = min(2, t.npg - 2 * b);   // pages in this block
+            ok = pf_wait(s_full, j & 1, abort, ctrl);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            uint32_t s[64];
-            tmem_ld32(tmem + lane_base + s_col + (j & 1) * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-            tmem_ld32(tmem + lane_base + s_col + (j & 1) * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+            uint32_t s[128];
+            #pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+                tmem_ld32(s_addr + 32 * q4, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * q4]));
             tmem_wait_ld();
+            const int key0 = pg0 * kPageSize;
             if (by_index) {
-                // keys c of this page visible to the row: key_lo <= pg*64 + c <= key_hi
-                // (cache positions, or indices of a canonical pack)
-                const int c_lo = key_lo - pg * kPageSize, c_hi = key_hi - pg * kPageSize;
-                if (!__all_sync(0xffffffffu, c_lo <= 0 && c_hi >= kPageSize - 1)) {
+                // keys c of this block visible to the row: key_lo <= key0 + c <= key_hi
+                const int c_lo = key_lo - key0, c_hi = min(key_hi - key0, npb * kPageSize - 1);
+                if (!__all_sync(0xffffffffu, c_lo <= 0 && c_hi >= 2 * kPageSize - 1)) {
                     #pragma unroll
-                    for (int c = 0; c < 64; ++c)
+                    for (int c = 0; c < 128; ++c)
                         if (c < c_lo || c > c_hi) s[c] = __float_as_uint(-INFINITY);
                 }
             } else {
-                // key c of block pg is visible when it belongs to the row's
-                // sequence at a position <= pos (and inside the window); a
-                // block wholly of that sequence and before pos skips the test
-                const int4 bi = blk[pg];
-                const bool full = active && bi.x && bi.y == seg && bi.w <= pos && (W <= 0 || bi.z > pos - W);
+                // key c is visible when it belongs to the row's sequence at a
+                // position <= pos (and inside the window); a page wholly of
+                // that sequence and before pos skips the test
+                bool full = active && npb == 2;
+                #pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int4 bi = blk[min(pg0 + q, pg0 + npb - 1)];
+                    full = full && bi.x && bi.y == seg && bi.w <= pos && (W <= 0 || bi.z > pos - W);
+                }
                 if (!__all_sync(0xffffffffu, full)) {
-                    const int st = (it + k) % C::kStages;
-                    // the stage's ids and positions came by bulk copy on kv_full
-                    mbar_wait(smem_u32(&kv_full[st]), ((it + k) / C::kStages) & 1, kPfTimeoutNs);
+                    const int st = (it + b) % C::kStages;
+                    // the stage's ids and positions came by bulk copy with V
+                    mbar_wait(smem_u32(&v_full[st]), ((it + b) / C::kStages) & 1, kPfTimeoutNs);
                     const int4* sg = reinterpret_cast<const int4*>(s_mask[st]);
-                    const int4* sp = reinterpret_cast<const int4*>(s_mask[st] + 64);
+                    const int4* sp = reinterpret_cast<const int4*>(s_mask[st] + 128);
                     #pragma unroll
-                    for (int c4 = 0; c4 < 16; ++c4) {
+                    for (int c4 = 0; c4 < 32; ++c4) {
                         const int4 g4 = sg[c4], p4 = sp[c4];
                         const int gs[4] = {g4.x, g4.y, g4.z, g4.w}, pp[4] = {p4.x, p4.y, p4.z, p4.w};
                         #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const bool vis = active && gs[e] == seg && pp[e] <= pos && (W <= 0 || pp[e] > pos - W);
-                            if (!vis) s[4 * c4 + e] = __float_as_uint(-INFINITY);
+                            const int c = 4 * c4 + e;
+                            const bool vis = active && c < npb * kPageSize && gs[e] == seg && pp[e] <= pos &&
+                                             (W <= 0 || pp[e] > pos - W);
+                            if (!vis) s[c] = __float_as_uint(-INFINITY);
                         }
                     }
                 }
             }
-            const float mx = max64(s) * sl2;               // scale > 0: the max commutes with it
+            const float mx = max128(s) * sl2;              // scale > 0: the max commutes with it
             const bool need = mx > m_run + kRescaleLog2;
             float alpha = 1.f;
             if (need) {
@@ -348,63 +382,61 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
                 l *= alpha;
             }
             const float neg_mu = m_run == -INFINITY ? 0.f : -m_run;
-            // The denominator sums the bf16 weights the PV MMA multiplies,
-            // so the normalised weights are an exact convex combination.
-            uint32_t pk[32];
-            float acc[8];
-            #pragma unroll
-            for (int c = 0; c < 64; c += 2) {
-                pk[c >> 1] = pack_bf16x2(exp2_approx(fmaf(__uint_as_float(s[c]), sl2, neg_mu)),
-                                         exp2_approx(fmaf(__uint_as_float(s[c + 1]), sl2, neg_mu)));
-                const float lo_w = __uint_as_float(pk[c >> 1] << 16), hi_w = __uint_as_float(pk[c >> 1] & 0xffff0000u);
-                const int k = (c >> 1) & 7;
-                acc[k] = c < 16 ? lo_w + hi_w : acc[k] + (lo_w + hi_w);
-            }
-            l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-            // O is rescaled (rarely: lazy threshold) only after the PV of the
-            // previous page; otherwise the softmax does not wait for the PV.
-            const bool rescale = k > 0 && __any_sync(0xffffffffu, need && alpha != 1.f);
-            if (rescale) {
-                ok = pv_wait(j - 1);
-                if (!ok) break;
-                tc_fence_after();
-            }
-            if (rescale) {
+            // O (complete up to the previous block: its PV preceded this S) is
+            // rescaled only when some row's max grew past the threshold
+            if (b > 0 && __any_sync(0xffffffffu, need && alpha != 1.f)) {
                 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t o[32];
-                    tmem_ld32(tmem + lane_base + o_col + c0, o);
+                    tmem_ld32(o_addr + c0, o);
                     tmem_wait_ld();
                     #pragma unroll
                     for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                    tmem_st32(tmem + lane_base + o_col + c0, o);
+                    tmem_st32(o_addr + c0, o);
                 }
-                tmem_wait_st();
             }
-            // P over the first 32 columns of its S buffer (S already read)
-            tmem_st32(tmem + lane_base + s_col + (j & 1) * 64, pk);
+            // P as bf16 pairs over the first 64 columns of S; the denominator
+            // sums the same rounded weights, so the normalised weights are an
+            // exact convex combination
+            float acc[8];
+            #pragma unroll
+            for (int h64 = 0; h64 < 2; ++h64) {
+                uint32_t pk[32];
+                #pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                    const int cc = 64 * h64 + c;
+                    pk[c >> 1] = pack_bf16x2(exp2_approx(fmaf(__uint_as_float(s[cc]), sl2, neg_mu)),
+                                             exp2_approx(fmaf(__uint_as_float(s[cc + 1]), sl2, neg_mu)));
+                    const float lw = __uint_as_float(pk[c >> 1] << 16), hw = __uint_as_float(pk[c >> 1] & 0xffff0000u);
+                    const int k = (c >> 1) & 7;
+                    acc[k] = (h64 == 0 && c < 16) ? lw + hw : acc[k] + (lw + hw);
+                }
+                tmem_st32(s_addr + 32 * h64, pk);
+            }
+            l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
             // V rows outside every row's range hold no cached value of this
             // tile (possibly stale or non-finite): half A zeroes them so that
-            // 0 * V stays 0 (the issuer runs PV_B after PV_A).
-            const int v_lo = t.lo_min - pg * kPageSize, v_hi = t.pos_max - pg * kPageSize;
-            if (half == 0 && (v_lo > 0 || v_hi < kPageSize - 1)) {
-                const uint32_t vb = st_s + ((it + k) % C::kStages) * C::kStageBytes + C::kKvBytes;
-                for (int i = m; i < kPageSize * C::kBoxes * 8; i += 128) {
+            // 0 * V stays 0 (the issuer runs PV_B after PV_A)
+            const int v_lo = t.lo_min - key0, v_hi = min(t.pos_max - key0, npb * kPageSize - 1);
+            if (half == 0 && (v_lo > 0 || v_hi < 2 * kPageSize - 1)) {
+                mbar_wait(smem_u32(&v_full[(it + b) % C::kStages]), ((it + b) / C::kStages) & 1, kPfTimeoutNs);
+                const uint32_t vb = st_s + ((it + b) % C::kStages) * C::kStageBytes + C::kKBytes;
+                for (int i = m; i < 2 * kPageSize * C::kBoxes * 8; i += 128) {
                     const int r = i / (C::kBoxes * 8), rest = i % (C::kBoxes * 8);
                     if (r < v_lo || r > v_hi)
                         asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};"
-                                     ::"r"(vb + (rest >> 3) * 8192 + r * 128 + (rest & 7) * 16), "r"(0)
+                                     ::"r"(vb + (rest >> 3) * 16384 + r * 128 + (rest & 7) * 16), "r"(0)
                                      : "memory");
                 }
-                fence_proxy_async_shared();   // zeroed V rows, read by the MMA
+                fence_proxy_async_shared();
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars.p_full[half][j & 1]));
+            mbar_arrive(p_full);
         }
         if (!ok) break;
         // Epilogue: O / l (with the sink's share of the denominator).
-        ok = pv_wait(ch + t.npg - 1);
+        ok = warp_wait(smem_u32(&bars.o_done[half]), uh & 1, abort, ctrl);
         if (!ok) break;
         tc_fence_after();
         const int h = kvh * g + jh;
@@ -420,7 +452,7 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
         #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t o[32];
-            tmem_ld32(tmem + lane_base + o_col + c0, o);
+            tmem_ld32(o_addr + c0, o);
             tmem_wait_ld();
             if (active) {
                 #pragma unroll
@@ -437,8 +469,9 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
         // The next unit's first PV overwrites O only after this read (its
         // p_full arrival follows in program order).
         tc_fence_before();
-        ch += t.npg;
-        it += t.npg;
+        ch += nb;
+        it += nb;
+        ++uh;
     }
 }
 
@@ -448,10 +481,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                    const __grid_constant__ CUtensorMap v_map, const __grid_constant__ PrefillArgs a) {
     using C = PfCfg<D, kPacked>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t kv_full[C::kStages];
-    __shared__ __align__(8) uint64_t kv_empty[C::kStages];
+    // K and V of a stage fill and drain separately: K is free once the
+    // block's S is done, V (with the packed mask) once its PV is
+    __shared__ __align__(8) uint64_t k_full[C::kStages], k_empty[C::kStages];
+    __shared__ __align__(8) uint64_t v_full[C::kStages], v_empty[C::kStages];
     __shared__ __align__(8) PfBars bars;
-    __shared__ __align__(16) int s_mask[C::kMaskStages][128];   // packed: segment ids [0,64), positions [64,128)
+    __shared__ __align__(16) int s_mask[C::kMaskStages][256];   // packed: segment ids [0,128), positions [128,256)
+    __shared__ int s_unit[kUnitSlots];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -467,19 +503,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         reinterpret_cast<uint4*>(sm + C::kOffQ)[i] = make_uint4(0, 0, 0, 0);
     if (tid == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(smem_u32(&kv_full[s]), 1);
-            mbar_init(smem_u32(&kv_empty[s]), 1);
+            mbar_init(smem_u32(&k_full[s]), 1);
+            mbar_init(smem_u32(&k_empty[s]), 1);
+            mbar_init(smem_u32(&v_full[s]), 1);
+            mbar_init(smem_u32(&v_empty[s]), 1);
         }
         mbar_init(smem_u32(&bars.q_full), 1);
         mbar_init(smem_u32(&bars.q_empty), 1);
         mbar_init(smem_u32(&bars.mma_done), 1);
+        for (int k = 0; k < kUnitSlots; ++k) {
+            mbar_init(smem_u32(&bars.unit_full[k]), 1);
+            mbar_init(smem_u32(&bars.unit_empty[k]), kUnitReaders);
+        }
         for (int h = 0; h < 2; ++h) {
-            mbar_init(smem_u32(&bars.s_full[h][0]), 1);
-            mbar_init(smem_u32(&bars.s_full[h][1]), 1);
-            for (int b = 0; b < 2; ++b) {
-                mbar_init(smem_u32(&bars.p_full[h][b]), 128);
-                mbar_init(smem_u32(&bars.pv_done[h][b]), 1);
-            }
+            mbar_init(smem_u32(&bars.s_full[h]), 1);
+            mbar_init(smem_u32(&bars.p_full[h]), 128);
+            mbar_init(smem_u32(&bars.o_done[h]), 1);
         }
         s_abort = 0;
         fence_barrier_init();
@@ -504,14 +543,38 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int n_units = (ctrl->magic == kPlanMagic ? ctrl->n_items : 0) * Hk;
     const PfTile* tiles = reinterpret_cast<const PfTile*>(a.ws + a.L.tiles);
 
-    if (warp == 0) {
+    // The issuing warpgroup hands registers to the softmax warpgroups.
+    if (warp >= 4) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+        // ---------------- softmax + epilogue: warps 4..7 half A, 8..11 half B ----------------
+        softmax_half<D, kPacked>(a, tiles, n_units, (warp - 4) >> 2, warp & 3, lane, tmem, st_s, bars, s_mask,
+                                 v_full, s_unit, abort, ctrl);
+    } else {
+      // one setmaxnreg site for the whole issuing warpgroup
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
+      if (warp == 0) {
         // ---------------- TMA producer (whole warp, one lane issues) ----------------
-        uint32_t it = 0, ui = 0;
+        uint32_t it = 0, ui = 0;     // blocks loaded, units whose Q was loaded
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ui) {
+        int u = blockIdx.x;
+        for (uint32_t k = 0; ok; ++k) {
+            if (k > 0) {
+                int v = 0;
+                if (lane == 0) v = (int)gridDim.x + atomicAdd(&ctrl->next_item, 1);
+                u = __shfl_sync(0xffffffffu, v, 0);
+            }
+            const int slot = k % kUnitSlots;
+            ok = warp_wait(smem_u32(&bars.unit_empty[slot]), ((k / kUnitSlots) & 1) ^ 1, abort, ctrl);
+            if (!ok) break;
+            if (lane == 0) {
+                s_unit[slot] = u < n_units ? u : -1;
+                mbar_arrive(smem_u32(&bars.unit_full[slot]));
+            }
+            __syncwarp();
+            if (u >= n_units) break;
             const PfTile t = tiles[u / Hk];
             const int kvh = u % Hk, nh = uni(t.ntok > Tq ? 2 : 1), npg = uni(t.npg), t0 = uni(t.t0);
-            const int first = uni(t.first_page), row = uni(t.row);
+            const int first = uni(t.first_page), row = uni(t.row), nb = (npg + 1) / 2;
             ok = warp_wait(smem_u32(&bars.q_empty), (ui & 1) ^ 1, abort, ctrl);
             if (!ok) break;
             elect_arrive_expect_tx(smem_u32(&bars.q_full), nh * C::kBoxes * 128 * g * Tq);
@@ -519,36 +582,54 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 for (int b = 0; b < C::kBoxes; ++b)
                     elect_tma_3d(q_s + h * C::kQBytes + b * 16384, &q_map, b * 64, kvh * g, t0 + h * Tq,
                                  smem_u32(&bars.q_full));
+            ++ui;
             const int* trow = kPacked ? nullptr : a.table + (size_t)row * a.pages_per_row + first;
-            for (int k = 0; k < npg; ++k, ++it) {
-                const int s = it % C::kStages;
-                ok = warp_wait(smem_u32(&kv_empty[s]), ((it / C::kStages) & 1) ^ 1, abort, ctrl);
+            for (int bk = 0; bk < nb; ++bk, ++it) {
+                const int s = it % C::kStages, npb = min(2, npg - 2 * bk);
+                const uint32_t kb = st_s + s * C::kStageBytes, vb = kb + C::kKBytes;
+                int page[2] = {0, 0}, blk0[2] = {0, 0};
+                for (int q = 0; q < npb; ++q) {
+                    if (kPacked) {
+                        blk0[q] = (first + 2 * bk + q) * kPageSize;
+                    } else {
+                        page[q] = uni(__ldg(trow + 2 * bk + q));
+                        if (page[q] < 0 || page[q] >= a.num_pages) {
+                            if (lane == 0) set_error(ctrl, kErrBadPage);
+                            page[q] = 0;
+                        }
+                    }
+                }
+                // page q of the block: rows [64 q, 64 q + 64) of every box
+                ok = warp_wait(smem_u32(&k_empty[s]), ((it / C::kStages) & 1) ^ 1, abort, ctrl);
                 if (!ok) break;
-                const uint32_t kb = st_s + s * C::kStageBytes, vb = kb + C::kKvBytes;
-                if (kPacked) {
-                    // key block first + k of the pack: tokens [64 blk, 64 blk + 64)
-                    const int blk0 = (first + k) * kPageSize;
-                    elect_arrive_expect_tx(smem_u32(&kv_full[s]), C::kStageBytes + 512);
+                elect_arrive_expect_tx(smem_u32(&k_full[s]), npb * C::kBoxes * C::kPageBytes);
+                for (int q = 0; q < npb; ++q)
                     for (int b = 0; b < C::kBoxes; ++b) {
-                        elect_tma_3d(kb + b * 8192, &k_map, b * 64, kvh, blk0, smem_u32(&kv_full[s]));
-                        elect_tma_3d(vb + b * 8192, &v_map, b * 64, kvh, blk0, smem_u32(&kv_full[s]));
+                        if (kPacked)
+                            elect_tma_3d(kb + b * 16384 + q * C::kPageBytes, &k_map, b * 64, kvh, blk0[q],
+                                         smem_u32(&k_full[s]));
+                        else
+                            elect_tma_2d(kb + b * 16384 + q * C::kPageBytes, &k_map, b * 64,
+                                         (page[q] * Hk + kvh) * kPageSize, smem_u32(&k_full[s]));
                     }
-                    const uint32_t mb = smem_u32(&s_mask[kPacked ? s : 0][0]);
-                    elect_bulk_load(mb, reinterpret_cast<const int*>(a.ws + a.L.seg_pad) + blk0, 256,
-                                    smem_u32(&kv_full[s]));
-                    elect_bulk_load(mb + 256, reinterpret_cast<const int*>(a.ws + a.L.pos_pad) + blk0, 256,
-                                    smem_u32(&kv_full[s]));
-                } else {
-                    int page = uni(__ldg(trow + k));
-                    if (page < 0 || page >= a.num_pages) {
-                        if (lane == 0) set_error(ctrl, kErrBadPage);
-                        page = 0;
-                    }
-                    const int y = (page * Hk + kvh) * kPageSize;
-                    elect_arrive_expect_tx(smem_u32(&kv_full[s]), C::kStageBytes);
+                ok = warp_wait(smem_u32(&v_empty[s]), ((it / C::kStages) & 1) ^ 1, abort, ctrl);
+                if (!ok) break;
+                const uint32_t vf = smem_u32(&v_full[s]);
+                elect_arrive_expect_tx(vf, npb * (C::kBoxes * C::kPageBytes + (kPacked ? 512 : 0)));
+                for (int q = 0; q < npb; ++q) {
                     for (int b = 0; b < C::kBoxes; ++b) {
-                        elect_tma_2d(kb + b * 8192, &k_map, b * 64, y, smem_u32(&kv_full[s]));
-                        elect_tma_2d(vb + b * 8192, &v_map, b * 64, y, smem_u32(&kv_full[s]));
+                        if (kPacked)
+                            elect_tma_3d(vb + b * 16384 + q * C::kPageBytes, &v_map, b * 64, kvh, blk0[q], vf);
+                        else
+                            elect_tma_2d(vb + b * 16384 + q * C::kPageBytes, &v_map, b * 64,
+                                         (page[q] * Hk + kvh) * kPageSize, vf);
+                    }
+                    if (kPacked) {
+                        const uint32_t mb = smem_u32(&s_mask[kPacked ? s : 0][0]);
+                        elect_bulk_load(mb + q * 256, reinterpret_cast<const int*>(a.ws + a.L.seg_pad) + blk0[q], 256,
+                                        vf);
+                        elect_bulk_load(mb + 512 + q * 256,
+                                        reinterpret_cast<const int*>(a.ws + a.L.pos_pad) + blk0[q], 256, vf);
                     }
                 }
             }
@@ -556,88 +637,110 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // Drain: the last load of each stage and of Q has landed before exit.
         for (uint32_t k = 0; k < (uint32_t)C::kStages && k < it; ++k) {
             const uint32_t j = it - 1 - k;
-            mbar_wait(smem_u32(&kv_full[j % C::kStages]), (j / C::kStages) & 1, kPfTimeoutNs);
+            mbar_wait(smem_u32(&k_full[j % C::kStages]), (j / C::kStages) & 1, kPfTimeoutNs);
+            mbar_wait(smem_u32(&v_full[j % C::kStages]), (j / C::kStages) & 1, kPfTimeoutNs);
         }
         if (ui > 0) mbar_wait(smem_u32(&bars.q_full), (ui - 1) & 1, kPfTimeoutNs);
     } else if (warp == 1) {
         // ---------------- MMA issuer (whole warp, one lane issues) ----------------
-        constexpr uint32_t idesc_s = instr_desc(128, 64, 0, 0);
+        constexpr uint32_t idesc_s = instr_desc(128, 128, 0, 0);
+        constexpr uint32_t idesc_s64 = instr_desc(128, 64, 0, 0);    // a block of one page
         constexpr uint32_t idesc_o = instr_desc(128, D, 0, 1);
         uint32_t it = 0, ui = 0, cnt0 = 0, cnt1 = 0;
+        bool issued = false;
         bool ok = true;
         // Descriptors are built once: the start-address field (bits 0..13,
         // address >> 4) is linear, so every operand below is a base
         // descriptor plus a constant.
         const uint64_t dq = smem_desc(q_s, 16, 1024), dk = smem_desc(st_s, 16, 1024);
-        const uint64_t dv = smem_desc(st_s + C::kKvBytes, 8192, 1024);
-        // S_h(j) = Q_h K^T into S buffer j & 1 of half h (K of stage s).
-        auto qk = [&](int h, uint32_t j, int s) {
+        const uint64_t dv = smem_desc(st_s + C::kKBytes, 16384, 1024);
+        // S_h = Q_h K^T of the block in stage s (N = 128 keys, or 64 when
+        // the block holds one page: the softmax masks the other 64 columns)
+        auto qk = [&](int h, int s, bool one_page) {
+            const uint32_t idesc = one_page ? idesc_s64 : idesc_s;
             const uint64_t a0 = dq + (uint64_t)(h * (C::kQBytes >> 4));
             const uint64_t b0 = dk + (uint64_t)(s * (C::kStageBytes >> 4));
-            const uint32_t d = tmem + 128u * h + (j & 1) * 64;
             #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
-                umma_bf16(d, a0 + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
-                          b0 + (uint64_t)((ks >> 2) * 512 + (ks & 3) * 2), idesc_s, ks > 0 ? 1u : 0u);
-            umma_commit(smem_u32(&bars.s_full[h][j & 1]));
+                umma_bf16(tmem + 128u * h, a0 + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
+                          b0 + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), idesc, ks > 0 ? 1u : 0u);
+            umma_commit(smem_u32(&bars.s_full[h]));
         };
-        // O_h += P_h V (V of stage s); the first page of a unit overwrites O_h.
-        auto pv = [&](int h, uint32_t j, int s, bool first) -> bool {
-            if (!warp_wait(smem_u32(&bars.p_full[h][j & 1]), (j >> 1) & 1, abort, ctrl)) return false;
+        // O_h += P_h V of the block in stage s; P of block j sits over S_h
+        // (8 columns per 16 keys); the first block of a unit overwrites O_h.
+        // A one-page block stops after 64 keys (the weights beyond are 0).
+        auto pv = [&](int h, uint32_t j, int s, bool first, bool one_page) -> bool {
+            if (!warp_wait(smem_u32(&bars.p_full[h]), j & 1, abort, ctrl)) return false;
             tc_fence_after();
-            // P of page j sits in S buffer j & 1 of the half (8 columns per 16 keys)
-            const uint32_t a0 = tmem + 128u * h + (j & 1) * 64;
             const uint64_t b0 = dv + (uint64_t)(s * (C::kStageBytes >> 4));
-            const uint32_t d = tmem + C::kColO + h * D;
             #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                umma_bf16_ts(d, a0 + ks * 8, b0 + (uint64_t)(ks * 128), idesc_o, (first && ks == 0) ? 0u : 1u);
-            umma_commit(smem_u32(&bars.pv_done[h][j & 1]));
+            for (int ks = 0; ks < 8; ++ks)
+                if (ks < 4 || !one_page)
+                    umma_bf16_ts(tmem + C::kColO + h * D, tmem + 128u * h + ks * 8, b0 + (uint64_t)(ks * 128),
+                                 idesc_o, (first && ks == 0) ? 0u : 1u);
             return true;
         };
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ui) {
+        for (uint32_t k = 0; ok; ++k, ++ui) {
+            const int u = take_unit(bars, s_unit, k, lane, abort, ctrl);
+            if (u < 0) break;
             const PfTile t = tiles[u / Hk];
-            const int nh = uni(t.ntok > Tq ? 2 : 1), npg = uni(t.npg);
+            const int nh = uni(t.ntok > Tq ? 2 : 1), npg = uni(t.npg), nb = (npg + 1) / 2;
             ok = warp_wait(smem_u32(&bars.q_full), ui & 1, abort, ctrl);
             if (!ok) break;
+            issued = true;
             tc_fence_after();
-            for (int k = 0; k <= npg && ok; ++k) {
-                const uint32_t j = it + k;
+            for (int bk = 0; bk <= nb && ok; ++bk) {
+                const uint32_t j = it + bk;
                 const int s = j % C::kStages, sp = (j - 1) % C::kStages;
-                if (k < npg) {
-                    ok = warp_wait(smem_u32(&kv_full[s]), (j / C::kStages) & 1, abort, ctrl);
-                    if (!ok) break;
-                    tc_fence_after();
-                    qk(0, cnt0 + k, s);
+                for (int h = 0; h < nh && ok; ++h) {
+                    const uint32_t jh = (h ? cnt1 : cnt0) + bk;
+                    if (bk > 0) {
+                        if (h == 0) {
+                            ok = warp_wait(smem_u32(&v_full[sp]), ((j - 1) / C::kStages) & 1, abort, ctrl);
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        ok = pv(h, jh - 1, sp, bk == 1, npg - 2 * (bk - 1) == 1);   // S_h of this block follows it
+                    }
+                    if (ok && bk < nb) {
+                        if (h == 0) {
+                            ok = warp_wait(smem_u32(&k_full[s]), (j / C::kStages) & 1, abort, ctrl);
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        qk(h, s, npg - 2 * bk == 1);
+                    }
                 }
-                if (k > 0) ok = pv(0, cnt0 + k - 1, sp, k == 1);
                 if (!ok) break;
-                if (nh == 2) {
-                    if (k < npg) qk(1, cnt1 + k, s);
-                    if (k > 0) ok = pv(1, cnt1 + k - 1, sp, k == 1);
-                    if (!ok) break;
-                }
-                if (k == npg - 1) umma_commit(smem_u32(&bars.q_empty));   // every S of the unit issued
-                if (k > 0) umma_commit(smem_u32(&kv_empty[sp]));
+                if (bk < nb) umma_commit(smem_u32(&k_empty[s]));          // the block's S issued
+                if (bk == nb - 1) umma_commit(smem_u32(&bars.q_empty));   // every S of the unit issued
+                if (bk > 0) umma_commit(smem_u32(&v_empty[sp]));
             }
-            it += npg;
-            cnt0 += npg;
-            if (nh == 2) cnt1 += npg;
+            if (!ok) break;
+            for (int h = 0; h < nh; ++h) umma_commit(smem_u32(&bars.o_done[h]));
+            it += nb;
+            cnt0 += nb;
+            if (nh == 2) cnt1 += nb;
         }
         // Drain: every MMA issued has finished before TMEM is freed.
-        if (ui > 0) {
+        if (issued) {
             umma_commit(smem_u32(&bars.mma_done));
             mbar_wait(smem_u32(&bars.mma_done), 0, kPfTimeoutNs);
         }
-    } else {
-        // ---------------- softmax + epilogue: warps 2..5 half A, 6..9 half B ----------------
-        softmax_half<D, kPacked>(a, tiles, n_units, (warp - 2) >> 2, warp & 3, lane, tmem, st_s, bars, s_mask,
-                                 kv_full, abort, ctrl);
+      }
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (tid == 0) {
+        // The last CTA out rewinds the unit cursor for the next launch.
+        __threadfence();
+        if (atomicAdd(&ctrl->done_ctas, 1) == (int)gridDim.x - 1) {
+            ctrl->next_item = 0;
+            ctrl->done_ctas = 0;
+        }
+    }
     if (warp == 1) {
         __syncwarp();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols)

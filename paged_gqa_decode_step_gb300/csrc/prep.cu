@@ -668,6 +668,8 @@ __device__ void build_prefill_plan(const PrefillPrepArgs& a) {
     if (tid == 0) {
         if (s_bad) set_error(ctrl, kErrBadPos);
         ctrl->n_items = s_bad ? 0 : n_tiles;
+        ctrl->next_item = 0;               // unit cursor: CTA b takes unit b first, later ones from here
+        ctrl->done_ctas = 0;
         ctrl->kv_heads = a.kv_heads;
         ctrl->group = a.heads / a.kv_heads;
         ctrl->head_dim = a.head_dim;
@@ -854,6 +856,8 @@ __device__ void build_packed_plan(const PrefillPrepArgs& a) {
     if (tid == 0) {
         if (s_bad) set_error(ctrl, kErrBadPos);
         ctrl->n_items = s_bad ? 0 : n_tiles;
+        ctrl->next_item = 0;               // unit cursor: CTA b takes unit b first, later ones from here
+        ctrl->done_ctas = 0;
         ctrl->kv_heads = a.kv_heads;
         ctrl->group = a.heads / a.kv_heads;
         ctrl->head_dim = a.head_dim;
