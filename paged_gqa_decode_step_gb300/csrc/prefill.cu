@@ -204,6 +204,20 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
+// Packed fp32 pairs (one instruction for two lanes of work): d = a * b + c
+// with b, c shared, and d += b.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+    asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %4};\n mov.b64 rc, {%5, %5};\n"
+        " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float b0, float b1) {
+    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%0, %1};\n mov.b64 rb, {%2, %3};\n"
+        " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+        : "+f"(d0), "+f"(d1) : "f"(b0), "f"(b1));
+}
+
 // Max of 64 values as eight short independent chains.
 __device__ __forceinline__ float max64(const uint32_t (&s)[64]) {
     float acc[8];
@@ -258,7 +272,8 @@ constexpr int kUnitSlots = 4;
 constexpr int kUnitReaders = 9;      // the issuing warp and the eight softmax warps
 
 struct PfBars {
-    uint64_t q_full, q_empty, mma_done;
+    uint64_t q_full[2], q_empty[2];   // [half]: Q loaded / every S of the unit reading it done
+    uint64_t mma_done;
     uint64_t unit_full[kUnitSlots], unit_empty[kUnitSlots];
     uint64_t s_full[2];      // [half]: S of the block done (its previous PV too)
     uint64_t p_full[2];      // [half]: P of the block written (128 arrivals)
@@ -405,11 +420,17 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
                 #pragma unroll
                 for (int c = 0; c < 64; c += 2) {
                     const int cc = 64 * h64 + c;
-                    pk[c >> 1] = pack_bf16x2(exp2_approx(fmaf(__uint_as_float(s[cc]), sl2, neg_mu)),
-                                             exp2_approx(fmaf(__uint_as_float(s[cc + 1]), sl2, neg_mu)));
+                    float x0, x1;
+                    ffma2(x0, x1, __uint_as_float(s[cc]), __uint_as_float(s[cc + 1]), sl2, neg_mu);
+                    pk[c >> 1] = pack_bf16x2(exp2_approx(x0), exp2_approx(x1));
                     const float lw = __uint_as_float(pk[c >> 1] << 16), hw = __uint_as_float(pk[c >> 1] & 0xffff0000u);
-                    const int k = (c >> 1) & 7;
-                    acc[k] = (h64 == 0 && c < 16) ? lw + hw : acc[k] + (lw + hw);
+                    const int k = (c >> 1) & 3;               // four pair accumulators
+                    if (h64 == 0 && c < 8) {
+                        acc[2 * k] = lw;
+                        acc[2 * k + 1] = hw;
+                    } else {
+                        fadd2(acc[2 * k], acc[2 * k + 1], lw, hw);
+                    }
                 }
                 tmem_st32(s_addr + 32 * h64, pk);
             }
@@ -508,8 +529,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             mbar_init(smem_u32(&v_full[s]), 1);
             mbar_init(smem_u32(&v_empty[s]), 1);
         }
-        mbar_init(smem_u32(&bars.q_full), 1);
-        mbar_init(smem_u32(&bars.q_empty), 1);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(smem_u32(&bars.q_full[h]), 1);
+            mbar_init(smem_u32(&bars.q_empty[h]), 1);
+        }
         mbar_init(smem_u32(&bars.mma_done), 1);
         for (int k = 0; k < kUnitSlots; ++k) {
             mbar_init(smem_u32(&bars.unit_full[k]), 1);
@@ -554,7 +577,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
       if (warp == 0) {
         // ---------------- TMA producer (whole warp, one lane issues) ----------------
-        uint32_t it = 0, ui = 0;     // blocks loaded, units whose Q was loaded
+        uint32_t kit = 0, vit = 0, uq[2] = {0, 0};   // K, V blocks loaded; units whose Q half h was loaded
         bool ok = true;
         int u = blockIdx.x;
         for (uint32_t k = 0; ok; ++k) {
@@ -575,78 +598,89 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const PfTile t = tiles[u / Hk];
             const int kvh = u % Hk, nh = uni(t.ntok > Tq ? 2 : 1), npg = uni(t.npg), t0 = uni(t.t0);
             const int first = uni(t.first_page), row = uni(t.row), nb = (npg + 1) / 2;
-            ok = warp_wait(smem_u32(&bars.q_empty), (ui & 1) ^ 1, abort, ctrl);
-            if (!ok) break;
-            elect_arrive_expect_tx(smem_u32(&bars.q_full), nh * C::kBoxes * 128 * g * Tq);
-            for (int h = 0; h < nh; ++h)
-                for (int b = 0; b < C::kBoxes; ++b)
-                    elect_tma_3d(q_s + h * C::kQBytes + b * 16384, &q_map, b * 64, kvh * g, t0 + h * Tq,
-                                 smem_u32(&bars.q_full));
-            ++ui;
             const int* trow = kPacked ? nullptr : a.table + (size_t)row * a.pages_per_row + first;
-            for (int bk = 0; bk < nb; ++bk, ++it) {
-                const int s = it % C::kStages, npb = min(2, npg - 2 * bk);
-                const uint32_t kb = st_s + s * C::kStageBytes, vb = kb + C::kKBytes;
-                int page[2] = {0, 0}, blk0[2] = {0, 0};
+            // Page q of block bk: the cache page (paged) or the pack's key
+            // index (packed) of rows [64 q, 64 q + 64) of every box.
+            auto page_of = [&](int bk, int q) -> int {
+                if (kPacked) return (first + 2 * bk + q) * kPageSize;
+                int page = uni(__ldg(trow + 2 * bk + q));
+                if (page < 0 || page >= a.num_pages) {
+                    if (lane == 0) set_error(ctrl, kErrBadPage);
+                    page = 0;
+                }
+                return (page * Hk + kvh) * kPageSize;
+            };
+            auto load_k = [&](int bk) -> bool {
+                const int s = kit % C::kStages, npb = min(2, npg - 2 * bk);
+                if (!warp_wait(smem_u32(&k_empty[s]), ((kit / C::kStages) & 1) ^ 1, abort, ctrl)) return false;
+                const uint32_t kb = st_s + s * C::kStageBytes, kf = smem_u32(&k_full[s]);
+                elect_arrive_expect_tx(kf, npb * C::kBoxes * C::kPageBytes);
                 for (int q = 0; q < npb; ++q) {
-                    if (kPacked) {
-                        blk0[q] = (first + 2 * bk + q) * kPageSize;
-                    } else {
-                        page[q] = uni(__ldg(trow + 2 * bk + q));
-                        if (page[q] < 0 || page[q] >= a.num_pages) {
-                            if (lane == 0) set_error(ctrl, kErrBadPage);
-                            page[q] = 0;
-                        }
+                    const int y = page_of(bk, q);
+                    for (int b = 0; b < C::kBoxes; ++b) {
+                        if (kPacked) elect_tma_3d(kb + b * 16384 + q * C::kPageBytes, &k_map, b * 64, kvh, y, kf);
+                        else elect_tma_2d(kb + b * 16384 + q * C::kPageBytes, &k_map, b * 64, y, kf);
                     }
                 }
-                // page q of the block: rows [64 q, 64 q + 64) of every box
-                ok = warp_wait(smem_u32(&k_empty[s]), ((it / C::kStages) & 1) ^ 1, abort, ctrl);
-                if (!ok) break;
-                elect_arrive_expect_tx(smem_u32(&k_full[s]), npb * C::kBoxes * C::kPageBytes);
-                for (int q = 0; q < npb; ++q)
-                    for (int b = 0; b < C::kBoxes; ++b) {
-                        if (kPacked)
-                            elect_tma_3d(kb + b * 16384 + q * C::kPageBytes, &k_map, b * 64, kvh, blk0[q],
-                                         smem_u32(&k_full[s]));
-                        else
-                            elect_tma_2d(kb + b * 16384 + q * C::kPageBytes, &k_map, b * 64,
-                                         (page[q] * Hk + kvh) * kPageSize, smem_u32(&k_full[s]));
-                    }
-                ok = warp_wait(smem_u32(&v_empty[s]), ((it / C::kStages) & 1) ^ 1, abort, ctrl);
-                if (!ok) break;
-                const uint32_t vf = smem_u32(&v_full[s]);
+                ++kit;
+                return true;
+            };
+            auto load_v = [&](int bk) -> bool {
+                const int s = vit % C::kStages, npb = min(2, npg - 2 * bk);
+                if (!warp_wait(smem_u32(&v_empty[s]), ((vit / C::kStages) & 1) ^ 1, abort, ctrl)) return false;
+                const uint32_t vb = st_s + s * C::kStageBytes + C::kKBytes, vf = smem_u32(&v_full[s]);
                 elect_arrive_expect_tx(vf, npb * (C::kBoxes * C::kPageBytes + (kPacked ? 512 : 0)));
                 for (int q = 0; q < npb; ++q) {
+                    const int y = page_of(bk, q);
                     for (int b = 0; b < C::kBoxes; ++b) {
-                        if (kPacked)
-                            elect_tma_3d(vb + b * 16384 + q * C::kPageBytes, &v_map, b * 64, kvh, blk0[q], vf);
-                        else
-                            elect_tma_2d(vb + b * 16384 + q * C::kPageBytes, &v_map, b * 64,
-                                         (page[q] * Hk + kvh) * kPageSize, vf);
+                        if (kPacked) elect_tma_3d(vb + b * 16384 + q * C::kPageBytes, &v_map, b * 64, kvh, y, vf);
+                        else elect_tma_2d(vb + b * 16384 + q * C::kPageBytes, &v_map, b * 64, y, vf);
                     }
                     if (kPacked) {
+                        // segment ids and positions of the block's keys, for the per-key mask
                         const uint32_t mb = smem_u32(&s_mask[kPacked ? s : 0][0]);
-                        elect_bulk_load(mb + q * 256, reinterpret_cast<const int*>(a.ws + a.L.seg_pad) + blk0[q], 256,
+                        elect_bulk_load(mb + q * 256, reinterpret_cast<const int*>(a.ws + a.L.seg_pad) + y, 256, vf);
+                        elect_bulk_load(mb + 512 + q * 256, reinterpret_cast<const int*>(a.ws + a.L.pos_pad) + y, 256,
                                         vf);
-                        elect_bulk_load(mb + 512 + q * 256,
-                                        reinterpret_cast<const int*>(a.ws + a.L.pos_pad) + blk0[q], 256, vf);
                     }
                 }
+                ++vit;
+                return true;
+            };
+            // K of the first block goes first: its stage frees before the
+            // previous unit's last S is done, which is what Q waits for.
+            ok = load_k(0);
+            #pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (!ok || h >= nh) break;
+                ok = warp_wait(smem_u32(&bars.q_empty[h]), (uq[h] & 1) ^ 1, abort, ctrl);
+                if (!ok) break;
+                const uint32_t qf = smem_u32(&bars.q_full[h]);
+                elect_arrive_expect_tx(qf, C::kBoxes * 128 * g * Tq);
+                for (int b = 0; b < C::kBoxes; ++b)
+                    elect_tma_3d(q_s + h * C::kQBytes + b * 16384, &q_map, b * 64, kvh * g, t0 + h * Tq, qf);
+                ++uq[h];
             }
+            ok = ok && load_v(0);
+            for (int bk = 1; bk < nb && ok; ++bk) ok = load_k(bk) && load_v(bk);
         }
-        // Drain: the last load of each stage and of Q has landed before exit.
-        for (uint32_t k = 0; k < (uint32_t)C::kStages && k < it; ++k) {
-            const uint32_t j = it - 1 - k;
+        // Drain: every load issued has landed before exit.
+        for (uint32_t k = 0; k < (uint32_t)C::kStages && k < kit; ++k) {
+            const uint32_t j = kit - 1 - k;
             mbar_wait(smem_u32(&k_full[j % C::kStages]), (j / C::kStages) & 1, kPfTimeoutNs);
+        }
+        for (uint32_t k = 0; k < (uint32_t)C::kStages && k < vit; ++k) {
+            const uint32_t j = vit - 1 - k;
             mbar_wait(smem_u32(&v_full[j % C::kStages]), (j / C::kStages) & 1, kPfTimeoutNs);
         }
-        if (ui > 0) mbar_wait(smem_u32(&bars.q_full), (ui - 1) & 1, kPfTimeoutNs);
+        #pragma unroll
+        for (int h = 0; h < 2; ++h)
+            if (uq[h] > 0) mbar_wait(smem_u32(&bars.q_full[h]), (uq[h] - 1) & 1, kPfTimeoutNs);
     } else if (warp == 1) {
         // ---------------- MMA issuer (whole warp, one lane issues) ----------------
         constexpr uint32_t idesc_s = instr_desc(128, 128, 0, 0);
         constexpr uint32_t idesc_s64 = instr_desc(128, 64, 0, 0);    // a block of one page
         constexpr uint32_t idesc_o = instr_desc(128, D, 0, 1);
-        uint32_t it = 0, ui = 0, cnt0 = 0, cnt1 = 0;
         bool issued = false;
         bool ok = true;
         // Descriptors are built once: the start-address field (bits 0..13,
@@ -680,47 +714,84 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                  idesc_o, (first && ks == 0) ? 0u : 1u);
             return true;
         };
-        for (uint32_t k = 0; ok; ++k, ++ui) {
-            const int u = take_unit(bars, s_unit, k, lane, abort, ctrl);
-            if (u < 0) break;
-            const PfTile t = tiles[u / Hk];
-            const int nh = uni(t.ntok > Tq ? 2 : 1), npg = uni(t.npg), nb = (npg + 1) / 2;
-            ok = warp_wait(smem_u32(&bars.q_full), ui & 1, abort, ctrl);
-            if (!ok) break;
-            issued = true;
-            tc_fence_after();
-            for (int bk = 0; bk <= nb && ok; ++bk) {
-                const uint32_t j = it + bk;
-                const int s = j % C::kStages, sp = (j - 1) % C::kStages;
-                for (int h = 0; h < nh && ok; ++h) {
-                    const uint32_t jh = (h ? cnt1 : cnt0) + bk;
-                    if (bk > 0) {
-                        if (h == 0) {
-                            ok = warp_wait(smem_u32(&v_full[sp]), ((j - 1) / C::kStages) & 1, abort, ctrl);
-                            if (!ok) break;
-                            tc_fence_after();
-                        }
-                        ok = pv(h, jh - 1, sp, bk == 1, npg - 2 * (bk - 1) == 1);   // S_h of this block follows it
-                    }
-                    if (ok && bk < nb) {
-                        if (h == 0) {
-                            ok = warp_wait(smem_u32(&k_full[s]), (j / C::kStages) & 1, abort, ctrl);
-                            if (!ok) break;
-                            tc_fence_after();
-                        }
-                        qk(h, s, npg - 2 * bk == 1);
-                    }
+        // Blocks of successive units form one stream: per half, the PV of the
+        // previous block (possibly the previous unit's last) goes before the
+        // S of the current one, so a unit boundary leaves no gap in the
+        // tensor pipe beyond the Q load.
+        // One step per block of the stream (and a last one for the end):
+        // for each half, PV of the pending block, then S of this one.  The
+        // pending block is always the previous one (index it - 1, counters
+        // cs_h - 1).  The half loop stays rolled so that each MMA sequence
+        // is issued from one place; per-half state is selected by value.
+        constexpr uint32_t kPend = 1, kPendFirst = 2, kPendLast = 4, kPendOne = 8, kPendB = 16, kEnd = 32;
+        uint32_t it = 0, uq0 = 0, uq1 = 0, cs0 = 0, cs1 = 0, f = 0;   // blocks; units / S per half; flags
+        int nh = 0, npg = 0, bk = 0;                                  // the current unit and block
+        for (uint32_t k = 0; ok;) {
+            if (2 * bk >= npg) {                                      // the unit is done: the next one
+                if (npg > 0) {
+                    ++uq0;
+                    if (nh == 2) ++uq1;
                 }
-                if (!ok) break;
-                if (bk < nb) umma_commit(smem_u32(&k_empty[s]));          // the block's S issued
-                if (bk == nb - 1) umma_commit(smem_u32(&bars.q_empty));   // every S of the unit issued
-                if (bk > 0) umma_commit(smem_u32(&v_empty[sp]));
+                const int u = take_unit(bars, s_unit, k++, lane, abort, ctrl);
+                if (u == -2) {
+                    ok = false;
+                    break;
+                }
+                nh = 0;
+                npg = 0;
+                bk = 0;
+                if (u < 0) {
+                    f |= kEnd;
+                } else {
+                    const PfTile t = tiles[u / Hk];
+                    nh = uni(t.ntok > Tq ? 2 : 1);
+                    npg = uni(t.npg);
+                }
+            }
+            const int s = it % C::kStages;
+            const bool one = npg - 2 * bk == 1;
+            #pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                if ((f & kPend) && (h == 0 || (f & kPendB))) {
+                    if (h == 0) {
+                        ok = warp_wait(smem_u32(&v_full[(it - 1) % C::kStages]), ((it - 1) / C::kStages) & 1, abort,
+                                       ctrl);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    ok = pv(h, (h ? cs1 : cs0) - 1, (it - 1) % C::kStages, f & kPendFirst, f & kPendOne);
+                    if (!ok) break;
+                    if (f & kPendLast) umma_commit(smem_u32(&bars.o_done[h]));
+                }
+                if (h < nh) {
+                    if (h == 0) {
+                        ok = warp_wait(smem_u32(&k_full[s]), (it / C::kStages) & 1, abort, ctrl);
+                        if (!ok) break;
+                    }
+                    if (bk == 0) {
+                        ok = warp_wait(smem_u32(&bars.q_full[h]), (h ? uq1 : uq0) & 1, abort, ctrl);
+                        if (!ok) break;
+                    }
+                    tc_fence_after();
+                    issued = true;
+                    qk(h, s, one);
+                }
             }
             if (!ok) break;
-            for (int h = 0; h < nh; ++h) umma_commit(smem_u32(&bars.o_done[h]));
-            it += nb;
-            cnt0 += nb;
-            if (nh == 2) cnt1 += nb;
+            if (f & kPend) umma_commit(smem_u32(&v_empty[(it - 1) % C::kStages]));   // the pending block's PV issued
+            if (f & kEnd) break;
+            umma_commit(smem_u32(&k_empty[s]));                                       // this block's S issued
+            const bool last = 2 * (bk + 1) >= npg;
+            if (last) {
+                umma_commit(smem_u32(&bars.q_empty[0]));
+                if (nh == 2) umma_commit(smem_u32(&bars.q_empty[1]));
+            }
+            f = kPend | (bk == 0 ? kPendFirst : 0) | (last ? kPendLast : 0) | (one ? kPendOne : 0) |
+                (nh == 2 ? kPendB : 0);
+            ++cs0;
+            if (nh == 2) ++cs1;
+            ++it;
+            ++bk;
         }
         // Drain: every MMA issued has finished before TMEM is freed.
         if (issued) {
