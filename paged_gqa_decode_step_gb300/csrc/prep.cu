@@ -888,7 +888,9 @@ __global__ void __launch_bounds__(128) packed_rope_kernel(const __grid_constant_
                               rope ? static_cast<const T*>(a.rope_cos) + (size_t)pos * D : nullptr,
                               rope ? static_cast<const T*>(a.rope_sin) + (size_t)pos * D : nullptr, Hq, Hk, D, true);
     }
-    griddep_wait();
+    // The last block (the last to start) waits for the planner, so this
+    // grid completes after it; the other blocks leave their SM slots at once.
+    if (blockIdx.x == gridDim.x - 1) griddep_wait();
 }
 
 // The tile list: one block.  Lets the rope kernel launched after it start
@@ -898,16 +900,17 @@ __global__ void __launch_bounds__(kPrepThreads) prefill_plan_kernel(const __grid
     build_prefill_plan(a);
 }
 
-// Block i rotates and writes token i.  It waits for the planner before it
-// exits, so that the completion of this grid (all the attention kernel
-// waits for) also covers the tile list.
+// Block i rotates and writes token i.  The last block waits for the planner
+// before it exits, so that the completion of this grid (all the attention
+// kernel waits for) also covers the tile list; the other blocks do not wait,
+// or a wave of them would hold every SM until the planner is done.
 constexpr int kRopeThreads = 128;
 
 template <typename T>
 __global__ void __launch_bounds__(kRopeThreads) prefill_rope_kernel(const __grid_constant__ PrefillPrepArgs a) {
     griddep_launch_dependents();
     rope_write_token<T>(a, blockIdx.x);
-    griddep_wait();
+    if (blockIdx.x == gridDim.x - 1) griddep_wait();
 }
 
 // ---------------------------------------------------------------------------
