@@ -19,9 +19,15 @@
 //                   V read from shared memory MN-major
 // The issuer runs PV_A(j-1) S_A(j) PV_B(j-1) S_B(j): each half's S follows
 // its previous PV (P lives in S's columns), and each half's softmax runs
-// while the tensor core works for the other half.  The running max is
-// raised lazily: O is rescaled in TMEM only when a row's max grows by more
-// than 2^8 (S of a block done implies the PV before it is done).
+// while the tensor core works for the other half.  Blocks of successive
+// units form one stream, so a unit's first S follows the previous unit's
+// last PV of the same half.  The running max is raised lazily: O is
+// rescaled in TMEM only when a row's max grows by more than 2^8 (S of a
+// block done implies the PV before it is done).
+//
+// Units are taken in the planner's descending-cost order: CTA b starts with
+// unit b, later ones come from a global cursor that the last CTA out rewinds.
+// K and V of a stage fill and drain on separate barriers.
 //
 // Packed sequences (Llama example page, `packed`) run the same kernel: the
 // pack is a contiguous cache of 64-token pages, K and V come by 3-D TMA from
