@@ -282,7 +282,7 @@ struct PfBars {
     uint64_t mma_done;
     uint64_t unit_full[kUnitSlots], unit_empty[kUnitSlots];
     uint64_t s_full[2];      // [half]: S of the block done (its previous PV too)
-    uint64_t p_full[2];      // [half]: P of the block written (128 arrivals)
+    uint64_t p_full[2];      // [half]: P of the block written (one arrival per warp of the half)
     uint64_t o_done[2];      // [half]: the unit's last PV done
 };
 
@@ -457,9 +457,12 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
                 }
                 fence_proxy_async_shared();
             }
+            // every lane's stores are complete and fenced before its warp's
+            // one arrival (128 single arrivals on one word serialise)
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(p_full);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
         }
         if (!ok) break;
         // Epilogue: O / l (with the sink's share of the denominator).
@@ -546,7 +549,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(smem_u32(&bars.s_full[h]), 1);
-            mbar_init(smem_u32(&bars.p_full[h]), 128);
+            mbar_init(smem_u32(&bars.p_full[h]), 4);
             mbar_init(smem_u32(&bars.o_done[h]), 1);
         }
         s_abort = 0;
@@ -605,11 +608,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const int kvh = u % Hk, nh = uni(t.ntok > Tq ? 2 : 1), npg = uni(t.npg), t0 = uni(t.t0);
             const int first = uni(t.first_page), row = uni(t.row), nb = (npg + 1) / 2;
             const int* trow = kPacked ? nullptr : a.table + (size_t)row * a.pages_per_row + first;
+            // The unit's page ids, 32 at a time: lane l holds page pid_base + l
+            // (pid_cur) and the next window's (pid_nxt, read a window ahead),
+            // so no load waits for the table but the unit's first.
+            int pid_base = -32, pid_cur = 0, pid_nxt = 0;
             // Page q of block bk: the cache page (paged) or the pack's key
             // index (packed) of rows [64 q, 64 q + 64) of every box.
             auto page_of = [&](int bk, int q) -> int {
                 if (kPacked) return (first + 2 * bk + q) * kPageSize;
-                int page = uni(__ldg(trow + 2 * bk + q));
+                const int pi = 2 * bk + q;              // pages are visited in order
+                if (pi - pid_base >= 32) {
+                    if (pid_base < 0) pid_cur = lane < npg ? __ldg(trow + lane) : 0;
+                    else pid_cur = pid_nxt;
+                    pid_base += 32;
+                    pid_nxt = pid_base + 32 + lane < npg ? __ldg(trow + pid_base + 32 + lane) : 0;
+                }
+                int page = __shfl_sync(0xffffffffu, pid_cur, pi & 31);
                 if (page < 0 || page >= a.num_pages) {
                     if (lane == 0) set_error(ctrl, kErrBadPage);
                     page = 0;
