@@ -734,15 +734,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                  idesc_o, (first && ks == 0) ? 0u : 1u);
             return true;
         };
-        // Blocks of successive units form one stream: per half, the PV of the
-        // previous block (possibly the previous unit's last) goes before the
-        // S of the current one, so a unit boundary leaves no gap in the
-        // tensor pipe beyond the Q load.
-        // One step per block of the stream (and a last one for the end):
-        // for each half, PV of the pending block, then S of this one.  The
-        // pending block is always the previous one (index it - 1, counters
-        // cs_h - 1).  The half loop stays rolled so that each MMA sequence
-        // is issued from one place; per-half state is selected by value.
+        // Blocks of successive units form one stream, one step per block (and
+        // a last one for the end): for each half, the PV of the pending block
+        // (possibly the previous unit's last), then the S of this one, so a
+        // unit boundary leaves no gap in the tensor pipe beyond the Q load.
+        // The pending block is always the previous one (index it - 1,
+        // counters cs_h - 1).  The half loop stays rolled so that each MMA
+        // sequence is issued from one place; per-half state is selected by
+        // value.
         constexpr uint32_t kPend = 1, kPendFirst = 2, kPendLast = 4, kPendOne = 8, kPendB = 16, kEnd = 32;
         uint32_t it = 0, uq0 = 0, uq1 = 0, cs0 = 0, cs1 = 0, f = 0;   // blocks; units / S per half; flags
         int nh = 0, npg = 0, bk = 0;                                  // the current unit and block
