@@ -49,3 +49,13 @@ def test_fewer_than_three_warmup_steps_are_refused():
     r = bench("--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "2")
     assert r.returncode != 0
     assert "warmup" in r.stderr
+
+
+def test_our_arm_fails_loudly_without_a_gpu():
+    # no CPU fallback: without a CUDA device the timed arm exits with an error
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    r = bench("--steps", "3", "--warmup", "3")
+    assert r.returncode != 0
+    assert not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
