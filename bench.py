@@ -116,13 +116,17 @@ def profiled_traffic(workload):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled while the GPU works."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons sampled while the GPU works.
+    summary() covers every sample; window(t0, t1) only those taken between
+    two time.time() stamps (a timed region)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, device):
         self.proc = None
+        self.rows = None
         self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         sel = []
         try:
@@ -148,26 +152,46 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    def _load(self):
+        if self.rows is not None:
+            return self.rows
+        import datetime
         self.out.flush()
         rows = []
         with open(self.out.name) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) != 9:
+                if len(parts) != 10:
                     continue
                 try:
-                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
                 except ValueError:
                     continue
         os.unlink(self.out.name)
+        self.rows = rows
+        return rows
+
+    def _summarise(self, rows, extra=None):
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
-        sm = sorted(r[0] for r in rows)
-        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
-                "samples": len(rows)}
+        reasons = sorted({self.REASONS[i] for _, _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        sm = sorted(r[1] for r in rows)
+        d = {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[2] for r in rows), "reasons": reasons,
+             "samples": len(rows)}
+        if extra:
+            d.update(extra)
+        return d
+
+    def summary(self):
+        return self._summarise(self._load())
+
+    def window(self, t0, t1):
+        rows = self._load()
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        if inside:
+            return self._summarise(inside, {"within_timed_region": True})
+        return self._summarise(rows, {"within_timed_region": False})
 
 
 # ------------------------------------------------------------- end to end --
@@ -231,6 +255,46 @@ def e2e_pipelined(dev_tensors, names, run, out, n_steps, world):
     secs = loop(n_steps) / n_steps
     h2d_bytes = sum(v.numel() * v.element_size() for v in host[0].values())
     return secs, h2d_bytes, host_out[0].numel() * host_out[0].element_size()
+
+
+# ------------------------------------------------------------- timing --
+def device_ms(fn, n, flush=None):
+    """Mean device milliseconds of n calls of fn on the current stream.  Without
+    `flush` (inputs larger than L2) one pair of CUDA events brackets all n
+    calls; with it, a pair brackets each call and L2 is flushed (a write of
+    `flush`, outside the events) before each."""
+    torch.cuda.synchronize()
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for e0, e1 in evs:
+        flush.fill_(1)
+        e0.record()
+        fn()
+        e1.record()
+    torch.cuda.synchronize()
+    return sum(e0.elapsed_time(e1) for e0, e1 in evs) / n
+
+
+def keep_busy(fn, seconds, flush=None):
+    """Untimed calls of fn for about `seconds` of wall time, so that the clock
+    samples around a short timed region see the GPU under this load."""
+    t_end = time.time() + seconds
+    i = 0
+    while time.time() < t_end:
+        if flush is not None:
+            flush.fill_(1)
+        fn()
+        i += 1
+        if i % 32 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
 
 
 # -------------------------------------------------------------- distributed --
@@ -312,6 +376,88 @@ def cpu_oracle_rate(w, host, budget_s, rows_per_step=None, max_steps=None, threa
     return done_bytes / spent / 1e9, spent, desc, steps
 
 
+# --------------------------------------------------- the other configs --
+DECODE_EXTRAS = ("llama8b_layer", "gptoss20b_full", "gptoss20b_sliding", "gpt2_f32")
+
+
+def measure_decode_config(args, b, w, dev, world, rank):
+    """One decode workload in light form: whole fused steps (CUDA events, L2
+    flushed unless the K/V outgrows it), the attention kernel alone against
+    the HBM roofline, and the clocks seen while the steps ran."""
+    t = wl.generate(w, dev, seed=rank_seed(w, rank))
+    pos_list = t["positions"].cpu().tolist()
+    num_pages = t["k_pool"].shape[0]
+    tables = b.rope_tables(w.rope_theta, w.head_dim, w.max_seq, w.torch_dtype) if w.rope_theta > 0 else (None, None)
+    p = b.make_params(w.rows, w.heads, w.kv_heads, w.head_dim, w.pages_per_row, num_pages, w.torch_dtype,
+                      window=w.window, rope_cos=tables[0], rope_sin=tables[1])
+    ws = b.new_workspace(p)
+    out = torch.empty_like(t["q"])
+    kvb = kv_bytes(w, pos_list)
+    large = kvb > 2 * L2_BYTES
+    flush = None if large else torch.empty(4 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def step():
+        b.decode_fused(p, t["q"], t["k_new"], t["v_new"], t["positions"], t["table"], t["k_pool"], t["v_pool"], out, ws)
+
+    for _ in range(args.warmup):
+        step()
+    b.check_status(ws)
+    with ClockSampler(dev) as clocks:
+        t_load = time.time()
+        if not args.quick:
+            keep_busy(step, 0.3, flush)
+        barrier(world)
+        ms = device_ms(step, args.steps, flush)
+        t_end = time.time()
+        barrier(world)
+    clk = clocks.window(t_load, t_end)
+    b.check_status(ws)
+    ms = max_over_ranks(ms, world)
+    all_kv = sum_over_ranks(kvb, world)
+
+    q_rot = torch.empty_like(t["q"])
+    b.rope_write_kv(p, t["q"], t["k_new"], t["v_new"], t["positions"], t["table"], q_rot, t["k_pool"], t["v_pool"], ws)
+    b.plan(p, t["positions"], ws)
+    att_ms = device_ms(lambda: b.attend(p, q_rot, t["positions"], t["table"], t["k_pool"], t["v_pool"], out, ws),
+                       max(20, min(args.steps, 400)), flush)
+    b.check_status(ws)
+    att_bytes = attend_bytes(w, pos_list)
+    peak, peak_kind = measured_hbm_peak()
+    achieved = att_bytes / (att_ms * 1e-3) / 1e9
+    value = all_kv / (ms * 1e-3) / 1e9
+    return {
+        "metric": "KV GB/s", "value": value, "unit": "GB/s", "ms_per_step": ms, "steps": args.steps,
+        "dtype": w.dtype, "rows": w.rows, "heads": w.heads, "kv_heads": w.kv_heads, "head_dim": w.head_dim,
+        "window": w.window, "positions": f"{w.positions} [{w.pos_lo}, {w.pos_hi}]",
+        "kv_bytes_per_step": kvb, "row_steps_per_s": w.rows * world / (ms * 1e-3),
+        "frac_of_hbm_peak": value / world / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "kernel": f"attend_kernel<{w.dtype},{w.head_dim}>", "bytes_per_launch": att_bytes,
+                     "launch_us": att_ms * 1e3, "peak_kind": peak_kind},
+        "l2": "inputs larger than L2" if large else "L2 flushed (512 MB write) between timed steps, outside the events",
+        "clocks": clk,
+    }
+
+
+def other_configs(args, world, rank, local):
+    """Every other workload of the step, measured in this process; keyed by name."""
+    from paged_gqa_decode_step_gb300 import binding as b
+    dev = torch.device("cuda", local)
+    res = {}
+    for name in DECODE_EXTRAS:
+        if name == args.workload:
+            continue
+        res[name] = measure_decode_config(args, b, wl.WORKLOADS[name], dev, world, rank)
+        torch.cuda.empty_cache()
+    for w in wl.PREFILL_WORKLOADS.values():
+        res[w.name] = run_prefill(args, w, world, rank, local, light=True)
+        torch.cuda.empty_cache()
+    for w in wl.PACKED_WORKLOADS.values():
+        res[w.name] = run_packed(args, w, world, rank, local, light=True)
+        torch.cuda.empty_cache()
+    return res
+
+
 # ---------------------------------------------------------------- our arm --
 def run_ours(args, w, world, rank, local):
     from paged_gqa_decode_step_gb300 import build
@@ -341,32 +487,16 @@ def run_ours(args, w, world, rank, local):
     b.check_status(ws)
     launches_per_step = b.last_launch_count()
 
-    # ---- timed region: K whole steps
+    # ---- timed region: K whole steps (clock samples over a loaded lead-in and the region)
     with ClockSampler(dev) as clocks:
+        t_load = time.time()
+        if not args.quick:
+            keep_busy(step, 0.3, flush)
         barrier(world)
-        torch.cuda.synchronize()
-        if large:
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(args.steps):
-                step()
-            e1.record()
-            torch.cuda.synchronize()
-            ms = e0.elapsed_time(e1) / args.steps
-        else:
-            total = 0.0
-            for _ in range(args.steps):
-                flush.fill_(1)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                step()
-                e1.record()
-                e1.synchronize()
-                total += e0.elapsed_time(e1)
-            ms = total / args.steps
-        torch.cuda.synchronize()
+        ms = device_ms(step, args.steps, flush)
+        t_end = time.time()
         barrier(world)
-    clk = clocks.summary()
+    clk = clocks.window(t_load, t_end)
     b.check_status(ws)
     if args.quick:
         # profiling mode: warm-up and timed steps only
@@ -409,18 +539,9 @@ def run_ours(args, w, world, rank, local):
     b.plan(p, t["positions"], ws)
     for _ in range(3):
         b.attend(p, q_rot, t["positions"], t["table"], t["k_pool"], t["v_pool"], out, ws)
-    n_att = max(20, min(args.steps, 400))
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_att)]
-    torch.cuda.synchronize()
-    for e0, e1 in evs:
-        if flush is not None:
-            flush.fill_(1)
-        e0.record()
-        b.attend(p, q_rot, t["positions"], t["table"], t["k_pool"], t["v_pool"], out, ws)
-        e1.record()
-    torch.cuda.synchronize()
+    att_ms = device_ms(lambda: b.attend(p, q_rot, t["positions"], t["table"], t["k_pool"], t["v_pool"], out, ws),
+                       max(20, min(args.steps, 400)), flush)
     b.check_status(ws)
-    att_ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / n_att
     att_bytes = attend_bytes(w, pos_list)
     peak, peak_kind = measured_hbm_peak()
     achieved = att_bytes / (att_ms * 1e-3) / 1e9
@@ -448,6 +569,8 @@ def run_ours(args, w, world, rank, local):
         rate, spent, desc, _ = cpu_oracle_rate(w, host, args.cpu_baseline_seconds, threads=n_cores)
         cpu_par = {"value": rate, "unit": "GB/s", "cores": n_cores, "kind": "oracle", "sample": desc,
                    "seconds": round(spent, 2), "cpu": cpu_model()}
+
+    extras = None if args.no_extra else other_configs(args, world, rank, local)
 
     if rank != 0:
         return None
@@ -488,6 +611,7 @@ def run_ours(args, w, world, rank, local):
             "what": "the same step captured once in a CUDA graph and replayed"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
+        "workloads": extras,
     }
     return line
 
@@ -581,7 +705,10 @@ def cpu_oracle_prefill_rate(w, host, budget_s, max_tokens=None, seed=0):
     return flops / spent / 1e12, spent, desc, tokens
 
 
-def run_prefill(args, w, world, rank, local):
+def run_prefill(args, w, world, rank, local, light=False):
+    """Whole prefill calls timed (value), the attention kernel alone (roofline),
+    end to end through pinned host buffers and the oracle; `light` keeps the
+    first two (a per-config entry of the decode line)."""
     from paged_gqa_decode_step_gb300 import build
     build.build()
     from paged_gqa_decode_step_gb300 import binding as b
@@ -609,22 +736,15 @@ def run_prefill(args, w, world, rank, local):
     b.check_status(ws)
     launches_per_step = b.last_launch_count()
 
-    def timed(fn, n):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-        torch.cuda.synchronize()
-        for e0, e1 in evs:
-            flush.fill_(1)
-            e0.record()
-            fn()
-            e1.record()
-        torch.cuda.synchronize()
-        return sum(e0.elapsed_time(e1) for e0, e1 in evs) / n
-
     with ClockSampler(dev) as clocks:
+        t_load = time.time()
+        if not args.quick:
+            keep_busy(step, 0.3, flush)
         barrier(world)
-        ms = timed(step, args.steps)
+        ms = device_ms(step, args.steps, flush)
+        t_end = time.time()
         barrier(world)
-    clk = clocks.summary()
+    clk = clocks.window(t_load, t_end)
     b.check_status(ws)
     if args.quick:
         if rank == 0:
@@ -636,11 +756,19 @@ def run_prefill(args, w, world, rank, local):
     value = all_flops / (ms * 1e-3) / 1e12
 
     # roofline: the attention kernel alone (prefill_attend), events around each launch
-    att_ms = timed(lambda: b.prefill_attend(p, t["positions"], t["table"], t["k_pool"], t["v_pool"], out, ws),
-                   max(20, min(args.steps, 200)))
+    att_ms = device_ms(lambda: b.prefill_attend(p, t["positions"], t["table"], t["k_pool"], t["v_pool"], out, ws),
+                       max(20, min(args.steps, 200)), flush)
     b.check_status(ws)
     peak, peak_kind = measured_tensor_peak()
     achieved = flops / (att_ms * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": None, "kernel": f"prefill_kernel<{w.head_dim}>",
+            "flops_per_launch": flops, "launch_us": att_ms * 1e3, "peak_kind": peak_kind}
+    if light:
+        return {"metric": PREFILL_METRIC, "value": value, "unit": "TFLOP/s", "ms_per_step": ms,
+                "steps": args.steps, "tokens": P, "flops_per_step": flops,
+                "frac_of_tensor_peak": value / world / peak, "roofline": roof,
+                "l2": "L2 flushed (512 MB write) between timed calls, outside the events", "clocks": clk}
 
     # end to end: pinned host inputs in, output back, every call
     e2e_s, h2d, d2h = e2e_pipelined(
@@ -671,9 +799,7 @@ def run_prefill(args, w, world, rank, local):
             "l2": "L2 flushed (512 MB write) between timed steps, outside the events",
             "parallelism": f"replicas x{world} (rows sharded across ranks, no exchange)",
         },
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None, "kernel": f"prefill_kernel<{w.head_dim}>",
-                     "flops_per_launch": flops, "launch_us": att_ms * 1e3, "peak_kind": peak_kind},
+        "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": all_flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
@@ -745,7 +871,8 @@ def cpu_oracle_packed_rate(w, host, budget_s, max_seqs=None):
     return flops / spent / 1e12, spent, desc, done
 
 
-def run_packed(args, w, world, rank, local):
+def run_packed(args, w, world, rank, local, light=False):
+    """As run_prefill, for sequences packed into one row."""
     from paged_gqa_decode_step_gb300 import build
     build.build()
     from paged_gqa_decode_step_gb300 import binding as b
@@ -772,22 +899,15 @@ def run_packed(args, w, world, rank, local):
     b.check_status(ws)
     launches_per_step = b.last_launch_count()
 
-    def timed(fn, n):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-        torch.cuda.synchronize()
-        for e0, e1 in evs:
-            flush.fill_(1)
-            e0.record()
-            fn()
-            e1.record()
-        torch.cuda.synchronize()
-        return sum(e0.elapsed_time(e1) for e0, e1 in evs) / n
-
     with ClockSampler(dev) as clocks:
+        t_load = time.time()
+        if not args.quick:
+            keep_busy(step, 0.3, flush)
         barrier(world)
-        ms = timed(step, args.steps)
+        ms = device_ms(step, args.steps, flush)
+        t_end = time.time()
         barrier(world)
-    clk = clocks.summary()
+    clk = clocks.window(t_load, t_end)
     b.check_status(ws)
     if args.quick:
         if rank == 0:
@@ -798,10 +918,19 @@ def run_packed(args, w, world, rank, local):
     all_flops = sum_over_ranks(flops, world)
     value = all_flops / (ms * 1e-3) / 1e12
 
-    att_ms = timed(lambda: b.packed_attend(p, t["v"], t["positions"], out, ws), max(20, min(args.steps, 200)))
+    att_ms = device_ms(lambda: b.packed_attend(p, t["v"], t["positions"], out, ws), max(20, min(args.steps, 200)),
+                       flush)
     b.check_status(ws)
     peak, peak_kind = measured_tensor_peak()
     achieved = flops / (att_ms * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": None, "kernel": f"prefill_kernel<{w.head_dim},packed>",
+            "flops_per_launch": flops, "launch_us": att_ms * 1e3, "peak_kind": peak_kind}
+    if light:
+        return {"metric": PACKED_METRIC, "value": value, "unit": "TFLOP/s", "ms_per_step": ms,
+                "steps": args.steps, "tokens": P, "flops_per_step": flops,
+                "frac_of_tensor_peak": value / world / peak, "roofline": roof,
+                "l2": "L2 flushed (512 MB write) between timed calls, outside the events", "clocks": clk}
 
     e2e_s, h2d, d2h = e2e_pipelined(t, names, lambda d, o: b.packed(p, *(d[k] for k in names), o, ws), out,
                                     max(10, min(args.steps, 100)), world)
@@ -827,9 +956,7 @@ def run_packed(args, w, world, rank, local):
             "l2": "L2 flushed (512 MB write) between timed steps, outside the events",
             "parallelism": f"replicas x{world} (rows sharded across ranks, no exchange)",
         },
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None, "kernel": f"prefill_kernel<{w.head_dim},packed>",
-                     "flops_per_launch": flops, "launch_us": att_ms * 1e3, "peak_kind": peak_kind},
+        "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": all_flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
@@ -874,6 +1001,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--chunk-pages", type=int, default=0,
                     help="pages per split (0: the planner chooses)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the per-config entries of the other workloads")
     ap.add_argument("--quick", action="store_true",
                     help="warm-up and timed steps only, no JSON line (for profiler captures)")
     args = ap.parse_args(argv)

@@ -165,12 +165,16 @@ pdattn_status pdattn_decode_fused(const pdattn_params* p, const void* q, const v
  * Parameters whose workspace (pdattn_workspace_size) exceeds 16 MiB are
  * rejected with PDATTN_EINVAL before any launch; the Llama-3.1-8B shape at
  * 256 rows needs about 10 MiB.  The first call on each device (with that
- * device current) looks up the array's device address and clears its control
- * block; make that first call before capturing any stream.  All calls on a
- * device share the one array: calls whose work overlaps on the GPU (other
- * streams, other threads) race and must be serialised by the caller.  Bad
- * positions or page ids found on the device are skipped but not reported;
- * check the inputs beforehand or use pdattn_decode_fused for reports.
+ * device current) looks up the array's device address, which issues no work
+ * on any stream; make that first call before capturing any stream.  All calls
+ * on a device share the one array: calls whose work overlaps on the GPU
+ * (other streams, other threads) race and must be serialised by the caller.
+ * No device-side error is reported: bad positions or page ids (those rows
+ * are skipped), a device wait that ran past its limit and a rejected plan
+ * all leave the call's return value PDATTN_OK, with the outputs of the
+ * affected rows (after a timeout or a rejected plan, possibly of any row)
+ * unwritten.  Check the inputs beforehand, or use pdattn_decode_fused and
+ * pdattn_check_status where such reports matter.
  */
 pdattn_status pdattn_decode_fused_noalloc(const pdattn_params* p, const void* q, const void* k_new,
                                           const void* v_new, const int32_t* positions,
@@ -264,7 +268,10 @@ pdattn_status pdattn_packed_attend(const pdattn_params* p, int32_t n_tokens, con
 
 /*
  * Synchronises `stream`, reads the workspace's device status word, clears
- * it and returns the first error it recorded (PDATTN_OK if none).
+ * it and returns the first error it recorded (PDATTN_OK if none).  After
+ * PDATTN_ETIMEOUT from decode attention the workspace's plan is withdrawn:
+ * pdattn_attend on it is refused (PDATTN_EINVAL) until pdattn_plan,
+ * pdattn_decode or pdattn_decode_fused plans again.
  */
 pdattn_status pdattn_check_status(void* workspace, pdattn_stream stream);
 

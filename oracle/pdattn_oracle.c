@@ -428,10 +428,27 @@ int oracle_packed(const oracle_shape* p, int n, const void* q, const void* k, co
         }
     }
     const double scale = (double)(float)(1.0 / sqrt((double)D)); /* rsqrt(f32(D)) */
-    double* w = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
-    double* acc = (double*)malloc(sizeof(double) * (size_t)D);
-    if (!w || !acc) { free(w); free(acc); return ORACLE_EINVAL; }
+    /* Tokens are independent once q and k are rotated; with OpenMP they run on
+     * oracle_set_threads() threads, each with its own score and sum buffers
+     * (the same arithmetic in the same order as the serial loop). */
+#ifdef _OPENMP
+    const int nthr = omp_get_max_threads();
+#else
+    const int nthr = 1;
+#endif
+    const size_t per = (size_t)(n > 0 ? n : 1) + (size_t)D;
+    double* buf = (double*)malloc(sizeof(double) * per * (size_t)nthr);
+    if (!buf) return ORACLE_EINVAL;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthr)
+#endif
     for (int i = 0; i < n; ++i) {
+#ifdef _OPENMP
+        double* w = buf + per * (size_t)omp_get_thread_num();
+#else
+        double* w = buf;
+#endif
+        double* acc = w + (n > 0 ? n : 1);
         for (int h = 0; h < Hq; ++h) {
             const int kvh = h / group;
             const size_t qo = ((size_t)i * Hq + h) * D;
@@ -465,8 +482,7 @@ int oracle_packed(const oracle_shape* p, int n, const void* q, const void* k, co
             }
         }
     }
-    free(w);
-    free(acc);
+    free(buf);
     return ORACLE_OK;
 }
 

@@ -638,7 +638,9 @@ int32_t pdattn_last_launch_count(void) { return g_launches; }
 // Host code cannot use the variable's name as a device address; the first
 // call on each device (with that device current) looks the address up with
 // cudaGetSymbolAddress and keeps it.  Make that first call before capturing
-// any stream.
+// any stream.  The set-up issues no work on any stream: the array starts out
+// zero-filled, and the planner that opens every call rewrites each control
+// field the attention kernel reads, so nothing needs clearing.
 // ---------------------------------------------------------------------------
 namespace {
 
@@ -660,9 +662,6 @@ pdattn_status static_scratch(void** out) {
         void* ptr = nullptr;
         e = cudaGetSymbolAddress(&ptr, g_static_scratch);
         if (e != cudaSuccess || ptr == nullptr) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
-        // The status word lives in the array; start it clean.
-        e = cudaMemset(ptr, 0, 256);
-        if (e != cudaSuccess) return cuda_fail(e, "clearing the static scratch control block");
         g_static_ptr[dev] = ptr;
     }
     *out = g_static_ptr[dev];

@@ -599,15 +599,13 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             queued += d1.y;
         }
         if (lane == 0) {
-            if (ok) {
-                // Last CTA to finish fetching rewinds the cursor for the next launch.
-                __threadfence();
-                if (atomicAdd(&ctrl->done_ctas, 1) == (int)gridDim.x - 1) {
-                    ctrl->next_item = (int)gridDim.x;
-                    ctrl->done_ctas = 0;
-                }
-            } else {
-                set_error(ctrl, kErrTimeout);
+            if (!ok) fail_timeout(ctrl);
+            // The last CTA to finish fetching rewinds the cursor for the next
+            // launch (after a timeout too: every scheduler has left its loop).
+            __threadfence();
+            if (atomicAdd(&ctrl->done_ctas, 1) == (int)gridDim.x - 1) {
+                ctrl->next_item = (int)gridDim.x;
+                ctrl->done_ctas = 0;
             }
         }
         return;
@@ -627,6 +625,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             uint32_t armed_par = 0;             // parity armed on stage s
             int issued = 0;
             bool ok = true;
+            bool hold = blockIdx.x == 0 && __ldcg(&ctrl->test_hold) != 0;
             while (ok) {
                 if (!mbar_wait(bar_ifull + 8 * islot, iphase)) { ok = false; break; }
                 const uint8_t* slotp = item_q + islot * C::kItemBytes;
@@ -643,6 +642,12 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                 for (int j = 0; j < npg; j += P) {
                     const int np = min(P, npg - j);
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1)) { ok = false; break; }
+                    if (hold) {
+                        // test hook: this stage is never armed nor filled
+                        hold = false;
+                        if (++stage == S) { stage = 0; phase ^= 1; }
+                        continue;
+                    }
                     const int t0 = (first_page + j) * kPageSize;
                     const int t_lo = max(lo, t0) - t0;
                     const int t_hi = min(pos, t0 + np * kPageSize - 1) - t0 + 1;
@@ -698,7 +703,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                 }
             }
             if (!ok) {
-                set_error(ctrl, kErrTimeout);
+                fail_timeout(ctrl);
                 // Let copies in flight land before the CTA's shared memory goes away.
                 for (int s2 = 0; s2 < S; ++s2)
                     if (armed & (1u << s2)) mbar_wait(bar_full + 8 * s2, (armed_par >> s2) & 1u, 200000000ull);
@@ -719,7 +724,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             int waited = 1;
             if (lane == 0) waited = mbar_wait(bar_efull + 8 * eslot, ephase) ? 1 : 0;
             waited = __shfl_sync(0xffffffffu, waited, 0);
-            if (!waited) { if (lane == 0) set_error(ctrl, kErrTimeout); break; }
+            if (!waited) { if (lane == 0) fail_timeout(ctrl); break; }
             const uint8_t* ep = epi_q + eslot * C::kEpiBytes;
             const Meta mt = *reinterpret_cast<const Meta*>(ep);
             if (mt.flags & kTerm) break;
@@ -804,7 +809,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     bool ok = true;
     while (true) {
         if (!mbar_wait(bar_full + 8 * stage, phase)) {
-            if (lane == 0) set_error(ctrl, kErrTimeout);
+            if (lane == 0) fail_timeout(ctrl);
             ok = false;
             break;
         }
@@ -845,7 +850,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         // ---- item done: merge the four warps into an epilogue slot
         cs.stash(sm_m, sm_l, sm_o, warp, lane);
         if (!csync.sync() || !mbar_wait(bar_eempty + 8 * eslot, ephase ^ 1)) {
-            if (lane == 0) set_error(ctrl, kErrTimeout);
+            if (lane == 0) fail_timeout(ctrl);
             ok = false;
             break;
         }
@@ -877,7 +882,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         mbar_arrive(bar_efull + 8 * eslot);
         if (++eslot == kEpiSlots) { eslot = 0; ephase ^= 1; }
         // the stash buffers are rewritten by the next item
-        if (!csync.sync()) { if (lane == 0) set_error(ctrl, kErrTimeout); ok = false; break; }
+        if (!csync.sync()) { if (lane == 0) fail_timeout(ctrl); ok = false; break; }
     }
     if (ok) {
         // Tell the epilogue warp that no more items follow.
@@ -885,7 +890,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             if (tid == 0) reinterpret_cast<Meta*>(epi_q + eslot * C::kEpiBytes)->flags = kTerm;
             mbar_arrive(bar_efull + 8 * eslot);
         } else if (lane == 0) {
-            set_error(ctrl, kErrTimeout);
+            fail_timeout(ctrl);
         }
     }
 }

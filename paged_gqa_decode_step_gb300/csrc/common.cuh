@@ -33,9 +33,14 @@ struct Ctrl {
     uint32_t magic;    // kPlanMagic once a plan is written
     int rows, kv_heads, pages_per_row, max_items, group, head_dim;
     int grid;          // persistent CTAs of the attention launch: CTA b starts with item b
-    int pad[51];
+    // Test hook, never set by a call: when nonzero, CTA 0 of the decode
+    // attention kernel leaves the first stage of its first item unissued, so
+    // that the consumers' bounded wait on it runs out (the timeout path).
+    int test_hold;
+    int pad[50];
 };
 static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
+static_assert(offsetof(Ctrl, test_hold) == 52, "test hook offset is part of the test contract");
 
 // One work item of the plan: pages [first_page, first_page + npg) of one
 // (row, kv head), chunk `chunk` of `nch`; `slot` indexes its fp32 partial.
@@ -296,5 +301,13 @@ __device__ __forceinline__ uint32_t swz128(uint32_t box, int row, int chunk) {
 }
 
 __device__ __forceinline__ void set_error(Ctrl* ctrl, int bits) { atomicOr(&ctrl->status, bits); }
+
+// A bounded wait ran out: record it and withdraw the plan, whose cursor and
+// merge counters are now stale, so that a later attention-only call on this
+// workspace is refused (kErrBadPlan) until a planner runs again.
+__device__ __forceinline__ void fail_timeout(Ctrl* ctrl) {
+    set_error(ctrl, kErrTimeout);
+    atomicExch(&ctrl->magic, 0u);
+}
 
 }  // namespace pdattn

@@ -4,6 +4,8 @@ The CUDA path (tile planner, rope of q and k, tensor-core attention over the
 pack's 64-token key blocks) through the C-ABI, and the oracle's packed
 attention on the same seeded inputs, outputs within the bf16 tolerance.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -114,21 +116,27 @@ def test_packed_one_sequence_in_two_runs():
     run(W("two_runs", (100, 50, 80), 8, 2, 64, seed=9), transform=split)
 
 
-def test_packed_full_size_sampled_sequences():
-    # the Llama-3.1-8B packed row (8192 tokens); the oracle runs the four
-    # shortest sequences alone (a sequence sees only its own tokens)
+def test_packed_full_size_whole_sequences():
+    # the Llama-3.1-8B packed row (8192 tokens); the oracle runs the longest
+    # sequence, a middle one and the two shortest alone (a sequence sees only
+    # its own tokens), its tokens on all host cores
     w = wl.PACKED_LLAMA
     t = wl.generate_packed(w, "cpu")
     a = {k: wl.to_numpy(v) for k, v in t.items()}
     out = gpu_packed(w, a).cpu()
     shape = oracle.make_shape(0, w.heads, w.kv_heads, w.head_dim, 1, 1, oracle.BF16, rope_theta=w.rope_theta)
     starts = np.concatenate([[0], np.cumsum(w.lengths)])
-    for s in np.argsort(w.lengths)[:4]:
-        lo, hi = starts[s], starts[s + 1]
-        sub = {k: np.ascontiguousarray(v[lo:hi]) for k, v in a.items()}
-        _, _, _, o64, rc = oracle.packed(shape, sub["q"], sub["k"], sub["v"], sub["positions"], sub["segments"])
-        assert rc == 0
-        assert_close(out[lo:hi], o64, "bf16", f"sequence {s}")
+    order = np.argsort(w.lengths)
+    oracle.set_threads(os.cpu_count() or 1)
+    try:
+        for s in (order[-1], order[len(order) // 2], order[0], order[1]):
+            lo, hi = starts[s], starts[s + 1]
+            sub = {k: np.ascontiguousarray(v[lo:hi]) for k, v in a.items()}
+            _, _, _, o64, rc = oracle.packed(shape, sub["q"], sub["k"], sub["v"], sub["positions"], sub["segments"])
+            assert rc == 0
+            assert_close(out[lo:hi], o64, "bf16", f"sequence {s} ({hi - lo} tokens)")
+    finally:
+        oracle.set_threads(1)
 
 
 def test_packed_attend_reruns_the_attention_bit_for_bit():

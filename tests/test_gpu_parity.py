@@ -4,6 +4,7 @@ Cache writes and rotated queries must match bit for bit; attention outputs
 within max |err| <= 2e-2 and mean |err| <= 2e-3 of the fp64 oracle for bf16,
 1e-5 for f32.
 """
+import os
 from dataclasses import replace
 
 import numpy as np
@@ -205,10 +206,10 @@ FULL = [wl.LLAMA_LAYER, wl.LLAMA_SERVING, wl.GPTOSS_FULL, wl.GPTOSS_SLIDING, wl.
 
 
 @pytest.mark.parametrize("w", FULL, ids=[w.name for w in FULL])
-def test_full_size_sampled_rows(w):
+def test_full_size_whole_batch(w):
     """The bench's launch (decode_fused, planner's split choice) at full size;
-    the oracle recomputes a sample of rows (shortest, longest, random) one by
-    one, including their cache writes."""
+    the oracle recomputes every row (its rows on all host cores) and both
+    pools are compared whole, bit for bit."""
     b = binding()
     t = wl.generate(w, "cuda")
     host = {k: wl.to_numpy(v) for k, v in t.items()}
@@ -219,24 +220,14 @@ def test_full_size_sampled_rows(w):
     out = torch.empty_like(t["q"])
     b.decode_fused(p, t["q"], t["k_new"], t["v_new"], t["positions"], t["table"], t["k_pool"], t["v_pool"], out, ws)
     b.check_status(ws)
-    pos = host["positions"]
-    order = np.argsort(pos)
-    rng = np.random.default_rng(0)
-    sample = sorted(set(order[:3].tolist() + order[-3:].tolist() + rng.choice(w.rows, 6, replace=False).tolist()))
-    sub = np.array(sample)
     kp, vp = host["k_pool"], host["v_pool"]
-    shape = oracle_shape(w, num_pages, rows=len(sub))
-    _, _, out64, rc = oracle.step(shape, np.ascontiguousarray(host["q"][sub]), np.ascontiguousarray(host["k_new"][sub]),
-                                  np.ascontiguousarray(host["v_new"][sub]), np.ascontiguousarray(pos[sub]),
-                                  np.ascontiguousarray(host["table"][sub]), kp, vp)
+    oracle.set_threads(os.cpu_count() or 1)
+    try:
+        _, _, out64, rc = oracle.step(oracle_shape(w, num_pages), host["q"], host["k_new"], host["v_new"],
+                                      host["positions"], host["table"], kp, vp)
+    finally:
+        oracle.set_threads(1)
     assert rc == 0
-    assert_close(out[torch.as_tensor(sub, device="cuda")], out64, w.dtype, w.name)
-    # the sampled rows' cache slots, bit for bit
-    pages = host["table"][sub, pos[sub] // 64]
-    offs = pos[sub] % 64
-    gk = wl.to_numpy(t["k_pool"][torch.as_tensor(pages, device="cuda"), :, torch.as_tensor(offs, device="cuda"), :])
-    gv = wl.to_numpy(t["v_pool"][torch.as_tensor(pages, device="cuda"), :, torch.as_tensor(offs, device="cuda"), :])
-    assert np.array_equal(gk.view(np.uint8), kp[pages, :, offs, :].view(np.uint8))
-    assert np.array_equal(gv.view(np.uint8), vp[pages, :, offs, :].view(np.uint8))
-    # every row is finite and, for bf16, inside the range of a convex combination of N(0,1) values
-    assert torch.isfinite(out.float()).all()
+    assert_close(out, out64, w.dtype, w.name)
+    assert np.array_equal(wl.to_numpy(t["k_pool"]).view(np.uint8), kp.view(np.uint8)), "k pool differs"
+    assert np.array_equal(wl.to_numpy(t["v_pool"]).view(np.uint8), vp.view(np.uint8)), "v pool differs"

@@ -4,6 +4,8 @@ The CUDA path (rope + write at slots, tile list, tensor-core attention)
 through the C-ABI, and the oracle's prefill on the same seeded inputs: the
 pools must match bit for bit, the outputs within the bf16 tolerance.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -150,14 +152,19 @@ def test_prefill_full_size_sampled_tokens():
     assert np.array_equal(wl.to_numpy(d["k_pool"]).view(np.uint8), kp.view(np.uint8))
     assert np.array_equal(wl.to_numpy(d["v_pool"]).view(np.uint8), vp.view(np.uint8))
     got = out.cpu()
-    one = oracle.make_shape(1, w.heads, w.kv_heads, w.head_dim, w.pages_per_row, num_pages, oracle.BF16)
-    rng = np.random.default_rng(11)
-    sample = np.concatenate([[0, P - 1], rng.choice(P, 40, replace=False)])
-    for i in sample:
-        r = int(a["rows"][i])
-        _, o64, rc = oracle.decode(one, q_rot[i:i + 1], a["positions"][i:i + 1], a["table"][r:r + 1], kp, vp)
-        assert rc == 0
-        assert_close(got[i:i + 1], o64, "bf16", f"token {i}")
+    # every token of two whole rows, the longest prefix and a middle one,
+    # each token a decode row of the oracle (its rows on all host cores)
+    rows = [w.rows - 1, w.rows // 2 - 1]
+    idx = np.flatnonzero(np.isin(a["rows"], rows))
+    shape = oracle.make_shape(len(idx), w.heads, w.kv_heads, w.head_dim, w.pages_per_row, num_pages, oracle.BF16)
+    oracle.set_threads(os.cpu_count() or 1)
+    try:
+        _, o64, rc = oracle.decode(shape, np.ascontiguousarray(q_rot[idx]), np.ascontiguousarray(a["positions"][idx]),
+                                   np.ascontiguousarray(tab_tok[idx]), kp, vp)
+    finally:
+        oracle.set_threads(1)
+    assert rc == 0
+    assert_close(got[torch.as_tensor(idx)], o64, "bf16", f"rows {rows}")
 
 
 def test_prefill_attend_reruns_the_attention_bit_for_bit():
