@@ -439,6 +439,81 @@ def measure_decode_config(args, b, w, dev, world, rank):
     }
 
 
+def measure_layers(args, b, w, n_layers, dev, world, rank):
+    """gpt-oss-20b decode step over n_layers layers (LayerPairs: a window-128
+    layer, then a full one; shared positions and page table, per-layer
+    caches): one pdattn_decode_layers call against one decode_fused call per
+    layer, back to back on the stream, and against those calls replayed from
+    a CUDA graph.  K/V bytes are all layers' visible pages."""
+    base = wl.generate(w, dev, seed=rank_seed(w, rank))
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(rank_seed(w, rank) + 1)
+    pos_list = base["positions"].cpu().tolist()
+    num_pages = base["k_pool"].shape[0]
+    cos, sin = b.rope_tables(w.rope_theta, w.head_dim, w.max_seq, w.torch_dtype)
+    windows = [128 if l % 2 == 0 else 0 for l in range(n_layers)]
+    layers = []
+    for l in range(n_layers):
+        y = {k: torch.randn(base[k].shape, generator=gen, device=dev, dtype=torch.float32).to(w.torch_dtype)
+             for k in ("q", "k_new", "v_new", "k_pool", "v_pool")}
+        y["out"] = torch.empty_like(y["q"])
+        y["window"] = windows[l]
+        layers.append(y)
+    p = b.make_params(w.rows, w.heads, w.kv_heads, w.head_dim, w.pages_per_row, num_pages, w.torch_dtype,
+                      rope_cos=cos, rope_sin=sin)
+    per_layer = [b.make_params(w.rows, w.heads, w.kv_heads, w.head_dim, w.pages_per_row, num_pages, w.torch_dtype,
+                               window=windows[l], rope_cos=cos, rope_sin=sin) for l in range(n_layers)]
+    ws = b.new_layers_workspace(p, n_layers)
+    ws_l = [b.new_workspace(q) for q in per_layer]
+    kvb = sum(kv_bytes(replace_window(w, windows[l]), pos_list) for l in range(n_layers))
+    large = kvb > 2 * L2_BYTES
+    flush = None if large else torch.empty(4 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def fused():
+        b.decode_layers(p, layers, base["positions"], base["table"], ws)
+
+    def separate():
+        for l, y in enumerate(layers):
+            b.decode_fused(per_layer[l], y["q"], y["k_new"], y["v_new"], base["positions"], base["table"],
+                           y["k_pool"], y["v_pool"], y["out"], ws_l[l])
+
+    res = {}
+    for name, fn in (("one_call", fused), ("per_layer_calls", separate)):
+        for _ in range(args.warmup):
+            fn()
+        with ClockSampler(dev) as clocks:
+            t_load = time.time()
+            keep_busy(fn, 0.3, flush)
+            ms = device_ms(fn, args.steps, flush)
+            t_end = time.time()
+        res[name] = {"ms_per_step": ms, "kv_gbs": kvb / (ms * 1e-3) / 1e9, "clocks": clocks.window(t_load, t_end)}
+    b.check_status(ws)
+    for q in ws_l:
+        b.check_status(q)
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            separate()
+        for _ in range(3):
+            graph.replay()
+        ms = device_ms(graph.replay, args.steps, flush)
+        res["per_layer_calls_graph"] = {"ms_per_step": ms, "kv_gbs": kvb / (ms * 1e-3) / 1e9}
+        del graph
+    except Exception as exc:  # an extra measurement; the two above stand on their own
+        print(f"graph capture skipped: {exc}", file=sys.stderr)
+    peak, peak_kind = measured_hbm_peak()
+    return {"layers": n_layers, "windows": "128, 0, 128, 0, ...", "rows": w.rows, "heads": w.heads,
+            "kv_heads": w.kv_heads, "head_dim": w.head_dim, "kv_bytes_per_step": kvb,
+            "frac_of_hbm_peak": res["one_call"]["kv_gbs"] / peak, "peak": peak, "peak_kind": peak_kind,
+            "l2": "inputs larger than L2" if large else "L2 flushed (512 MB write) between timed steps",
+            **res}
+
+
+def replace_window(w, window):
+    from dataclasses import replace
+    return replace(w, window=window)
+
+
 def other_configs(args, world, rank, local):
     """Every other workload of the step, measured in this process; keyed by name."""
     from paged_gqa_decode_step_gb300 import binding as b
@@ -448,6 +523,9 @@ def other_configs(args, world, rank, local):
         if name == args.workload:
             continue
         res[name] = measure_decode_config(args, b, wl.WORKLOADS[name], dev, world, rank)
+        torch.cuda.empty_cache()
+    for n_layers in (2, 24):
+        res[f"gptoss20b_layers{n_layers}"] = measure_layers(args, b, wl.GPTOSS_FULL, n_layers, dev, world, rank)
         torch.cuda.empty_cache()
     for w in wl.PREFILL_WORKLOADS.values():
         res[w.name] = run_prefill(args, w, world, rank, local, light=True)

@@ -156,6 +156,61 @@ pdattn_status pdattn_decode_fused(const pdattn_params* p, const void* q, const v
                                   void* workspace, size_t workspace_bytes, pdattn_stream stream);
 
 /*
+ * One layer of a multi-layer decode call: that layer's inputs, cache and
+ * output (device pointers, layouts as in pdattn_decode_fused), its window
+ * (<= 0: attend [0, pos]) and its attention sinks (NULL or [heads] of T).
+ */
+typedef struct {
+    const void* q;          /* [rows, heads, head_dim] */
+    const void* k_new;      /* [rows, kv_heads, head_dim] */
+    const void* v_new;      /* [rows, kv_heads, head_dim] */
+    void* k_pool;           /* [num_pages, kv_heads, 64, head_dim] of this layer */
+    void* v_pool;
+    void* out;              /* [rows, heads, head_dim] */
+    int32_t window;
+    int32_t reserved;       /* must be 0 */
+    const void* sinks;
+} pdattn_layer;
+
+/* Layers that one launch pair of pdattn_decode_layers serves. */
+#define PDATTN_LAYERS_PER_LAUNCH 32
+
+/*
+ * Bytes of workspace pdattn_decode_layers needs for n_layers layers of these
+ * parameters (0 if they are invalid); it covers
+ * min(n_layers, PDATTN_LAYERS_PER_LAUNCH) layers' rows.
+ */
+size_t pdattn_layers_workspace_size(const pdattn_params* p, int32_t n_layers);
+
+/*
+ * The decode step of several layers at once.  The blocks of the model pages
+ * repeat one decoder layer `Layers` times (llama-3.1-8b-instruct page; the
+ * gpt-oss-20b page alternates a sliding-window and a full layer in each
+ * `LayerPair`), every layer with its own cache under the same page table and
+ * positions.  For each layer l the result is that of pdattn_decode_fused
+ * with p and layers[l] (its pointers, window and sinks; p->window and
+ * p->sinks are not read): rope and cache write at positions[r] through
+ * table[r], then attention over that layer's pool.  All layers of up to
+ * PDATTN_LAYERS_PER_LAUNCH share two launches: one prep launch rotates and
+ * writes every layer's rows and plans their work items together, and one
+ * persistent attention launch runs every layer's items, largest first, so
+ * short (sliding-window) layers fill in beside long ones.  More layers run
+ * as successive launch pairs on the same workspace.  `layers` is a HOST
+ * array of n_layers descriptors, read during the call only.  The layers'
+ * pools must not overlap one another.  A layer's q, k_new, v_new or out may
+ * not alias another layer's.  n_layers == 0 or p->rows == 0 is a no-op.
+ * Device errors are reported by pdattn_check_status(workspace).  This is a
+ * batching of independent layers: each layer's q must be known when the call
+ * is made, so it serves callers that hold several layers' queries at once
+ * (several models or requests sharing a step, or layers whose inputs do not
+ * depend on one another), not the layer-after-layer dependency of one
+ * forward pass.
+ */
+pdattn_status pdattn_decode_layers(const pdattn_params* p, int32_t n_layers, const pdattn_layer* layers,
+                                   const int32_t* positions, const int32_t* table, void* workspace,
+                                   size_t workspace_bytes, pdattn_stream stream);
+
+/*
  * pdattn_decode_fused without a workspace, for callers that cannot allocate
  * device memory (an allocator that is frozen once serving starts, a plugin
  * inside a program that owns all device memory, a C caller with no CUDA

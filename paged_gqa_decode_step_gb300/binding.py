@@ -36,6 +36,17 @@ class Params(ctypes.Structure):
     ]
 
 
+class Layer(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+        ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("out", ctypes.c_void_p),
+        ("window", ctypes.c_int32), ("reserved", ctypes.c_int32), ("sinks", ctypes.c_void_p),
+    ]
+
+
+LAYERS_PER_LAUNCH = 32
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with "
@@ -51,6 +62,8 @@ def _load():
         "pdattn_decode": (i32, [P, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "pdattn_decode_fused": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
         "pdattn_decode_fused_noalloc": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
+        "pdattn_layers_workspace_size": (sz, [P, i32]),
+        "pdattn_decode_layers": (i32, [P, i32, ctypes.POINTER(Layer), vp, vp, vp, sz, vp]),
         "pdattn_prefill_workspace_size": (sz, [P, i32]),
         "pdattn_prefill_paged": (i32, [P, i32] + [vp] * 11 + [sz, vp]),
         "pdattn_prefill_attend": (i32, [P, i32] + [vp] * 6 + [sz, vp]),
@@ -202,6 +215,43 @@ def decode_fused_noalloc(p, q, k_new, v_new, positions, table, k_pool, v_pool, o
     _check_q(p, q=q, k_new=k_new, v_new=v_new, out=out)
     _check(lib.pdattn_decode_fused_noalloc(ctypes.byref(p), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions),
                                            _ptr(table), _ptr(k_pool), _ptr(v_pool), _ptr(out), _stream(stream)))
+
+
+def layers_workspace_size(p, n_layers):
+    n = lib.pdattn_layers_workspace_size(ctypes.byref(p), n_layers)
+    if n == 0:
+        raise PdattnError(EINVAL, lib.pdattn_last_error().decode() or "invalid parameters")
+    return n
+
+
+def new_layers_workspace(p, n_layers, device="cuda"):
+    return torch.zeros(layers_workspace_size(p, n_layers), dtype=torch.uint8, device=device)
+
+
+def decode_layers(p, layers, positions, table, ws, stream=None):
+    """The decode step of several layers in one launch pair (per 32 layers).
+    layers: a sequence of dicts with q, k_new, v_new, k_pool, v_pool, out
+    (tensors shaped as for decode_fused) and optional window (int) and sinks
+    ([heads] tensor); p.window and p.sinks are not read."""
+    _expect("positions", positions, (p.rows,), torch.int32)
+    _expect("table", table, (p.rows, p.pages_per_row), torch.int32)
+    arr = (Layer * max(1, len(layers)))()
+    keep = []
+    pool = (p.num_pages, p.kv_heads, 64, p.head_dim)
+    for i, y in enumerate(layers):
+        _check_q(p, q=y["q"], k_new=y["k_new"], v_new=y["v_new"], out=y["out"])
+        _expect("k_pool", y["k_pool"], pool, _dt(p))
+        _expect("v_pool", y["v_pool"], pool, _dt(p))
+        sinks = y.get("sinks")
+        if sinks is not None:
+            _expect("sinks", sinks, (p.heads,), _dt(p))
+        arr[i] = Layer(y["q"].data_ptr(), y["k_new"].data_ptr(), y["v_new"].data_ptr(), y["k_pool"].data_ptr(),
+                       y["v_pool"].data_ptr(), y["out"].data_ptr(), int(y.get("window", 0)), 0,
+                       None if sinks is None else sinks.data_ptr())
+        keep.append(y)
+    w, n = _ws(ws)
+    _check(lib.pdattn_decode_layers(ctypes.byref(p), len(layers), arr, _ptr(positions), _ptr(table), w, n,
+                                    _stream(stream)))
 
 
 def prefill_workspace_size(p, n_tokens):

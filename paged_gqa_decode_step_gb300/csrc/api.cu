@@ -343,6 +343,111 @@ pdattn_status pdattn_decode_fused(const pdattn_params* p, const void* q, const v
     return s;
 }
 
+// Rows of one multi-layer launch: layers x rows, within the plan's int ranges.
+static pdattn_status layers_rows(const pdattn_params* p, int32_t n_layers, int* v_rows) {
+    const int lg = n_layers < kMaxLayers ? n_layers : kMaxLayers;
+    const long long v = (long long)lg * p->rows;
+    if (v * p->kv_heads * (long long)p->pages_per_row >= (1ll << 31) || v * p->heads >= (1ll << 31))
+        return fail(PDATTN_EUNSUPPORTED, "layers x rows too large for one launch");
+    *v_rows = (int)v;
+    return PDATTN_OK;
+}
+
+static pdattn_params with_rows(const pdattn_params* p, int rows) {
+    pdattn_params q = *p;
+    q.rows = rows;
+    return q;
+}
+
+size_t pdattn_layers_workspace_size(const pdattn_params* p, int32_t n_layers) {
+    if (check_params(p) != PDATTN_OK || n_layers < 0) return 0;
+    int v = 0;
+    if (layers_rows(p, n_layers > 0 ? n_layers : 1, &v) != PDATTN_OK) return 0;
+    const int grid = sm_count();
+    if (grid <= 0) return 0;
+    const pdattn_params pv = with_rows(p, v);
+    return layout_for(&pv, grid).total;
+}
+
+pdattn_status pdattn_decode_layers(const pdattn_params* p, int32_t n_layers, const pdattn_layer* layers,
+                                   const int32_t* positions, const int32_t* table, void* workspace,
+                                   size_t workspace_bytes, pdattn_stream stream) {
+    g_launches = 0;
+    pdattn_status s = check_params(p);
+    if (s != PDATTN_OK) return s;
+    if (n_layers < 0) return fail(PDATTN_EINVAL, "n_layers < 0");
+    if (n_layers == 0 || p->rows == 0) return PDATTN_OK;
+    if (!layers) return fail(PDATTN_EINVAL, "layers is NULL");
+    if (!positions || !table) return fail(PDATTN_EINVAL, "NULL positions or table");
+    for (int l = 0; l < n_layers; ++l) {
+        const pdattn_layer& y = layers[l];
+        if (!y.q || !y.k_new || !y.v_new || !y.k_pool || !y.v_pool || !y.out)
+            return fail(PDATTN_EINVAL, "layer %d: NULL data pointer", l);
+        if (!aligned16(y.q) || !aligned16(y.k_new) || !aligned16(y.v_new) || !aligned16(y.k_pool) ||
+            !aligned16(y.v_pool) || !aligned16(y.out))
+            return fail(PDATTN_EINVAL, "layer %d: q, k_new, v_new, the pools and out must be 16-byte aligned", l);
+        if (y.reserved != 0) return fail(PDATTN_EINVAL, "layer %d: reserved field must be 0", l);
+    }
+    int v_max = 0;
+    s = layers_rows(p, n_layers, &v_max);
+    if (s != PDATTN_OK) return s;
+    const int grid = sm_count();
+    if (grid <= 0) return fail(PDATTN_ECUDA, "no CUDA device");
+    const pdattn_params pmax = with_rows(p, v_max);
+    WsLayout Lmax;
+    s = check_ws(&pmax, workspace, workspace_bytes, grid, &Lmax);
+    if (s != PDATTN_OK) return s;
+    char* ws = static_cast<char*>(workspace);
+    int launches = 0;
+    for (int l0 = 0; l0 < n_layers; l0 += kMaxLayers) {
+        const int lg = n_layers - l0 < kMaxLayers ? n_layers - l0 : kMaxLayers;
+        const pdattn_params pv = with_rows(p, lg * p->rows);
+        const WsLayout L = layout_for(&pv, grid);
+        PrepArgs a = prep_args(&pv, positions, table, ws, L, grid);
+        a.layer_rows = p->rows;
+        a.q_out = ws + L.q_rot;
+        a.rope_blocks = pv.rows;
+        a.do_plan = 1;
+        PrepLayers pl = {};
+        AttendLayers al = {};
+        for (int j = 0; j < lg; ++j) {
+            const pdattn_layer& y = layers[l0 + j];
+            pl.q[j] = y.q;
+            pl.k_new[j] = y.k_new;
+            pl.v_new[j] = y.v_new;
+            pl.k_pool[j] = y.k_pool;
+            pl.v_pool[j] = y.v_pool;
+            pl.window[j] = y.window;
+            if ((s = make_pool_map(&al.k[j], y.k_pool, p)) != PDATTN_OK) return s;
+            if ((s = make_pool_map(&al.v[j], y.v_pool, p)) != PDATTN_OK) return s;
+            al.out[j] = y.out;
+            al.sinks[j] = y.sinks;
+        }
+        cudaError_t e = launch_prep_layers(a, pl, p->dtype, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "multi-layer rope/write/plan launch");
+        AttendArgs aa = {};
+        aa.rows = pv.rows;
+        aa.heads = p->heads;
+        aa.kv_heads = p->kv_heads;
+        aa.group = p->heads / p->kv_heads;
+        aa.head_dim = p->head_dim;
+        aa.pages_per_row = p->pages_per_row;
+        aa.num_pages = p->num_pages;
+        aa.layer_rows = p->rows;
+        aa.n_layers = lg;
+        aa.scale_log2 = scale_log2(p);
+        aa.q = ws + L.q_rot;
+        aa.table = table;
+        aa.ws = ws;
+        aa.L = L;
+        e = launch_attend_layers(aa, al, p->dtype, grid, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "multi-layer attention launch");
+        launches += 2;
+    }
+    g_launches = launches;
+    return PDATTN_OK;
+}
+
 size_t pdattn_prefill_workspace_size(const pdattn_params* p, int32_t n_tokens) {
     if (check_params(p) != PDATTN_OK || n_tokens < 0) return 0;
     return pf_layout(n_tokens, p->heads, p->head_dim, elem_bytes(p)).total;

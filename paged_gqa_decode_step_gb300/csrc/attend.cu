@@ -29,6 +29,8 @@
 //     all partials of the (row, kv head) and writes the output.
 // Every mbarrier wait is bounded; a wait that runs out records
 // kErrTimeout in the status word and the kernel winds down.
+#include <type_traits>
+
 #include "internal.h"
 
 namespace pdattn {
@@ -443,11 +445,14 @@ struct Consumer<float, D, G> {
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <typename T, int D, int G>
+template <typename T, int D, int G, typename Lay>
 __global__ void __launch_bounds__(kThreads, 1)
 attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
-              const __grid_constant__ AttendArgs a) {
+              const __grid_constant__ AttendArgs a, const __grid_constant__ Lay lay) {
     using C = Cfg<T, D>;
+    // Multi-layer launch: item row v is row v % layer_rows of layer
+    // v / layer_rows, whose pools, output and sinks come from `lay`.
+    constexpr bool kMulti = std::is_same<Lay, AttendLayers>::value;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -490,7 +495,12 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     for (int i = threadIdx.x; i < S * C::kQBytes / 16; i += kThreads)
         reinterpret_cast<uint4*>(smem + C::kOffQ)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_shared();
-    if (warp == kProducerWarp && lane == 0) {
+    if constexpr (kMulti) {
+        if (warp == kProducerWarp && lane < a.n_layers) {
+            prefetch_tensormap(&lay.k[lane]);
+            prefetch_tensormap(&lay.v[lane]);
+        }
+    } else if (warp == kProducerWarp && lane == 0) {
         prefetch_tensormap(&k_map);
         prefetch_tensormap(&v_map);
     }
@@ -570,7 +580,8 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                        pos < a.pages_per_row * kPageSize && first + npg - 1 <= pos / kPageSize &&
                        first >= lo / kPageSize;
                 if (good) {
-                    const int* trow = a.table + (size_t)row * a.pages_per_row + first;
+                    const int trow_i = kMulti ? row % a.layer_rows : row;
+                    const int* trow = a.table + (size_t)trow_i * a.pages_per_row + first;
                     if (lane < npg) pid0 = __ldg(trow + lane);
                     if (lane + 32 < npg) pid1 = __ldg(trow + lane + 32);
                 } else if (lane == 0) {
@@ -638,6 +649,13 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                 const int first_page = d1.x, pos = d1.z, lo = d1.w;
                 const int y_kv = kvh * kPageSize;
                 const T* qsrc = static_cast<const T*>(a.q) + ((size_t)row * a.heads + kvh * g) * D;
+                const CUtensorMap* km = &k_map;
+                const CUtensorMap* vm = &v_map;
+                if constexpr (kMulti) {
+                    const int l = row / a.layer_rows;
+                    km = &lay.k[l];
+                    vm = &lay.v[l];
+                }
                 constexpr int P = C::kPagesPerStage;
                 for (int j = 0; j < npg; j += P) {
                     const int np = min(P, npg - j);
@@ -676,8 +694,8 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                             const int y = pidv[p] * Hk * kPageSize + y_kv;
                             #pragma unroll
                             for (int bx = 0; bx < C::kBoxes; ++bx) {
-                                tma_load_2d(dst + p * C::kTileBytes + bx * C::kBoxBytes, &k_map, bx * C::kBoxCols, y, fb);
-                                tma_load_2d(dst + (P + p) * C::kTileBytes + bx * C::kBoxBytes, &v_map, bx * C::kBoxCols, y,
+                                tma_load_2d(dst + p * C::kTileBytes + bx * C::kBoxBytes, km, bx * C::kBoxCols, y, fb);
+                                tma_load_2d(dst + (P + p) * C::kTileBytes + bx * C::kBoxBytes, vm, bx * C::kBoxCols, y,
                                             fb);
                             }
                         }
@@ -732,11 +750,17 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             const float* eo = reinterpret_cast<const float*>(ep + sizeof(Meta) + kMaxGroup * 8);
             const int row = mt.row, kvh = mt.kvh, nch = mt.nch, slot = mt.slot;
             T* out_base = static_cast<T*>(a.out) + ((size_t)row * a.heads + kvh * g) * D;
-            const bool has_sink = a.sinks != nullptr;
+            const void* sinks = a.sinks;
+            if constexpr (kMulti) {
+                const int l = row / a.layer_rows;
+                out_base = static_cast<T*>(lay.out[l]) + ((size_t)(row - l * a.layer_rows) * a.heads + kvh * g) * D;
+                sinks = lay.sinks[l];
+            }
+            const bool has_sink = sinks != nullptr;
             if (nch == 1) {
                 for (int u = lane; u < g * D / 8; u += 32) {
                     const int j = u / (D / 8), d0 = (u % (D / 8)) * 8;
-                    const float sk = has_sink ? load_f32<T>(a.sinks, kvh * g + j) * 1.4426950408889634f : 0.f;
+                    const float sk = has_sink ? load_f32<T>(sinks, kvh * g + j) * 1.4426950408889634f : 0.f;
                     const float inv = out_scale(eml[j].x, eml[j].y, has_sink, sk);
                     float O[8];
                     #pragma unroll
@@ -783,7 +807,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                             O[0] += f * p0.x; O[1] += f * p0.y; O[2] += f * p0.z; O[3] += f * p0.w;
                             O[4] += f * p1.x; O[5] += f * p1.y; O[6] += f * p1.z; O[7] += f * p1.w;
                         }
-                        const float sk = has_sink ? load_f32<T>(a.sinks, kvh * g + j) * 1.4426950408889634f : 0.f;
+                        const float sk = has_sink ? load_f32<T>(sinks, kvh * g + j) * 1.4426950408889634f : 0.f;
                         const float inv = out_scale(M, L, has_sink, sk);
                         #pragma unroll
                         for (int e = 0; e < 8; ++e) O[e] *= inv;
@@ -898,11 +922,11 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
 // ---------------------------------------------------------------------------
 // Host launcher
 // ---------------------------------------------------------------------------
-template <typename T, int D, int G>
+template <typename T, int D, int G, typename Lay = NoLayers>
 static cudaError_t launch_one(const AttendArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
-                              int grid, bool programmatic, cudaStream_t stream) {
+                              int grid, bool programmatic, cudaStream_t stream, const Lay& lay = Lay{}) {
     using C = Cfg<T, D>;
-    auto kern = attend_kernel<T, D, G>;
+    auto kern = attend_kernel<T, D, G, Lay>;
     // The shared-memory opt-in is per function and device; setting it again is cheap.
     static int configured_mask = 0;   // bit per device id < 31
     int dev = 0;
@@ -923,7 +947,7 @@ static cudaError_t launch_one(const AttendArgs& a, const CUtensorMap& k_map, con
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = programmatic ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, k_map, v_map, a);
+    return cudaLaunchKernelEx(&cfg, kern, k_map, v_map, a, lay);
 }
 
 template <int D>
@@ -943,6 +967,26 @@ cudaError_t launch_attend(const AttendArgs& a, const CUtensorMap& k_map, const C
         return launch_one<__nv_bfloat16, 64, kMaxGroup>(a, k_map, v_map, grid, programmatic, stream);
     if (dtype == 1 && a.head_dim == 128) return launch_f32<128>(a, k_map, v_map, grid, programmatic, stream);
     if (dtype == 1 && a.head_dim == 64) return launch_f32<64>(a, k_map, v_map, grid, programmatic, stream);
+    return cudaErrorInvalidValue;
+}
+
+// Multi-layer launches: bf16 at head dim 64 / 128 (groups up to 8 on one
+// instance) and f32 with one-head groups (plain multi-head attention) or any
+// group up to 8.  Always a programmatic dependent of the prep launch.
+cudaError_t launch_attend_layers(const AttendArgs& a, const AttendLayers& lay, int dtype, int grid,
+                                 cudaStream_t stream) {
+    const CUtensorMap& k0 = lay.k[0];
+    const CUtensorMap& v0 = lay.v[0];
+    if (dtype == 0 && a.head_dim == 128)
+        return launch_one<__nv_bfloat16, 128, kMaxGroup, AttendLayers>(a, k0, v0, grid, true, stream, lay);
+    if (dtype == 0 && a.head_dim == 64)
+        return launch_one<__nv_bfloat16, 64, kMaxGroup, AttendLayers>(a, k0, v0, grid, true, stream, lay);
+    if (dtype == 1 && a.head_dim == 128)
+        return a.group <= 1 ? launch_one<float, 128, 1, AttendLayers>(a, k0, v0, grid, true, stream, lay)
+                            : launch_one<float, 128, 8, AttendLayers>(a, k0, v0, grid, true, stream, lay);
+    if (dtype == 1 && a.head_dim == 64)
+        return a.group <= 1 ? launch_one<float, 64, 1, AttendLayers>(a, k0, v0, grid, true, stream, lay)
+                            : launch_one<float, 64, 8, AttendLayers>(a, k0, v0, grid, true, stream, lay);
     return cudaErrorInvalidValue;
 }
 

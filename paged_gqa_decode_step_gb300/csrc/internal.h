@@ -5,8 +5,36 @@
 
 namespace pdattn {
 
+// Layers one multi-layer decode launch serves (its per-layer pointers and
+// tensor maps travel as kernel parameters).
+constexpr int kMaxLayers = 32;
+
+// Parameter block of the single-layer launches: nothing per layer.
+struct NoLayers {};
+
+// Per-layer inputs of a multi-layer prep launch.  Row v of the launch is row
+// v % layer_rows of layer v / layer_rows.
+struct PrepLayers {
+    const void* q[kMaxLayers];
+    const void* k_new[kMaxLayers];
+    const void* v_new[kMaxLayers];
+    void* k_pool[kMaxLayers];
+    void* v_pool[kMaxLayers];
+    int window[kMaxLayers];
+};
+
+// Per-layer pools (as TMA maps), outputs and sinks of a multi-layer
+// attention launch.
+struct AttendLayers {
+    CUtensorMap k[kMaxLayers];
+    CUtensorMap v[kMaxLayers];
+    void* out[kMaxLayers];
+    const void* sinks[kMaxLayers];
+};
+
 struct PrepArgs {
     int rows, heads, kv_heads, head_dim, pages_per_row, num_pages, window, rope_len;
+    int layer_rows;         // multi-layer launches: rows per layer (rows = layers x layer_rows)
     const void* q;
     const void* k_new;
     const void* v_new;
@@ -27,6 +55,7 @@ struct PrepArgs {
 
 struct AttendArgs {
     int rows, heads, kv_heads, group, head_dim, pages_per_row, num_pages;
+    int layer_rows, n_layers;   // multi-layer launches: rows per layer, layers
     float scale_log2;       // score scale times log2(e)
     const void* q;          // rotated queries [rows, heads, D]
     const int* table;
@@ -68,9 +97,14 @@ struct PrefillArgs {
 cudaError_t launch_rope_tables(float theta, int D, int S, int dtype, void* cos_out, void* sin_out,
                                cudaStream_t stream);
 cudaError_t launch_prep(const PrepArgs& a, int dtype, cudaStream_t stream);
+// Multi-layer prep: rope + write of every layer's rows, one plan over all.
+cudaError_t launch_prep_layers(const PrepArgs& a, const PrepLayers& lay, int dtype, cudaStream_t stream);
 // Sets the kernel's shared-memory limit (once per device) and launches.
 cudaError_t launch_attend(const AttendArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
                           int dtype, int grid, bool programmatic, cudaStream_t stream);
+// Multi-layer attention: one persistent launch over every layer's items.
+cudaError_t launch_attend_layers(const AttendArgs& a, const AttendLayers& lay, int dtype, int grid,
+                                 cudaStream_t stream);
 size_t attend_smem_bytes(int dtype, int head_dim);
 // The tile list (one block), then the rope + write of every token at its
 // slot (programmatic launch that ends after the tile list): two launches.

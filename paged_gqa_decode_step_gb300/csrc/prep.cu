@@ -5,6 +5,7 @@
 // `write_at` of k and v) for the write, with the paged slot of the
 // llama-3.1-8b-instruct architecture page (`decode_paged`, PageSize = 64).
 #include <climits>
+#include <type_traits>
 
 #include "internal.h"
 
@@ -167,25 +168,52 @@ __device__ __forceinline__ T* pool_slot(void* pool, int page, int Hk, int off, i
     return static_cast<T*>(pool) + (((size_t)page * Hk) * kPageSize + off) * D;
 }
 
-template <typename T>
-__device__ void rope_write_row(const PrepArgs& a, int row) {
+// Launch row v: row v of the call, or in a multi-layer launch row
+// v % layer_rows of layer v / layer_rows (the table and the positions are
+// shared by every layer).
+template <typename Lay>
+__device__ __forceinline__ int table_row(const PrepArgs& a, int v) {
+    if constexpr (std::is_same<Lay, PrepLayers>::value) return v % a.layer_rows;
+    else return v;
+}
+
+template <typename Lay>
+__device__ __forceinline__ int row_window(const PrepArgs& a, const Lay& lay, int v) {
+    if constexpr (std::is_same<Lay, PrepLayers>::value) return lay.window[v / a.layer_rows];
+    else return a.window;
+}
+
+template <typename T, typename Lay>
+__device__ void rope_write_row(const PrepArgs& a, const Lay& lay, int row) {
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(a.ws + a.L.ctrl);
     const int D = a.head_dim, Hq = a.heads, Hk = a.kv_heads;
-    const int pos = __ldg(a.positions + row);
+    const void *q = a.q, *k_new = a.k_new, *v_new = a.v_new;
+    void *k_pool = a.k_pool, *v_pool = a.v_pool;
+    int r = row;
+    if constexpr (std::is_same<Lay, PrepLayers>::value) {
+        const int l = row / a.layer_rows;
+        r = row - l * a.layer_rows;
+        q = lay.q[l];
+        k_new = lay.k_new[l];
+        v_new = lay.v_new[l];
+        k_pool = lay.k_pool[l];
+        v_pool = lay.v_pool[l];
+    }
+    const int pos = __ldg(a.positions + r);
     const bool rope = a.rope_cos != nullptr;
     if (pos < 0 || pos >= a.pages_per_row * kPageSize || (rope && pos >= a.rope_len)) {
         if (threadIdx.x == 0) set_error(ctrl, kErrBadPos);
         return;
     }
-    const int page = __ldg(a.table + (size_t)row * a.pages_per_row + pos / kPageSize);
+    const int page = __ldg(a.table + (size_t)r * a.pages_per_row + pos / kPageSize);
     const bool page_ok = page >= 0 && page < a.num_pages;
     if (!page_ok && threadIdx.x == 0) set_error(ctrl, kErrBadPage);
     const int off = pos % kPageSize, pg = page_ok ? page : 0;
-    rope_write_vectors<T>(static_cast<const T*>(a.q) + (size_t)row * Hq * D,
+    rope_write_vectors<T>(static_cast<const T*>(q) + (size_t)r * Hq * D,
                           static_cast<T*>(a.q_out) + (size_t)row * Hq * D,
-                          static_cast<const T*>(a.k_new) + (size_t)row * Hk * D,
-                          static_cast<const T*>(a.v_new) + (size_t)row * Hk * D, pool_slot<T>(a.k_pool, pg, Hk, off, D),
-                          pool_slot<T>(a.v_pool, pg, Hk, off, D), (size_t)kPageSize * D,
+                          static_cast<const T*>(k_new) + (size_t)r * Hk * D,
+                          static_cast<const T*>(v_new) + (size_t)r * Hk * D, pool_slot<T>(k_pool, pg, Hk, off, D),
+                          pool_slot<T>(v_pool, pg, Hk, off, D), (size_t)kPageSize * D,
                           rope ? static_cast<const T*>(a.rope_cos) + (size_t)pos * D : nullptr,
                           rope ? static_cast<const T*>(a.rope_sin) + (size_t)pos * D : nullptr, Hq, Hk, D, page_ok);
 }
@@ -225,7 +253,8 @@ __device__ __forceinline__ int choose_chunk(unsigned long long row_pages, int ma
 // One row per thread (rows <= block size): every value stays in registers or
 // shared memory after the positions are read once, so the plan costs one
 // global round trip plus its stores.
-__device__ bool build_plan_small(const PrepArgs& a) {
+template <typename Lay>
+__device__ bool build_plan_small(const PrepArgs& a, const Lay& lay) {
     __shared__ int4 s_row[512];
     __shared__ int2 s_at2[512];
     __shared__ int s_cnt[kChunkMax + 1];
@@ -242,10 +271,10 @@ __device__ bool build_plan_small(const PrepArgs& a) {
     int* merge_cnt = reinterpret_cast<int*>(a.ws + a.L.merge_cnt);
 
     const bool mine = tid < R;
-    const int pos = mine ? __ldg(a.positions + tid) : -1;
+    const int pos = mine ? __ldg(a.positions + table_row<Lay>(a, tid)) : -1;
     const bool ok = mine && pos >= 0 && pos < max_pos;
     if (mine && !ok) set_error(ctrl, kErrBadPos);
-    const int lo = ok ? row_lo(pos, a.window) : 0;
+    const int lo = ok ? row_lo(pos, row_window(a, lay, tid)) : 0;
     const int first = lo / kPageSize;
     const int n = ok ? pos / kPageSize - first + 1 : 0;
     for (int i = tid; i <= kChunkMax; i += blockDim.x) s_cnt[i] = 0;
@@ -327,8 +356,9 @@ __device__ bool build_plan_small(const PrepArgs& a) {
     return true;
 }
 
-__device__ void build_plan(const PrepArgs& a) {
-    if (build_plan_small(a)) return;
+template <typename Lay>
+__device__ void build_plan(const PrepArgs& a, const Lay& lay) {
+    if (build_plan_small(a, lay)) return;
     __shared__ int2 s_at[kPlanRowsCap];
     __shared__ int s_cnt[kChunkMax + 1];
     __shared__ int s_cur[kChunkMax + 1];
@@ -349,9 +379,9 @@ __device__ void build_plan(const PrepArgs& a) {
     unsigned long long w = 0;
     int longest = 0;
     for (int r = tid; r < R; r += blockDim.x) {
-        const int pos = __ldg(a.positions + r);
+        const int pos = __ldg(a.positions + table_row<Lay>(a, r));
         if (pos >= 0 && pos < max_pos) {
-            const int n = pos / kPageSize - row_lo(pos, a.window) / kPageSize + 1;
+            const int n = pos / kPageSize - row_lo(pos, row_window(a, lay, r)) / kPageSize + 1;
             w += n;
             longest = max(longest, n);
         }
@@ -371,10 +401,10 @@ __device__ void build_plan(const PrepArgs& a) {
     const int C = s_chunk;
 
     for (int r = tid; r < R; r += blockDim.x) {
-        const int pos = __ldg(a.positions + r);
+        const int pos = __ldg(a.positions + table_row<Lay>(a, r));
         const bool ok = pos >= 0 && pos < max_pos;
         if (!ok) set_error(ctrl, kErrBadPos);
-        const int lo = ok ? row_lo(pos, a.window) : 0;
+        const int lo = ok ? row_lo(pos, row_window(a, lay, r)) : 0;
         const int n = ok ? pos / kPageSize - lo / kPageSize + 1 : 0;
         const int nch = (n + C - 1) / C;
         if (n / C) atomicAdd(&s_cnt[C], (n / C) * Hk);
@@ -452,16 +482,17 @@ __device__ void build_plan(const PrepArgs& a) {
     }
 }
 
-template <typename T>
-__global__ void __launch_bounds__(512) prep_kernel(const __grid_constant__ PrepArgs a) {
+template <typename T, typename Lay>
+__global__ void __launch_bounds__(512) prep_kernel(const __grid_constant__ PrepArgs a,
+                                                  const __grid_constant__ Lay lay) {
     // Let the attention kernel that follows start its prologue now; it waits
     // for this grid's completion before it reads anything written here.
     griddep_launch_dependents();
     if (a.do_plan && blockIdx.x == gridDim.x - 1) {
-        build_plan(a);
+        build_plan(a, lay);
         return;
     }
-    rope_write_row<T>(a, blockIdx.x);
+    rope_write_row<T>(a, lay, blockIdx.x);
 }
 
 // ---------------------------------------------------------------------------
@@ -935,9 +966,19 @@ cudaError_t launch_prep(const PrepArgs& a, int dtype, cudaStream_t stream) {
     const int blocks = a.rope_blocks + (a.do_plan ? 1 : 0);
     if (blocks == 0) return cudaSuccess;
     if (dtype == 0)
-        prep_kernel<__nv_bfloat16><<<blocks, 512, 0, stream>>>(a);
+        prep_kernel<__nv_bfloat16, NoLayers><<<blocks, 512, 0, stream>>>(a, NoLayers{});
     else
-        prep_kernel<float><<<blocks, 512, 0, stream>>>(a);
+        prep_kernel<float, NoLayers><<<blocks, 512, 0, stream>>>(a, NoLayers{});
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prep_layers(const PrepArgs& a, const PrepLayers& lay, int dtype, cudaStream_t stream) {
+    const int blocks = a.rope_blocks + (a.do_plan ? 1 : 0);
+    if (blocks == 0) return cudaSuccess;
+    if (dtype == 0)
+        prep_kernel<__nv_bfloat16, PrepLayers><<<blocks, 512, 0, stream>>>(a, lay);
+    else
+        prep_kernel<float, PrepLayers><<<blocks, 512, 0, stream>>>(a, lay);
     return cudaGetLastError();
 }
 

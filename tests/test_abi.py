@@ -7,8 +7,10 @@ import ctypes
 import os
 import re
 import subprocess
+import tempfile
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "pdattn.h")
@@ -177,3 +179,46 @@ def test_packed_host_validation(lib):
     n = lib.lib.pdattn_packed_workspace_size(ctypes.byref(p), 1000)
     # control, two tile lists, rotated q and k, padded ids and positions, block summaries
     assert n >= 256 + 2 * 32 * 1000 + 2 * 1000 * (8 + 2) * 64 + 2 * 4 * 1024 + 16 * 16 and n % 256 == 0
+
+
+def test_layer_struct_layout_matches_header(lib):
+    src = r"""
+#include <stddef.h>
+#include <stdio.h>
+#include "pdattn.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %d\n", sizeof(pdattn_layer), offsetof(pdattn_layer, out),
+         offsetof(pdattn_layer, window), offsetof(pdattn_layer, sinks), PDATTN_LAYERS_PER_LAUNCH);
+  return 0;
+}
+"""
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "l.c")
+        exe = os.path.join(d, "l")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
+        got = [int(x) for x in subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()]
+    L = lib.Layer
+    assert got == [ctypes.sizeof(L), L.out.offset, L.window.offset, L.sinks.offset, lib.LAYERS_PER_LAUNCH]
+
+
+def test_decode_layers_host_validation(lib):
+    p = lib.make_params(4, 32, 8, 128, 8, 40, torch.bfloat16)
+    null = ctypes.c_void_p(0)
+    f = lib.lib.pdattn_decode_layers
+    # zero layers: a no-op; NULL layer array or pointers: rejected before any launch
+    assert f(ctypes.byref(p), 0, None, null, null, null, 0, null) == lib.OK
+    assert lib.last_launch_count() == 0
+    assert f(ctypes.byref(p), 2, None, null, null, null, 0, null) == lib.EINVAL
+    arr = (lib.Layer * 2)()
+    assert f(ctypes.byref(p), 2, arr, ctypes.c_void_p(256), ctypes.c_void_p(256), null, 0, null) == lib.EINVAL
+    assert b"layer 0" in lib.lib.pdattn_last_error()
+    assert f(ctypes.byref(p), -1, arr, null, null, null, 0, null) == lib.EINVAL
+    assert lib.last_launch_count() == 0
+    assert lib.lib.pdattn_layers_workspace_size(ctypes.byref(p), -1) == 0
+    if torch.cuda.is_available():
+        # the workspace covers up to one launch's layers
+        n1 = lib.lib.pdattn_layers_workspace_size(ctypes.byref(p), 1)
+        n32 = lib.lib.pdattn_layers_workspace_size(ctypes.byref(p), 32)
+        n64 = lib.lib.pdattn_layers_workspace_size(ctypes.byref(p), 64)
+        assert 0 < n1 < n32 == n64
