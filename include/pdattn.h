@@ -146,8 +146,9 @@ pdattn_status pdattn_decode(const pdattn_params* p, const void* q_rot, const int
                             pdattn_stream stream);
 
 /*
- * The whole step: RoPE and cache write (rotated q kept in the workspace)
- * with the plan in the same launch, then attention.  Equivalent to
+ * The whole step: the split plan, RoPE and cache write (rotated q kept in
+ * the workspace), then attention; three launches, each a programmatic
+ * dependent of the one before, with no host synchronisation.  Equivalent to
  * pdattn_rope_write_kv + pdattn_decode.
  */
 pdattn_status pdattn_decode_fused(const pdattn_params* p, const void* q, const void* k_new,
@@ -172,7 +173,7 @@ typedef struct {
     const void* sinks;
 } pdattn_layer;
 
-/* Layers that one launch pair of pdattn_decode_layers serves. */
+/* Layers that one group of launches of pdattn_decode_layers serves. */
 #define PDATTN_LAYERS_PER_LAUNCH 32
 
 /*
@@ -190,12 +191,13 @@ size_t pdattn_layers_workspace_size(const pdattn_params* p, int32_t n_layers);
  * positions.  For each layer l the result is that of pdattn_decode_fused
  * with p and layers[l] (its pointers, window and sinks; p->window and
  * p->sinks are not read): rope and cache write at positions[r] through
- * table[r], then attention over that layer's pool.  All layers of up to
- * PDATTN_LAYERS_PER_LAUNCH share two launches: one prep launch rotates and
- * writes every layer's rows and plans their work items together, and one
- * persistent attention launch runs every layer's items, largest first, so
- * short (sliding-window) layers fill in beside long ones.  More layers run
- * as successive launch pairs on the same workspace.  `layers` is a HOST
+ * table[r], then attention over that layer's pool.  Up to
+ * PDATTN_LAYERS_PER_LAUNCH layers share three launches: one planner lists
+ * every layer's work items together, one launch rotates and writes every
+ * layer's rows, and one persistent attention launch runs every layer's
+ * items, largest first, so short (sliding-window) layers fill in beside long
+ * ones.  More layers run as successive groups of launches on the same
+ * workspace.  `layers` is a HOST
  * array of n_layers descriptors, read during the call only.  The layers'
  * pools must not overlap one another.  A layer's q, k_new, v_new or out may
  * not alias another layer's.  n_layers == 0 or p->rows == 0 is a no-op.

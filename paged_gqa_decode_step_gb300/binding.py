@@ -229,7 +229,7 @@ def new_layers_workspace(p, n_layers, device="cuda"):
 
 
 def decode_layers(p, layers, positions, table, ws, stream=None):
-    """The decode step of several layers in one launch pair (per 32 layers).
+    """The decode step of several layers in one group of launches (per 32 layers).
     layers: a sequence of dicts with q, k_new, v_new, k_pool, v_pool, out
     (tensors shaped as for decode_fused) and optional window (int) and sinks
     ([heads] tensor); p.window and p.sinks are not read."""

@@ -231,9 +231,10 @@ pdattn_status pdattn_rope_write_kv(const pdattn_params* p, const void* q, const 
     a.v_pool = v_pool;
     a.rope_blocks = p->rows;
     a.do_plan = 0;
-    cudaError_t e = launch_prep(a, p->dtype, (cudaStream_t)stream);
+    int n = 0;
+    cudaError_t e = launch_prep(a, p->dtype, (cudaStream_t)stream, &n);
     if (e != cudaSuccess) return cuda_fail(e, "rope/write launch");
-    g_launches = 1;
+    g_launches = n;
     return PDATTN_OK;
 }
 
@@ -252,9 +253,10 @@ pdattn_status pdattn_plan(const pdattn_params* p, const int32_t* positions, void
     PrepArgs a = prep_args(p, positions, nullptr, static_cast<char*>(workspace), L, grid);
     a.rope_blocks = 0;
     a.do_plan = 1;
-    cudaError_t e = launch_prep(a, p->dtype, (cudaStream_t)stream);
+    int n = 0;
+    cudaError_t e = launch_prep(a, p->dtype, (cudaStream_t)stream, &n);
     if (e != cudaSuccess) return cuda_fail(e, "plan launch");
-    g_launches = 1;
+    g_launches = n;
     return PDATTN_OK;
 }
 
@@ -301,11 +303,12 @@ pdattn_status pdattn_decode(const pdattn_params* p, const void* q_rot, const int
     PrepArgs a = prep_args(p, positions, table, static_cast<char*>(workspace), L, grid);
     a.rope_blocks = 0;
     a.do_plan = 1;
-    cudaError_t e = launch_prep(a, p->dtype, (cudaStream_t)stream);
+    int n = 0;
+    cudaError_t e = launch_prep(a, p->dtype, (cudaStream_t)stream, &n);
     if (e != cudaSuccess) return cuda_fail(e, "plan launch");
     s = attend_impl(p, q_rot, table, k_pool, v_pool, out, static_cast<char*>(workspace), L, grid, true,
                     (cudaStream_t)stream);
-    if (s == PDATTN_OK) g_launches = 2;
+    if (s == PDATTN_OK) g_launches = n + 1;
     return s;
 }
 
@@ -336,10 +339,11 @@ pdattn_status pdattn_decode_fused(const pdattn_params* p, const void* q, const v
     a.v_pool = v_pool;
     a.rope_blocks = p->rows;
     a.do_plan = 1;
-    cudaError_t e = launch_prep(a, p->dtype, (cudaStream_t)stream);
-    if (e != cudaSuccess) return cuda_fail(e, "rope/write/plan launch");
+    int n = 0;
+    cudaError_t e = launch_prep(a, p->dtype, (cudaStream_t)stream, &n);
+    if (e != cudaSuccess) return cuda_fail(e, "plan + rope/write launches");
     s = attend_impl(p, q_rot, table, k_pool, v_pool, out, ws, L, grid, true, (cudaStream_t)stream);
-    if (s == PDATTN_OK) g_launches = 2;
+    if (s == PDATTN_OK) g_launches = n + 1;
     return s;
 }
 
@@ -423,8 +427,10 @@ pdattn_status pdattn_decode_layers(const pdattn_params* p, int32_t n_layers, con
             al.out[j] = y.out;
             al.sinks[j] = y.sinks;
         }
-        cudaError_t e = launch_prep_layers(a, pl, p->dtype, (cudaStream_t)stream);
-        if (e != cudaSuccess) return cuda_fail(e, "multi-layer rope/write/plan launch");
+        int n = 0;
+        cudaError_t e = launch_prep_layers(a, pl, p->dtype, (cudaStream_t)stream, &n);
+        if (e != cudaSuccess) return cuda_fail(e, "multi-layer plan + rope/write launches");
+        launches += n;
         AttendArgs aa = {};
         aa.rows = pv.rows;
         aa.heads = p->heads;
@@ -442,7 +448,7 @@ pdattn_status pdattn_decode_layers(const pdattn_params* p, int32_t n_layers, con
         aa.L = L;
         e = launch_attend_layers(aa, al, p->dtype, grid, (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, "multi-layer attention launch");
-        launches += 2;
+        launches += 1;
     }
     g_launches = launches;
     return PDATTN_OK;

@@ -42,8 +42,9 @@ constexpr int kEpilogueWarp = kConsumerWarps + 2;
 constexpr int kThreads = (kConsumerWarps + 3) * 32;
 constexpr int kItemSlots = 4;           // items the scheduler may hold ahead of the producer
 constexpr int kBacklogBytes = 256 << 10;  // K/V bytes queued ahead of the TMA issue point
-constexpr int kEpiSlots = 2;            // finished items waiting for the epilogue warp
+constexpr int kEpiSlots = 4;            // finished items waiting for the epilogue warp
 constexpr float kNegBig = -1.0e30f;     // running-max start: finite, so exp2(m - m) = 1
+constexpr size_t kTablePrefetchMax = size_t(8) << 20;   // larger page tables are not prefetched
 
 enum : int { kFirst = 1, kLast = 2, kTerm = 8 };
 
@@ -57,6 +58,12 @@ struct Meta {
 constexpr int kPagesShift = 8;
 constexpr int kValidShift = 16;
 
+// Bytes from one query head to the next in a stage's query-group buffer:
+// bf16 rows are padded by 16 bytes so that the eight row addresses of each
+// ldmatrix fall in different banks; f32 rows stay packed.
+template <typename T, int D>
+__host__ __device__ constexpr int q_row_bytes() { return sizeof(T) == 2 ? D * 2 + 16 : D * (int)sizeof(T); }
+
 template <typename T, int D>
 struct Cfg {
     static constexpr int kElem = sizeof(T);
@@ -69,7 +76,8 @@ struct Cfg {
     static constexpr int kPagesPerStage = (kTileBytes == kBoxBytes && kElem == 2) ? 2 : 1;
     static constexpr int kStageBytes = 2 * kPagesPerStage * kTileBytes;   // K pages, then V pages
     static constexpr int kStages = (kStageBytes <= 16384) ? 10 : (kStageBytes <= 32768 ? 5 : 2);
-    static constexpr int kQBytes = kMaxGroup * D * kElem;
+    static constexpr int kQRow = q_row_bytes<T, D>();
+    static constexpr int kQBytes = kMaxGroup * kQRow;
     static constexpr int kORow = D + 4;                          // padded row of the merge buffer
     static constexpr int kMergeFloats = 2 * kConsumerWarps * kMaxGroup + kConsumerWarps * kMaxGroup * kORow;
     static constexpr int kOffQ = kStages * kStageBytes;
@@ -166,7 +174,7 @@ struct Consumer<__nv_bfloat16, D, G> {
         #pragma unroll
         for (int p = 0; p < KS / 2; ++p) {
             const int head = lane & 7, chunk = 4 * p + (lane >> 3);
-            ldsm_x4(qbuf + head * D * 2 + chunk * 16, qf[2 * p][0], qf[2 * p][1], qf[2 * p + 1][0],
+            ldsm_x4(qbuf + head * q_row_bytes<__nv_bfloat16, D>() + chunk * 16, qf[2 * p][0], qf[2 * p][1], qf[2 * p + 1][0],
                     qf[2 * p + 1][1]);
         }
         #pragma unroll
@@ -504,6 +512,17 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         prefetch_tensormap(&k_map);
         prefetch_tensormap(&v_map);
     }
+    if (warp == kSchedulerWarp) {
+        // The page table is an input of the call (no launch of this call
+        // writes it): pull it into L2 while the preceding launch finishes, so
+        // that the page-id reads after the wait below hit L2.
+        const size_t tbytes = (size_t)(kMulti ? a.layer_rows : a.rows) * a.pages_per_row * sizeof(int);
+        if (tbytes <= kTablePrefetchMax) {
+            const char* tb = reinterpret_cast<const char*>(a.table);
+            for (size_t off = ((size_t)blockIdx.x * 32 + lane) * 128; off < tbytes; off += (size_t)gridDim.x * 32 * 128)
+                prefetch_l2(tb + off);
+        }
+    }
     __syncthreads();
 
     // Everything below reads what the preceding launch wrote.
@@ -524,16 +543,21 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         first_d0 = __ldcg(reinterpret_cast<const int4*>(items + blockIdx.x));
         first_d1 = __ldcg(reinterpret_cast<const int4*>(items + blockIdx.x) + 1);
     }
-    const uint32_t magic = __ldcg(&ctrl->magic);
-    const int n_items = __ldcg(&ctrl->n_items);
-    const int chunk_pages = __ldcg(&ctrl->chunk_pages);
-    if (magic != kPlanMagic || __ldcg(&ctrl->rows) != a.rows || __ldcg(&ctrl->kv_heads) != Hk ||
-        __ldcg(&ctrl->pages_per_row) != a.pages_per_row || __ldcg(&ctrl->max_items) != a.L.max_items ||
-        __ldcg(&ctrl->group) != g || __ldcg(&ctrl->head_dim) != D || chunk_pages < 1 ||
-        chunk_pages > kChunkMax || n_items > a.L.max_items || __ldcg(&ctrl->grid) != (int)gridDim.x) {
+    // The plan header in one round trip: four independent 16-byte loads
+    // (fields status .. test_hold; see Ctrl), checked in registers.
+    const int4 h0 = __ldcg(reinterpret_cast<const int4*>(ctrl));
+    const int4 h1 = __ldcg(reinterpret_cast<const int4*>(ctrl) + 1);
+    const int4 h2 = __ldcg(reinterpret_cast<const int4*>(ctrl) + 2);
+    const int4 h3 = __ldcg(reinterpret_cast<const int4*>(ctrl) + 3);
+    const int n_items = h0.w, chunk_pages = h1.x;
+    const bool plan_ok = (uint32_t)h1.y == kPlanMagic && h1.z == a.rows && h1.w == Hk && h2.x == a.pages_per_row &&
+                         h2.y == a.L.max_items && h2.z == g && h2.w == D && h3.x == (int)gridDim.x &&
+                         chunk_pages >= 1 && chunk_pages <= kChunkMax && n_items <= a.L.max_items;
+    if (!plan_ok) {
         if (threadIdx.x == 0) set_error(ctrl, kErrBadPlan);
         return;
     }
+    const int test_hold = h3.y;
 
     if (warp == kSchedulerWarp) {
         // ================= scheduler =================
@@ -636,7 +660,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             uint32_t armed_par = 0;             // parity armed on stage s
             int issued = 0;
             bool ok = true;
-            bool hold = blockIdx.x == 0 && __ldcg(&ctrl->test_hold) != 0;
+            bool hold = blockIdx.x == 0 && test_hold != 0;
             while (ok) {
                 if (!mbar_wait(bar_ifull + 8 * islot, iphase)) { ok = false; break; }
                 const uint8_t* slotp = item_q + islot * C::kItemBytes;
@@ -700,7 +724,14 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                             }
                         }
                     }
-                    if (j == 0) bulk_load(sbase + C::kOffQ + stage * C::kQBytes, qsrc, g * D * C::kElem, fb);
+                    if (j == 0) {
+                        const uint32_t qdst = sbase + C::kOffQ + stage * C::kQBytes;
+                        if constexpr (C::kQRow == D * C::kElem) {
+                            bulk_load(qdst, qsrc, g * D * C::kElem, fb);
+                        } else {
+                            for (int h = 0; h < g; ++h) bulk_load(qdst + h * C::kQRow, qsrc + h * D, D * C::kElem, fb);
+                        }
+                    }
                     armed |= 1u << stage;
                     armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
                     issued += np;
@@ -778,15 +809,14 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                 __syncwarp();
                 int last = 0;
                 if (lane == 0) {
-                    __threadfence();
-                    const int done = atomicAdd(merge_cnt + (size_t)row * Hk + kvh, 1);
+                    // Release this chunk's partial and, for the last chunk to
+                    // arrive, acquire every other chunk's (one acq_rel atomic).
+                    const int done = atomic_add_acq_rel_gpu(merge_cnt + (size_t)row * Hk + kvh, 1);
                     last = done == nch - 1;
-                    if (last) {
-                        merge_cnt[(size_t)row * Hk + kvh] = 0;
-                        __threadfence();
-                    }
+                    if (last) merge_cnt[(size_t)row * Hk + kvh] = 0;   // ready for the next launch
                 }
                 last = __shfl_sync(0xffffffffu, last, 0);
+                __syncwarp();
                 if (last) {
                     // out = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c over the chunks
                     const int slot0 = slot - mt.chunk;

@@ -214,6 +214,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
     }
 }
 
+// Fetch the 128-byte line holding `p` into L2 (a hint: no data returns).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
@@ -301,6 +306,16 @@ __device__ __forceinline__ uint32_t swz128(uint32_t box, int row, int chunk) {
 }
 
 __device__ __forceinline__ void set_error(Ctrl* ctrl, int bits) { atomicOr(&ctrl->status, bits); }
+
+// atomicAdd with acquire-release semantics at GPU scope: the caller's earlier
+// writes (and those ordered before them in its warp) are visible to whoever
+// acquires the new value, and writes released before the value it reads are
+// visible to the caller.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
 
 // A bounded wait ran out: record it and withdraw the plan, whose cursor and
 // merge counters are now stale, so that a later attention-only call on this

@@ -46,7 +46,7 @@ struct PrepArgs {
     void* k_pool;
     void* v_pool;
     int rope_blocks;        // rows to rotate and write (0: none)
-    int do_plan;            // 1: the last block builds the split plan
+    int do_plan;            // 1: a planner launch builds the split plan first
     int grid_attend;        // persistent CTAs of the attention launch
     int chunk_pages;        // 0: planner's choice
     char* ws;
@@ -96,9 +96,13 @@ struct PrefillArgs {
 
 cudaError_t launch_rope_tables(float theta, int D, int S, int dtype, void* cos_out, void* sin_out,
                                cudaStream_t stream);
-cudaError_t launch_prep(const PrepArgs& a, int dtype, cudaStream_t stream);
+// The split planner (one block, if a.do_plan), then the rope + cache write of
+// a.rope_blocks rows (a programmatic dependent of the planner); *launches
+// gets the number of launches made.
+cudaError_t launch_prep(const PrepArgs& a, int dtype, cudaStream_t stream, int* launches);
 // Multi-layer prep: rope + write of every layer's rows, one plan over all.
-cudaError_t launch_prep_layers(const PrepArgs& a, const PrepLayers& lay, int dtype, cudaStream_t stream);
+cudaError_t launch_prep_layers(const PrepArgs& a, const PrepLayers& lay, int dtype, cudaStream_t stream,
+                               int* launches);
 // Sets the kernel's shared-memory limit (once per device) and launches.
 cudaError_t launch_attend(const AttendArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
                           int dtype, int grid, bool programmatic, cudaStream_t stream);

@@ -250,6 +250,17 @@ __device__ __forceinline__ int choose_chunk(unsigned long long row_pages, int ma
     return (int)(cc < 1 ? 1 : (cc > kChunkMax ? kChunkMax : cc));
 }
 
+// A row of n visible pages in nch = ceil(n / C) chunks of equal size, up to
+// one page apart: the first `big` chunks hold q + 1 pages, the others q (so
+// no row ends in a short tail chunk whose merge would come last).
+struct Chunking {
+    int nch, q, big;
+    __device__ Chunking(int n, int C) : nch((n + C - 1) / C), q(n > 0 ? n / ((n + C - 1) / C) : 0),
+                                        big(n > 0 ? n % ((n + C - 1) / C) : 0) {}
+    __device__ int size(int c) const { return c < big ? q + 1 : q; }
+    __device__ int start(int c) const { return c * q + (c < big ? c : big); }   // pages after the row's first
+};
+
 // One row per thread (rows <= block size): every value stays in registers or
 // shared memory after the positions are read once, so the plan costs one
 // global round trip plus its stores.
@@ -298,12 +309,13 @@ __device__ bool build_plan_small(const PrepArgs& a, const Lay& lay) {
     }
     __syncthreads();
     const int C = s_chunk;
-    const int nch = (n + C - 1) / C, full = n / C, tail = n % C;
+    const Chunking ch(n, C);
+    const int nch = ch.nch;
     int base = 0;
     if (ok) {
-        if (full) atomicAdd(&s_cnt[C], full * Hk);
-        if (tail) atomicAdd(&s_cnt[tail], Hk);
-        base = nch ? atomicAdd(&s_slots, nch * Hk) : 0;
+        if (ch.big) atomicAdd(&s_cnt[ch.q + 1], ch.big * Hk);
+        atomicAdd(&s_cnt[ch.q], (nch - ch.big) * Hk);
+        base = atomicAdd(&s_slots, nch * Hk);
     }
     if (mine) row_info[tid] = make_int4(ok ? pos : -1, lo, nch, base);
     __syncthreads();
@@ -316,13 +328,13 @@ __device__ bool build_plan_small(const PrepArgs& a, const Lay& lay) {
     const int n_items = s_cnt[0];
     const bool fits = n_items <= a.L.max_items;
     if (mine) {
-        int at_full = 0, at_tail = 0;
+        int at_big = 0, at_small = 0;
         if (ok && fits) {
-            at_full = full ? atomicAdd(&s_cur[C], full * Hk) : 0;
-            at_tail = tail ? atomicAdd(&s_cur[tail], Hk) : 0;
+            at_big = ch.big ? atomicAdd(&s_cur[ch.q + 1], ch.big * Hk) : 0;
+            at_small = atomicAdd(&s_cur[ch.q], (nch - ch.big) * Hk);
         }
         s_row[tid] = make_int4(ok ? pos : -1, lo, nch, base);
-        s_at2[tid] = make_int2(at_full, at_tail);
+        s_at2[tid] = make_int2(at_big, at_small);
     }
     __syncthreads();
     for (int pr = tid; pr < R * Hk; pr += blockDim.x) {
@@ -331,11 +343,11 @@ __device__ bool build_plan_small(const PrepArgs& a, const Lay& lay) {
         const int4 ri = s_row[r];
         if (!fits || ri.x < 0) continue;
         const int2 at = s_at2[r];
-        const int rf = ri.y / kPageSize, rn = ri.x / kPageSize - rf + 1;
-        const int rfull = rn / C, rtail = rn % C;
+        const int rf = ri.y / kPageSize;
+        const Chunking rc(ri.x / kPageSize - rf + 1, C);
         for (int c = 0; c < ri.z; ++c)
-            write_item(items, c < rfull ? at.x + c * Hk + h : at.y + h, r, h, c, ri.z, ri.w, rf + c * C,
-                       c < rfull ? C : rtail, ri.x, ri.y);
+            write_item(items, c < rc.big ? at.x + c * Hk + h : at.y + (c - rc.big) * Hk + h, r, h, c, ri.z, ri.w,
+                       rf + rc.start(c), rc.size(c), ri.x, ri.y);
     }
     __syncthreads();
     if (tid == 0) {
@@ -406,11 +418,11 @@ __device__ void build_plan(const PrepArgs& a, const Lay& lay) {
         if (!ok) set_error(ctrl, kErrBadPos);
         const int lo = ok ? row_lo(pos, row_window(a, lay, r)) : 0;
         const int n = ok ? pos / kPageSize - lo / kPageSize + 1 : 0;
-        const int nch = (n + C - 1) / C;
-        if (n / C) atomicAdd(&s_cnt[C], (n / C) * Hk);
-        if (n % C) atomicAdd(&s_cnt[n % C], Hk);
-        const int base = nch ? atomicAdd(&s_slots, nch * Hk) : 0;
-        row_info[r] = make_int4(ok ? pos : -1, lo, nch, base);
+        const Chunking ch(n, C);
+        if (ch.big) atomicAdd(&s_cnt[ch.q + 1], ch.big * Hk);
+        if (n) atomicAdd(&s_cnt[ch.q], (ch.nch - ch.big) * Hk);
+        const int base = ch.nch ? atomicAdd(&s_slots, ch.nch * Hk) : 0;
+        row_info[r] = make_int4(ok ? pos : -1, lo, ch.nch, base);
     }
     __syncthreads();
     if (tid == 0) {
@@ -428,21 +440,20 @@ __device__ void build_plan(const PrepArgs& a, const Lay& lay) {
         for (int r = tid; r < R; r += blockDim.x) {
             const int4 ri = row_info[r];
             const int pos = ri.x, lo = ri.y, nch = ri.z, base = ri.w;
-            int at_full = 0, at_tail = 0;
+            int at_big = 0, at_small = 0;
             if (pos >= 0) {
                 const int first = lo / kPageSize;
-                const int n = pos / kPageSize - first + 1;
-                const int full = n / C, tail = n % C;
-                at_full = full ? atomicAdd(&s_cur[C], full * Hk) : 0;
-                at_tail = tail ? atomicAdd(&s_cur[tail], Hk) : 0;
+                const Chunking ch(pos / kPageSize - first + 1, C);
+                at_big = ch.big ? atomicAdd(&s_cur[ch.q + 1], ch.big * Hk) : 0;
+                at_small = atomicAdd(&s_cur[ch.q], (nch - ch.big) * Hk);
                 if (r >= kPlanRowsCap) {
                     for (int c = 0; c < nch; ++c)
                         for (int h = 0; h < Hk; ++h)
-                            write_item(items, c < full ? at_full + c * Hk + h : at_tail + h, r, h, c, nch, base,
-                                       first + c * C, c < full ? C : tail, pos, lo);
+                            write_item(items, c < ch.big ? at_big + c * Hk + h : at_small + (c - ch.big) * Hk + h, r,
+                                       h, c, nch, base, first + ch.start(c), ch.size(c), pos, lo);
                 }
             }
-            if (r < kPlanRowsCap) s_at[r] = make_int2(at_full, at_tail);
+            if (r < kPlanRowsCap) s_at[r] = make_int2(at_big, at_small);
         }
         __syncthreads();
         const int Rc = R < kPlanRowsCap ? R : kPlanRowsCap;
@@ -454,12 +465,11 @@ __device__ void build_plan(const PrepArgs& a, const Lay& lay) {
             const int pos = ri.x, lo = ri.y, nch = ri.z, base = ri.w;
             if (pos < 0) continue;
             const int first = lo / kPageSize;
-            const int n = pos / kPageSize - first + 1;
-            const int full = n / C, tail = n % C;
+            const Chunking ch(pos / kPageSize - first + 1, C);
             const int2 at = s_at[r];
             for (int c = 0; c < nch; ++c)
-                write_item(items, c < full ? at.x + c * Hk + h : at.y + h, r, h, c, nch, base, first + c * C,
-                           c < full ? C : tail, pos, lo);
+                write_item(items, c < ch.big ? at.x + c * Hk + h : at.y + (c - ch.big) * Hk + h, r, h, c, nch, base,
+                           first + ch.start(c), ch.size(c), pos, lo);
         }
     } else {
         for (long long pr = tid; pr < (long long)R * Hk; pr += blockDim.x) merge_cnt[pr] = 0;
@@ -482,17 +492,29 @@ __device__ void build_plan(const PrepArgs& a, const Lay& lay) {
     }
 }
 
-template <typename T, typename Lay>
-__global__ void __launch_bounds__(512) prep_kernel(const __grid_constant__ PrepArgs a,
+// The split planner: one block.  It lets the launch that follows start at
+// once (the rope and cache-write blocks do not read the plan).
+template <typename Lay>
+__global__ void __launch_bounds__(512) plan_kernel(const __grid_constant__ PrepArgs a,
                                                   const __grid_constant__ Lay lay) {
-    // Let the attention kernel that follows start its prologue now; it waits
-    // for this grid's completion before it reads anything written here.
     griddep_launch_dependents();
-    if (a.do_plan && blockIdx.x == gridDim.x - 1) {
-        build_plan(a, lay);
-        return;
-    }
+    build_plan(a, lay);
+}
+
+// RoPE and cache write: one block per row, no shared memory, so that the
+// attention launch that follows (programmatic, one CTA per SM with most of
+// the SM's shared memory) can start its prologue beside these blocks.  When
+// a planner launch precedes this one (do_plan), the last block exits only
+// after the planner has finished: the attention launch waits for this grid
+// alone, and that wait then covers the plan as well.
+constexpr int kRopeRowThreads = 256;
+
+template <typename T, typename Lay>
+__global__ void __launch_bounds__(kRopeRowThreads) rope_write_kernel(const __grid_constant__ PrepArgs a,
+                                                                     const __grid_constant__ Lay lay) {
+    griddep_launch_dependents();
     rope_write_row<T>(a, lay, blockIdx.x);
+    if (a.do_plan && blockIdx.x == gridDim.x - 1) griddep_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -962,24 +984,41 @@ cudaError_t launch_rope_tables(float theta, int D, int S, int dtype, void* cos_o
     return cudaGetLastError();
 }
 
-cudaError_t launch_prep(const PrepArgs& a, int dtype, cudaStream_t stream) {
-    const int blocks = a.rope_blocks + (a.do_plan ? 1 : 0);
-    if (blocks == 0) return cudaSuccess;
-    if (dtype == 0)
-        prep_kernel<__nv_bfloat16, NoLayers><<<blocks, 512, 0, stream>>>(a, NoLayers{});
-    else
-        prep_kernel<float, NoLayers><<<blocks, 512, 0, stream>>>(a, NoLayers{});
-    return cudaGetLastError();
+// The planner (if a.do_plan) as an ordinary launch, then the rope + write
+// blocks (if any) as its programmatic dependent.
+template <typename Lay>
+static cudaError_t launch_prep_any(const PrepArgs& a, const Lay& lay, int dtype, cudaStream_t stream,
+                                   int* launches) {
+    *launches = 0;
+    if (a.do_plan) {
+        plan_kernel<Lay><<<1, 512, 0, stream>>>(a, lay);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        ++*launches;
+    }
+    if (a.rope_blocks == 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.rope_blocks);
+    cfg.blockDim = dim3(kRopeRowThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.do_plan ? 1 : 0;
+    cudaError_t e = dtype == 0 ? cudaLaunchKernelEx(&cfg, rope_write_kernel<__nv_bfloat16, Lay>, a, lay)
+                               : cudaLaunchKernelEx(&cfg, rope_write_kernel<float, Lay>, a, lay);
+    if (e == cudaSuccess) ++*launches;
+    return e;
 }
 
-cudaError_t launch_prep_layers(const PrepArgs& a, const PrepLayers& lay, int dtype, cudaStream_t stream) {
-    const int blocks = a.rope_blocks + (a.do_plan ? 1 : 0);
-    if (blocks == 0) return cudaSuccess;
-    if (dtype == 0)
-        prep_kernel<__nv_bfloat16, PrepLayers><<<blocks, 512, 0, stream>>>(a, lay);
-    else
-        prep_kernel<float, PrepLayers><<<blocks, 512, 0, stream>>>(a, lay);
-    return cudaGetLastError();
+cudaError_t launch_prep(const PrepArgs& a, int dtype, cudaStream_t stream, int* launches) {
+    return launch_prep_any(a, NoLayers{}, dtype, stream, launches);
+}
+
+cudaError_t launch_prep_layers(const PrepArgs& a, const PrepLayers& lay, int dtype, cudaStream_t stream,
+                               int* launches) {
+    return launch_prep_any(a, lay, dtype, stream, launches);
 }
 
 cudaError_t launch_prefill_prep(const PrefillPrepArgs& a, int dtype, cudaStream_t stream) {

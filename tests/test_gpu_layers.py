@@ -1,4 +1,4 @@
-"""Several layers' decode steps in one launch pair (pdattn_decode_layers)
+"""Several layers' decode steps in one group of launches (pdattn_decode_layers)
 against the oracle run layer by layer.
 
 Every layer has its own q, new k and v, pools, window and sinks; positions
@@ -83,7 +83,7 @@ def run_layers(w, n_layers, windows, sink_heads=None, seed=0, repeat=1):
     for _ in range(repeat):
         b.decode_layers(p, d_layers, positions, table, ws)
         b.check_status(ws)
-        assert b.last_launch_count() == 2 * ((n_layers + b.LAYERS_PER_LAUNCH - 1) // b.LAYERS_PER_LAUNCH)
+        assert b.last_launch_count() == 3 * ((n_layers + b.LAYERS_PER_LAUNCH - 1) // b.LAYERS_PER_LAUNCH)
     for l, (d, (out64, kp, vp)) in enumerate(zip(d_layers, want)):
         assert_close(d["out"], out64, w.dtype, f"layer {l}")
         assert np.array_equal(wl.to_numpy(d["k_pool"]).view(np.uint8), kp.view(np.uint8)), f"layer {l} k pool"
@@ -104,7 +104,7 @@ def test_twelve_layers_alternating_called_twice():
 
 
 def test_more_layers_than_one_launch_serves():
-    # 35 layers: a launch pair of 32, then one of 3, on the same workspace
+    # 35 layers: a group of launches for 32, then one for 3, on the same workspace
     w = wl.Workload("many", rows=3, heads=32, kv_heads=8, head_dim=128, pages_per_row=4, dtype="bf16",
                     rope_theta=500000.0, positions="fixed", fixed_positions=(0, 130, 255), seed=52)
     run_layers(w, 35, windows=(0, 64), seed=3)
