@@ -151,7 +151,7 @@ float scale_log2(const pdattn_params* p) {
     return (float)(s * 1.4426950408889634);
 }
 
-pdattn_status attend_impl(const pdattn_params* p, const void* q_rot, const int32_t* table,
+pdattn_status attend_impl(const pdattn_params* p, const void* q_rot, const int32_t* positions, const int32_t* table,
                           const void* k_pool, const void* v_pool, void* out, char* ws,
                           const WsLayout& L, int grid, bool programmatic, cudaStream_t stream) {
     CUtensorMap km, vm;
@@ -167,8 +167,11 @@ pdattn_status attend_impl(const pdattn_params* p, const void* q_rot, const int32
     a.head_dim = p->head_dim;
     a.pages_per_row = p->pages_per_row;
     a.num_pages = p->num_pages;
+    a.window = p->window;
+    a.chunk_pages = p->chunk_pages;
     a.scale_log2 = scale_log2(p);
     a.q = q_rot;
+    a.positions = positions;
     a.table = table;
     a.sinks = p->sinks;
     a.out = out;
@@ -282,7 +285,7 @@ pdattn_status pdattn_attend(const pdattn_params* p, const void* q_rot, const int
     WsLayout L;
     s = check_ws(p, workspace, workspace_bytes, grid, &L);
     if (s != PDATTN_OK) return s;
-    return attend_impl(p, q_rot, table, k_pool, v_pool, out, static_cast<char*>(workspace), L, grid, false,
+    return attend_impl(p, q_rot, positions, table, k_pool, v_pool, out, static_cast<char*>(workspace), L, grid, false,
                        (cudaStream_t)stream);
 }
 
@@ -306,7 +309,7 @@ pdattn_status pdattn_decode(const pdattn_params* p, const void* q_rot, const int
     int n = 0;
     cudaError_t e = launch_prep(a, p->dtype, (cudaStream_t)stream, &n);
     if (e != cudaSuccess) return cuda_fail(e, "plan launch");
-    s = attend_impl(p, q_rot, table, k_pool, v_pool, out, static_cast<char*>(workspace), L, grid, true,
+    s = attend_impl(p, q_rot, positions, table, k_pool, v_pool, out, static_cast<char*>(workspace), L, grid, true,
                     (cudaStream_t)stream);
     if (s == PDATTN_OK) g_launches = n + 1;
     return s;
@@ -342,7 +345,7 @@ pdattn_status pdattn_decode_fused(const pdattn_params* p, const void* q, const v
     int n = 0;
     cudaError_t e = launch_prep(a, p->dtype, (cudaStream_t)stream, &n);
     if (e != cudaSuccess) return cuda_fail(e, "plan + rope/write launches");
-    s = attend_impl(p, q_rot, table, k_pool, v_pool, out, ws, L, grid, true, (cudaStream_t)stream);
+    s = attend_impl(p, q_rot, positions, table, k_pool, v_pool, out, ws, L, grid, true, (cudaStream_t)stream);
     if (s == PDATTN_OK) g_launches = n + 1;
     return s;
 }
@@ -426,6 +429,7 @@ pdattn_status pdattn_decode_layers(const pdattn_params* p, int32_t n_layers, con
             if ((s = make_pool_map(&al.v[j], y.v_pool, p)) != PDATTN_OK) return s;
             al.out[j] = y.out;
             al.sinks[j] = y.sinks;
+            al.window[j] = y.window;
         }
         int n = 0;
         cudaError_t e = launch_prep_layers(a, pl, p->dtype, (cudaStream_t)stream, &n);
@@ -441,8 +445,10 @@ pdattn_status pdattn_decode_layers(const pdattn_params* p, int32_t n_layers, con
         aa.num_pages = p->num_pages;
         aa.layer_rows = p->rows;
         aa.n_layers = lg;
+        aa.chunk_pages = p->chunk_pages;
         aa.scale_log2 = scale_log2(p);
         aa.q = ws + L.q_rot;
+        aa.positions = positions;
         aa.table = table;
         aa.ws = ws;
         aa.L = L;

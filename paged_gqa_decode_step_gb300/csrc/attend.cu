@@ -38,8 +38,9 @@ namespace pdattn {
 constexpr int kConsumerWarps = 4;
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kSchedulerWarp = kConsumerWarps + 1;
-constexpr int kEpilogueWarp = kConsumerWarps + 2;
-constexpr int kThreads = (kConsumerWarps + 3) * 32;
+constexpr int kEpilogueWarp = kConsumerWarps + 2;   // and the next warp: two epilogue warps
+constexpr int kEpilogueWarps = 2;
+constexpr int kThreads = (kConsumerWarps + 2 + kEpilogueWarps) * 32;
 constexpr int kItemSlots = 4;           // items the scheduler may hold ahead of the producer
 constexpr int kBacklogBytes = 256 << 10;  // K/V bytes queued ahead of the TMA issue point
 constexpr int kEpiSlots = 4;            // finished items waiting for the epilogue warp
@@ -97,7 +98,8 @@ struct Cfg {
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffMisc + 16 + 1024;           // + alignment slack
     // pages the scheduler keeps queued beyond the producer's issue point
-    static constexpr int kBacklogPages = kBacklogBytes / kStageBytes > 2 ? kBacklogBytes / kStageBytes : 2;
+    static constexpr int kPageBytes = 2 * kTileBytes;                 // K and V of one page
+    static constexpr int kBacklogPages = kBacklogBytes / kPageBytes > 2 ? kBacklogBytes / kPageBytes : 2;
     static_assert(kSmem <= 232448, "shared memory per CTA");
     static_assert(kOffBar % 8 == 0, "mbarrier alignment");
 };
@@ -301,7 +303,12 @@ struct Consumer<__nv_bfloat16, D, G> {
 //           the two parities are summed once per item in stash().
 // The probabilities go through a small per-warp buffer (read back as
 // broadcast float4s).  G bounds the group at compile time; a one-head group
-// keeps its query in registers.
+// keeps its query in registers.  The softmax is lazy: the running maximum is
+// raised only when a score exceeds it by more than kLazyLog2 (one vote per
+// page instead of a max reduction), so the weights stay below 2^kLazyLog2,
+// and each lane keeps its own partial denominator, summed once per item.
+constexpr float kLazyLog2 = 8.f;
+
 template <int D, int G>
 struct Consumer<float, D, G> {
     static constexpr int VD = D / 16;          // value dimensions per lane
@@ -385,19 +392,19 @@ struct Consumer<float, D, G> {
             if (j < g) {
                 float sc = acc[j] + __shfl_xor_sync(0xffffffffu, acc[j], 16);
                 sc = valid ? sc * sl2 : -INFINITY;
-                float x = sc;
-                #pragma unroll
-                for (int sh = 1; sh < 16; sh <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, sh));
-                const float n = fmaxf(m[j], x);
-                const float al = exp2_approx(m[j] - n);
-                m[j] = n;
-                const float pj = exp2_approx(sc - n);
-                float ps = pj;
-                #pragma unroll
-                for (int sh = 1; sh < 16; sh <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, sh);
-                l[j] = l[j] * al + ps;
-                #pragma unroll
-                for (int e = 0; e < VD; ++e) o[j][e] *= al;
+                if (__any_sync(0xffffffffu, sc > m[j] + kLazyLog2)) {
+                    float x = sc;
+                    #pragma unroll
+                    for (int sh = 1; sh < 16; sh <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, sh));
+                    const float n = fmaxf(m[j], x);
+                    const float al = exp2_approx(m[j] - n);
+                    m[j] = n;
+                    l[j] *= al;
+                    #pragma unroll
+                    for (int e = 0; e < VD; ++e) o[j][e] *= al;
+                }
+                const float pj = exp2_approx(sc - m[j]);
+                if (half == 0) l[j] += pj;          // this lane's token; summed over lanes in stash()
                 // token tl goes to slot parity * 8 + index within its parity
                 if (half == 0) sp[j * 16 + (tl & 1) * 8 + (tl >> 1)] = pj;
             }
@@ -436,9 +443,12 @@ struct Consumer<float, D, G> {
         #pragma unroll
         for (int j = 0; j < G; ++j) {
             if (j < g) {
+                float lt = l[j];
+                #pragma unroll
+                for (int sh = 1; sh < 32; sh <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, sh);
                 if (lane == 0) {
                     sm_m[warp * kMaxGroup + j] = m[j];
-                    sm_l[warp * kMaxGroup + j] = l[j];
+                    sm_l[warp * kMaxGroup + j] = lt;
                 }
                 #pragma unroll
                 for (int e = 0; e < VD; ++e) {
@@ -449,6 +459,52 @@ struct Consumer<float, D, G> {
         }
     }
 };
+
+// ---------------------------------------------------------------------------
+// The first-wave item of CTA b (chunk 0 of (row, kv head) pair b), derived
+// from the call's inputs exactly as the planner derives it: the positions
+// and windows give every row's visible pages, their total and maximum give
+// the split size, and the merge slot starts at the prefix sum of nch *
+// kv_heads over the rows before.  Whole warp.  Returns false for a row
+// whose position is out of range (the planner leaves an empty item there).
+// ---------------------------------------------------------------------------
+template <typename Lay>
+__device__ bool first_wave_item(const AttendArgs& a, const Lay& lay, int b, int lane, int grid, int4* d0, int4* d1) {
+    constexpr bool kMulti = std::is_same<Lay, AttendLayers>::value;
+    const int Hk = a.kv_heads, max_pos = a.pages_per_row * kPageSize;
+    auto pages_of = [&](int v, int* pos_out, int* lo_out) -> int {
+        const int pos = __ldg(a.positions + (kMulti ? v % a.layer_rows : v));
+        if (pos < 0 || pos >= max_pos) return 0;
+        int w = a.window;
+        if constexpr (kMulti) w = lay.window[v / a.layer_rows];
+        const int lo = row_lo(pos, w);
+        *pos_out = pos;
+        *lo_out = lo;
+        return pos / kPageSize - lo / kPageSize + 1;
+    };
+    int pos = 0, lo = 0;
+    unsigned long long tot = 0;
+    int longest = 0;
+    for (int v = lane; v < a.rows; v += 32) {
+        const int n = pages_of(v, &pos, &lo);
+        tot += (unsigned long long)n;
+        longest = max(longest, n);
+    }
+    #pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, sh);
+    longest = (int)__reduce_max_sync(0xffffffffu, (unsigned)longest);
+    const int C = a.chunk_pages > 0 ? a.chunk_pages : choose_chunk(tot, longest, Hk, grid);
+    const int row = b / Hk, kvh = b % Hk;
+    int part = 0;
+    for (int v = lane; v < row; v += 32) part += Chunking(pages_of(v, &pos, &lo), C).nch;
+    part = (int)__reduce_add_sync(0xffffffffu, (unsigned)part);
+    const int n = pages_of(row, &pos, &lo);
+    if (n == 0) return false;
+    const Chunking ch(n, C);
+    *d0 = make_int4(row, kvh << 16, ch.nch, part * Hk + kvh * ch.nch);
+    *d1 = make_int4(lo / kPageSize, ch.size(0), pos, lo);
+    return true;
+}
 
 // ---------------------------------------------------------------------------
 // The kernel
@@ -478,6 +534,8 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     float* sm_o = sm_l + kConsumerWarps * kMaxGroup;
     int* s_flag = reinterpret_cast<int*>(smem + C::kOffMisc);
     volatile int* s_issued = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);  // pages issued so far
+    volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);   // 1: the plan was refused
+    volatile int* s_early = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 12);  // 1: item 0 queued before the wait
     uint8_t* item_q = smem + C::kOffItems;
     uint8_t* epi_q = smem + C::kOffEpi;
 
@@ -489,6 +547,8 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         }
         mbar_init(bar_sync, kConsumerWarps * 32);
         *s_issued = 0;
+        *s_abort = 0;
+        *s_early = 0;
         for (int s = 0; s < kItemSlots; ++s) {
             mbar_init(bar_ifull + 8 * s, 1);
             mbar_init(bar_iempty + 8 * s, 1);
@@ -525,48 +585,105 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     }
     __syncthreads();
 
-    // Everything below reads what the preceding launch wrote.
-    griddep_wait();
-
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(a.ws + a.L.ctrl);
     const ItemDesc* items = reinterpret_cast<const ItemDesc*>(a.ws + a.L.items);
     int* merge_cnt = reinterpret_cast<int*>(a.ws + a.L.merge_cnt);
     float2* part_ml = reinterpret_cast<float2*>(a.ws + a.L.part_ml);
     float* part_o = reinterpret_cast<float*>(a.ws + a.L.part_o);
     const int g = a.group, Hk = a.kv_heads;
+    const int nf = first_wave(a.rows, Hk, gridDim.x);
 
-    // The scheduler's first item is this CTA's index; its descriptor load is
-    // issued before the plan header is checked (the index is inside the
-    // workspace whatever the plan says) and used only once the check passed.
-    int4 first_d0 = make_int4(0, 0, 0, 0), first_d1 = make_int4(0, 0, 0, 0);
-    if (warp == kSchedulerWarp && (int)blockIdx.x < a.L.max_items) {
-        first_d0 = __ldcg(reinterpret_cast<const int4*>(items + blockIdx.x));
-        first_d1 = __ldcg(reinterpret_cast<const int4*>(items + blockIdx.x) + 1);
-    }
     // The plan header in one round trip: four independent 16-byte loads
-    // (fields status .. test_hold; see Ctrl), checked in registers.
-    const int4 h0 = __ldcg(reinterpret_cast<const int4*>(ctrl));
-    const int4 h1 = __ldcg(reinterpret_cast<const int4*>(ctrl) + 1);
-    const int4 h2 = __ldcg(reinterpret_cast<const int4*>(ctrl) + 2);
-    const int4 h3 = __ldcg(reinterpret_cast<const int4*>(ctrl) + 3);
-    const int n_items = h0.w, chunk_pages = h1.x;
-    const bool plan_ok = (uint32_t)h1.y == kPlanMagic && h1.z == a.rows && h1.w == Hk && h2.x == a.pages_per_row &&
-                         h2.y == a.L.max_items && h2.z == g && h2.w == D && h3.x == (int)gridDim.x &&
-                         chunk_pages >= 1 && chunk_pages <= kChunkMax && n_items <= a.L.max_items;
-    if (!plan_ok) {
-        if (threadIdx.x == 0) set_error(ctrl, kErrBadPlan);
-        return;
-    }
-    const int test_hold = h3.y;
+    // (fields status .. test_hold; see Ctrl), checked in registers.  Only
+    // after the wait for the preceding launch (the planner's).
+    auto read_plan = [&](int* n_items, int* chunk_pages) -> bool {
+        const int4 h0 = __ldcg(reinterpret_cast<const int4*>(ctrl));
+        const int4 h1 = __ldcg(reinterpret_cast<const int4*>(ctrl) + 1);
+        const int4 h2 = __ldcg(reinterpret_cast<const int4*>(ctrl) + 2);
+        const int4 h3 = __ldcg(reinterpret_cast<const int4*>(ctrl) + 3);
+        *n_items = h0.w;
+        *chunk_pages = h1.x;
+        return (uint32_t)h1.y == kPlanMagic && h1.z == a.rows && h1.w == Hk && h2.x == a.pages_per_row &&
+               h2.y == a.L.max_items && h2.z == g && h2.w == D && h3.x == (int)gridDim.x && h1.x >= 1 &&
+               h1.x <= kChunkMax && h0.w <= a.L.max_items;
+    };
 
     if (warp == kSchedulerWarp) {
         // ================= scheduler =================
-        // Item slot layout: ItemDesc (npg < 0 marks the end), then 64 page ids.
+        // Item slot layout: ItemDesc (npg < 0 marks the end, 0 an empty
+        // item), then 64 page ids.
         int islot = 0;
         uint32_t iphase = 0;
         bool ok = true;
-        bool first = true;
         int queued = 0;                     // pages handed to the producer so far
+        auto queue_item = [&](int4 d0, int4 d1, int pid0, int pid1) -> bool {
+            int waited = 1;
+            if (lane == 0) waited = mbar_wait(bar_iempty + 8 * islot, iphase ^ 1) ? 1 : 0;
+            waited = __shfl_sync(0xffffffffu, waited, 0);
+            if (!waited) return false;
+            uint8_t* slotp = item_q + islot * C::kItemBytes;
+            if (lane == 0) {
+                reinterpret_cast<int4*>(slotp)[0] = d0;
+                reinterpret_cast<int4*>(slotp)[1] = d1;
+            }
+            int* pids = reinterpret_cast<int*>(slotp + sizeof(ItemDesc));
+            pids[lane] = pid0;
+            pids[lane + 32] = pid1;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_ifull + 8 * islot);
+            if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
+            return true;
+        };
+        auto load_pids = [&](int row, int first, int npg, int* pid0, int* pid1) {
+            const int trow_i = kMulti ? row % a.layer_rows : row;
+            const int* trow = a.table + (size_t)trow_i * a.pages_per_row + first;
+            *pid0 = lane < npg ? __ldg(trow + lane) : -1;
+            *pid1 = lane + 32 < npg ? __ldg(trow + lane + 32) : -1;
+        };
+        // The first-wave item comes from the call's inputs (positions, the
+        // table), which no launch of this call writes: it is queued before
+        // the wait, so that its pages load while the planner and the rope
+        // launch finish.
+        int4 sd0 = make_int4(0, 0, 0, 0), sd1 = make_int4(0, 0, 0, 0);
+        bool static_item = false;
+        if ((int)blockIdx.x < nf) {
+            static_item = first_wave_item(a, lay, (int)blockIdx.x, lane, (int)gridDim.x, &sd0, &sd1);
+            if (static_item) {
+                int pid0, pid1;
+                load_pids(sd0.x, sd1.x, sd1.y, &pid0, &pid1);
+                if (lane == 0) *s_early = 1;   // published by the item barrier's arrival
+                ok = queue_item(sd0, sd1, pid0, pid1);
+                queued += sd1.y;
+            }
+        }
+
+        // Everything below reads what the preceding launch wrote.
+        griddep_wait();
+        int4 first_d0 = make_int4(0, 0, 0, 0), first_d1 = make_int4(0, 0, 0, 0);
+        if ((int)blockIdx.x < a.L.max_items) {
+            first_d0 = __ldcg(reinterpret_cast<const int4*>(items + blockIdx.x));
+            first_d1 = __ldcg(reinterpret_cast<const int4*>(items + blockIdx.x) + 1);
+        }
+        int n_items = 0, chunk_pages = 0;
+        const bool plan_ok = read_plan(&n_items, &chunk_pages);
+        if (!plan_ok || !ok) {
+            if (lane == 0) {
+                if (!plan_ok) set_error(ctrl, kErrBadPlan);
+                else fail_timeout(ctrl);
+                *s_abort = 1;
+            }
+            // let the producer leave its item wait at once
+            queue_item(make_int4(0, 0, 0, 0), make_int4(0, -1, 0, 0), -1, -1);
+            return;
+        }
+        if (static_item) {
+            // the planner's item b must be the one derived above
+            const bool same = first_d0.x == sd0.x && first_d0.y == sd0.y && first_d0.z == sd0.z &&
+                              first_d0.w == sd0.w && first_d1.x == sd1.x && first_d1.y == sd1.y &&
+                              first_d1.z == sd1.z && first_d1.w == sd1.w && (int)blockIdx.x < n_items;
+            if (!same && lane == 0) set_error(ctrl, kErrBadPlan);
+        }
+        bool first = !static_item;
         while (true) {
             int it = (int)blockIdx.x;
             if (!first) {
@@ -597,39 +714,20 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                     d0 = __ldcg(reinterpret_cast<const int4*>(items + it));
                     d1 = __ldcg(reinterpret_cast<const int4*>(items + it) + 1);
                 }
+                if (d1.y == 0) { first = false; continue; }   // an empty first-wave item (a bad row)
                 const int row = d0.x, kvh = d0.y >> 16, chunk = d0.y & 0xffff, nch = d0.z, slot = d0.w;
                 const int first = d1.x, npg = d1.y, pos = d1.z, lo = d1.w;
                 good = row >= 0 && row < a.rows && kvh < Hk && chunk < nch && slot >= 0 && slot < n_items &&
                        npg >= 1 && npg <= chunk_pages && first >= 0 && pos >= 0 && lo >= 0 && lo <= pos &&
                        pos < a.pages_per_row * kPageSize && first + npg - 1 <= pos / kPageSize &&
                        first >= lo / kPageSize;
-                if (good) {
-                    const int trow_i = kMulti ? row % a.layer_rows : row;
-                    const int* trow = a.table + (size_t)trow_i * a.pages_per_row + first;
-                    if (lane < npg) pid0 = __ldg(trow + lane);
-                    if (lane + 32 < npg) pid1 = __ldg(trow + lane + 32);
-                } else if (lane == 0) {
-                    set_error(ctrl, kErrBadPlan);
-                }
+                if (good) load_pids(row, first, npg, &pid0, &pid1);
+                else if (lane == 0) set_error(ctrl, kErrBadPlan);
             }
             first = false;
             if (!good) continue;
-            int waited = 1;
-            if (lane == 0) waited = mbar_wait(bar_iempty + 8 * islot, iphase ^ 1) ? 1 : 0;
-            waited = __shfl_sync(0xffffffffu, waited, 0);
-            if (!waited) { ok = false; break; }
-            uint8_t* slotp = item_q + islot * C::kItemBytes;
-            if (lane == 0) {
-                if (term) d1.y = -1;
-                reinterpret_cast<int4*>(slotp)[0] = d0;
-                reinterpret_cast<int4*>(slotp)[1] = d1;
-            }
-            int* pids = reinterpret_cast<int*>(slotp + sizeof(ItemDesc));
-            pids[lane] = pid0;
-            pids[lane + 32] = pid1;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_ifull + 8 * islot);
-            if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
+            if (term) d1.y = -1;
+            if (!queue_item(d0, d1, pid0, pid1)) { ok = false; break; }
             if (term) break;
             queued += d1.y;
         }
@@ -659,9 +757,39 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             uint32_t armed = 0;                 // bit s: stage s has an unfinished arm
             uint32_t armed_par = 0;             // parity armed on stage s
             int issued = 0;
-            bool ok = true;
-            bool hold = blockIdx.x == 0 && test_hold != 0;
-            while (ok) {
+            bool ok = true, aborted = false;
+            // test hook, written (if at all) before the call
+            bool hold = blockIdx.x == 0 && __ldcg(&ctrl->test_hold) != 0;
+            // Until the wait for the preceding launch, only the first-wave
+            // item's pages are loaded: not the row's last page (this call
+            // writes a slot there) and not its rotated queries (the rope
+            // launch writes them), and no more stages than the ring holds.
+            bool dep = false;
+            bool q_pending = false;
+            uint32_t q_dst = 0, q_bar = 0;
+            const T* q_src = nullptr;
+            int pre_stages = 0;
+            bool first_item = true;
+            auto issue_q = [&](uint32_t qdst, const T* qsrc, uint32_t fb) {
+                if constexpr (C::kQRow == D * C::kElem) {
+                    bulk_load(qdst, qsrc, g * D * C::kElem, fb);
+                } else {
+                    for (int h = 0; h < g; ++h) bulk_load(qdst + h * C::kQRow, qsrc + h * D, D * C::kElem, fb);
+                }
+            };
+            auto resolve = [&]() {
+                if (dep) return;
+                griddep_wait();
+                dep = true;
+                int n_items, chunk_pages;
+                if (!read_plan(&n_items, &chunk_pages)) aborted = true;   // the scheduler reports it
+                // Issued even for a refused plan (the source lies inside the
+                // rotated queries either way), so that every armed stage
+                // completes and can be waited for before the CTA exits.
+                if (q_pending) issue_q(q_dst, q_src, q_bar);
+                q_pending = false;
+            };
+            while (ok && !aborted) {
                 if (!mbar_wait(bar_ifull + 8 * islot, iphase)) { ok = false; break; }
                 const uint8_t* slotp = item_q + islot * C::kItemBytes;
                 const int4 d0 = reinterpret_cast<const int4*>(slotp)[0];
@@ -680,13 +808,20 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                     km = &lay.k[l];
                     vm = &lay.v[l];
                 }
+                if (!(first_item && *s_early)) resolve();   // only the first-wave item starts early
+                first_item = false;
+                if (aborted) break;
                 constexpr int P = C::kPagesPerStage;
+                const int last_page = pos / kPageSize;   // holds this call's new slot
                 for (int j = 0; j < npg; j += P) {
                     const int np = min(P, npg - j);
+                    if (!dep && (pre_stages >= S || first_page + j + np - 1 >= last_page)) resolve();
+                    if (aborted) break;
                     if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1)) { ok = false; break; }
                     if (hold) {
                         // test hook: this stage is never armed nor filled
                         hold = false;
+                        if (!dep) ++pre_stages;
                         if (++stage == S) { stage = 0; phase ^= 1; }
                         continue;
                     }
@@ -726,23 +861,29 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                     }
                     if (j == 0) {
                         const uint32_t qdst = sbase + C::kOffQ + stage * C::kQBytes;
-                        if constexpr (C::kQRow == D * C::kElem) {
-                            bulk_load(qdst, qsrc, g * D * C::kElem, fb);
+                        if (dep) {
+                            issue_q(qdst, qsrc, fb);
                         } else {
-                            for (int h = 0; h < g; ++h) bulk_load(qdst + h * C::kQRow, qsrc + h * D, D * C::kElem, fb);
+                            q_pending = true;
+                            q_dst = qdst;
+                            q_src = qsrc;
+                            q_bar = fb;
                         }
                     }
+                    if (!dep) ++pre_stages;
                     armed |= 1u << stage;
                     armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
                     issued += np;
                     *s_issued = issued;
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
-                if (!ok) break;
+                if (!ok || aborted) break;
+                resolve();   // later items come after the wait
+                if (aborted) break;
                 mbar_arrive(bar_iempty + 8 * islot);
                 if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
             }
-            if (ok) {
+            if (ok && !aborted) {
                 // Terminator: the next stage carries no data, only the end flag.
                 if (mbar_wait(bar_empty + 8 * stage, phase ^ 1)) {
                     meta[stage].flags = kTerm;
@@ -751,9 +892,12 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                     ok = false;
                 }
             }
-            if (!ok) {
-                fail_timeout(ctrl);
-                // Let copies in flight land before the CTA's shared memory goes away.
+            if (!ok || aborted) {
+                if (!ok) fail_timeout(ctrl);
+                resolve();   // issues a pending query copy, so that its stage completes
+                // Let the copies in flight land before the CTA's shared memory
+                // goes away (after a refused plan the consumers have left and
+                // nothing reads them).
                 for (int s2 = 0; s2 < S; ++s2)
                     if (armed & (1u << s2)) mbar_wait(bar_full + 8 * s2, (armed_par >> s2) & 1u, 200000000ull);
             }
@@ -762,12 +906,24 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         return;
     }
 
-    if (warp == kEpilogueWarp) {
+    // Consumers and epilogue: everything below reads what the preceding
+    // launch wrote.
+    griddep_wait();
+    {
+        int n_items, chunk_pages;
+        if (!read_plan(&n_items, &chunk_pages)) return;   // the scheduler reports it
+    }
+
+    if (warp >= kEpilogueWarp) {
         // ================= epilogue =================
         // Writes finished items: the output when the (row, kv head) is one
         // chunk, else the chunk's fp32 partial; the last chunk of a (row, kv
-        // head) to arrive merges every partial and writes the output.
-        int eslot = 0;
+        // head) to arrive merges every partial and writes the output.  Two
+        // warps share the slots (warp e takes slots e, e + 2, ...), so one
+        // item's atomic and merge reads overlap the next item's work.
+        static_assert(kEpiSlots % kEpilogueWarps == 0, "epilogue slots split evenly over the warps");
+        const int ew = warp - kEpilogueWarp;
+        int eslot = ew;
         uint32_t ephase = 0;
         while (true) {
             int waited = 1;
@@ -822,9 +978,9 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                     const int slot0 = slot - mt.chunk;
                     for (int u = lane; u < g * D / 8; u += 32) {
                         const int j = u / (D / 8), d0 = (u % (D / 8)) * 8;
-                        float M = kNegBig;
-                        for (int c = 0; c < nch; ++c) M = fmaxf(M, __ldcg(part_ml + (size_t)(slot0 + c) * g + j).x);
-                        float L = 0.f, O[8];
+                        // one pass with a running maximum, so the loads of
+                        // every chunk go out together
+                        float M = kNegBig, L = 0.f, O[8];
                         #pragma unroll
                         for (int e = 0; e < 8; ++e) O[e] = 0.f;
                         #pragma unroll 4
@@ -832,10 +988,14 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
                             const float2 ml = __ldcg(part_ml + (size_t)(slot0 + c) * g + j);
                             const float4* src = reinterpret_cast<const float4*>(part_o + ((size_t)(slot0 + c) * g + j) * D + d0);
                             const float4 p0 = __ldcg(src), p1 = __ldcg(src + 1);
-                            const float f = exp2_approx(ml.x - M);
-                            L += f * ml.y;
-                            O[0] += f * p0.x; O[1] += f * p0.y; O[2] += f * p0.z; O[3] += f * p0.w;
-                            O[4] += f * p1.x; O[5] += f * p1.y; O[6] += f * p1.z; O[7] += f * p1.w;
+                            const float Mn = fmaxf(M, ml.x);
+                            const float fa = exp2_approx(M - Mn), f = exp2_approx(ml.x - Mn);
+                            M = Mn;
+                            L = L * fa + f * ml.y;
+                            O[0] = O[0] * fa + f * p0.x; O[1] = O[1] * fa + f * p0.y;
+                            O[2] = O[2] * fa + f * p0.z; O[3] = O[3] * fa + f * p0.w;
+                            O[4] = O[4] * fa + f * p1.x; O[5] = O[5] * fa + f * p1.y;
+                            O[6] = O[6] * fa + f * p1.z; O[7] = O[7] * fa + f * p1.w;
                         }
                         const float sk = has_sink ? load_f32<T>(sinks, kvh * g + j) * 1.4426950408889634f : 0.f;
                         const float inv = out_scale(M, L, has_sink, sk);
@@ -847,7 +1007,8 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_eempty + 8 * eslot);
-            if (++eslot == kEpiSlots) { eslot = 0; ephase ^= 1; }
+            eslot += kEpilogueWarps;
+            if (eslot >= kEpiSlots) { eslot -= kEpiSlots; ephase ^= 1; }
         }
         return;
     }
@@ -938,14 +1099,17 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         // the stash buffers are rewritten by the next item
         if (!csync.sync()) { if (lane == 0) fail_timeout(ctrl); ok = false; break; }
     }
-    if (ok) {
-        // Tell the epilogue warp that no more items follow.
+    // Tell each epilogue warp that no more items follow: the next slot of
+    // each warp's share (the next kEpilogueWarps slots) carries the end flag.
+    for (int e = 0; ok && e < kEpilogueWarps; ++e) {
         if (mbar_wait(bar_eempty + 8 * eslot, ephase ^ 1)) {
             if (tid == 0) reinterpret_cast<Meta*>(epi_q + eslot * C::kEpiBytes)->flags = kTerm;
             mbar_arrive(bar_efull + 8 * eslot);
-        } else if (lane == 0) {
-            fail_timeout(ctrl);
+        } else {
+            if (lane == 0) fail_timeout(ctrl);
+            ok = false;
         }
+        if (++eslot == kEpiSlots) { eslot = 0; ephase ^= 1; }
     }
 }
 

@@ -59,7 +59,57 @@ struct WsLayout {
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// max work items: min over split choices of the planner, see the planner.
+// ---------------------------------------------------------------------------
+// The split plan's arithmetic, shared by the planner and by the attention
+// kernel, which derives its first item from the same inputs (positions,
+// windows, split size) before the plan is ready.
+// ---------------------------------------------------------------------------
+
+// Visible positions of a row: [lo, pos] with lo = 0 or pos - window + 1.
+__host__ __device__ __forceinline__ int row_lo(int pos, int window) {
+    return (window > 0 && pos - window + 1 > 0) ? pos - window + 1 : 0;
+}
+
+// Pages per split.  A split costs its chunk a partial write and the row a
+// merge, so rows stay whole (up to kChunkMax pages) unless the longest row
+// exceeds twice the average work per CTA; only then do chunks aim at
+// kItemsPerCta items per CTA.  A sweep on GB300 (gpt-oss-20b, Llama layer)
+// found whole rows 4-21% faster wherever the balance allows them.
+__host__ __device__ __forceinline__ int choose_chunk(unsigned long long row_pages, int max_row_pages, int Hk,
+                                                     int grid) {
+    const unsigned long long work = row_pages * (unsigned long long)Hk;   // page items
+    if ((unsigned long long)max_row_pages * grid <= 2ull * work) return kChunkMax;
+    const unsigned long long per = (unsigned long long)kItemsPerCta * grid;
+    const unsigned long long cc = (work + per - 1) / per;
+    return (int)(cc < 1 ? 1 : (cc > kChunkMax ? kChunkMax : cc));
+}
+
+// A row of n visible pages in nch = ceil(n / C) chunks of equal size, up to
+// one page apart: the first `big` chunks hold q + 1 pages, the others q (so
+// no row ends in a short tail chunk whose merge would come last).
+struct Chunking {
+    int nch, q, big;
+    __host__ __device__ Chunking(int n, int C)
+        : nch((n + C - 1) / C), q(n > 0 ? n / ((n + C - 1) / C) : 0), big(n > 0 ? n % ((n + C - 1) / C) : 0) {}
+    __host__ __device__ int size(int c) const { return c < big ? q + 1 : q; }
+    __host__ __device__ int start(int c) const { return c * q + (c < big ? c : big); }   // pages after the row's first
+};
+
+// The plan's first wave.  With at most kFirstWaveRows rows, items
+// [0, first_wave) are chunk 0 of the (row, kv head) pairs 0, 1, ... in
+// row-major order (an invalid row leaves an empty item, npg 0), and the
+// chunks' merge slots start at an exclusive prefix sum of nch * kv_heads over
+// the rows.  The attention kernel's CTA b can then derive item b from the
+// call's inputs and start loading it before the planner has finished.  The
+// other items follow, largest first.
+constexpr int kFirstWaveRows = 512;
+__host__ __device__ __forceinline__ int first_wave(int rows, int kv_heads, int grid) {
+    const long long pairs = (long long)rows * kv_heads;
+    return rows <= kFirstWaveRows ? (int)(pairs < grid ? pairs : grid) : 0;
+}
+
+// max work items: min over split choices of the planner, see the planner
+// (plus one empty first-wave item per CTA at most).
 __host__ __device__ inline int plan_max_items(int rows, int kv_heads, int pages_per_row,
                                               int chunk_pages, int grid) {
     long long rh = (long long)rows * kv_heads;
@@ -71,7 +121,7 @@ __host__ __device__ inline int plan_max_items(int rows, int kv_heads, int pages_
         long long b = rh * ((pages_per_row + kChunkMax - 1) / kChunkMax);
         n = a > b ? a : b;
     }
-    return (int)n;
+    return (int)(n + grid);
 }
 
 __host__ __device__ inline WsLayout ws_layout(int rows, int heads, int kv_heads, int head_dim,

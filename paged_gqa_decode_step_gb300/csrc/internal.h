@@ -30,6 +30,7 @@ struct AttendLayers {
     CUtensorMap v[kMaxLayers];
     void* out[kMaxLayers];
     const void* sinks[kMaxLayers];
+    int window[kMaxLayers];
 };
 
 struct PrepArgs {
@@ -56,8 +57,10 @@ struct PrepArgs {
 struct AttendArgs {
     int rows, heads, kv_heads, group, head_dim, pages_per_row, num_pages;
     int layer_rows, n_layers;   // multi-layer launches: rows per layer, layers
+    int window, chunk_pages;    // as given to the planner (first-wave items are derived from them)
     float scale_log2;       // score scale times log2(e)
     const void* q;          // rotated queries [rows, heads, D]
+    const int* positions;   // [rows] (per layer in a multi-layer launch)
     const int* table;
     const void* sinks;      // nullptr, or [heads] of T
     void* out;

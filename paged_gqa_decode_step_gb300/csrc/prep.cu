@@ -218,10 +218,6 @@ __device__ void rope_write_row(const PrepArgs& a, const Lay& lay, int row) {
                           rope ? static_cast<const T*>(a.rope_sin) + (size_t)pos * D : nullptr, Hq, Hk, D, page_ok);
 }
 
-// Visible positions of a row: [lo, pos] with lo = 0 or pos - window + 1.
-__device__ __forceinline__ int row_lo(int pos, int window) {
-    return (window > 0 && pos - window + 1 > 0) ? pos - window + 1 : 0;
-}
 
 // One block.  Splits every row's visible pages [lo / 64, pos / 64] into
 // chunks of C pages and lists the (row, kv head, chunk) items sorted by size,
@@ -237,49 +233,61 @@ __device__ __forceinline__ void write_item(ItemDesc* items, int at, int r, int h
     dst[1] = make_int4(first_page, npg, pos, lo);
 }
 
-// Pages per split.  A split costs its chunk a partial write and the row a
-// merge, so rows stay whole (up to kChunkMax pages) unless the longest row
-// exceeds twice the average work per CTA; only then do chunks aim at
-// kItemsPerCta items per CTA.  A sweep on GB300 (gpt-oss-20b, Llama layer)
-// found whole rows 4-21% faster wherever the balance allows them.
-__device__ __forceinline__ int choose_chunk(unsigned long long row_pages, int max_row_pages, int Hk, int grid) {
-    const unsigned long long work = row_pages * (unsigned long long)Hk;   // page items
-    if ((unsigned long long)max_row_pages * grid <= 2ull * work) return kChunkMax;
-    const unsigned long long per = (unsigned long long)kItemsPerCta * grid;
-    const unsigned long long cc = (work + per - 1) / per;
-    return (int)(cc < 1 ? 1 : (cc > kChunkMax ? kChunkMax : cc));
+// Exclusive block scan (sum, or max with kMax) of one int per thread, with
+// `identity` before the first thread; blockDim.x a multiple of 32.  *total
+// gets the block's sum or max.
+template <bool kMax>
+__device__ int block_scan_excl(int v, int identity, int* s_warp, int* total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
+    #pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x = kMax ? max(x, o) : x + o;
+    }
+    if (lane == 31) s_warp[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int t = lane < nw ? s_warp[lane] : identity;
+        #pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, t, d);
+            if (lane >= d) t = kMax ? max(t, o) : t + o;
+        }
+        if (lane < nw) s_warp[lane] = t;
+    }
+    __syncthreads();
+    int up = __shfl_up_sync(0xffffffffu, x, 1);
+    if (lane == 0) up = identity;
+    const int pre = w > 0 ? s_warp[w - 1] : identity;
+    const int ex = kMax ? max(pre, up) : pre + up;
+    *total = s_warp[nw - 1];
+    __syncthreads();
+    return ex;
 }
 
-// A row of n visible pages in nch = ceil(n / C) chunks of equal size, up to
-// one page apart: the first `big` chunks hold q + 1 pages, the others q (so
-// no row ends in a short tail chunk whose merge would come last).
-struct Chunking {
-    int nch, q, big;
-    __device__ Chunking(int n, int C) : nch((n + C - 1) / C), q(n > 0 ? n / ((n + C - 1) / C) : 0),
-                                        big(n > 0 ? n % ((n + C - 1) / C) : 0) {}
-    __device__ int size(int c) const { return c < big ? q + 1 : q; }
-    __device__ int start(int c) const { return c * q + (c < big ? c : big); }   // pages after the row's first
-};
-
-// One row per thread (rows <= block size): every value stays in registers or
-// shared memory after the positions are read once, so the plan costs one
-// global round trip plus its stores.
+// One row per thread (rows <= kFirstWaveRows <= block size): every value
+// stays in registers or shared memory after the positions are read once, so
+// the plan costs one global round trip plus its stores.  The first wave
+// (first_wave) takes items [0, nf); merge slots start at the exclusive prefix
+// sum of nch * kv_heads; the other items follow, largest first.
 template <typename Lay>
 __device__ bool build_plan_small(const PrepArgs& a, const Lay& lay) {
-    __shared__ int4 s_row[512];
-    __shared__ int2 s_at2[512];
-    __shared__ int s_cnt[kChunkMax + 1];
-    __shared__ int s_cur[kChunkMax + 1];
+    __shared__ int4 s_row[kFirstWaveRows];
+    __shared__ int2 s_at2[kFirstWaveRows];
+    __shared__ int s_cnt[kChunkMax + 2];
+    __shared__ int s_cur[kChunkMax + 2];
     __shared__ int s_warp[16];
     __shared__ int s_warp_max[16];
-    __shared__ int s_slots;
+    __shared__ int s_scan[32];
     __shared__ int s_chunk;
     const int tid = threadIdx.x, R = a.rows, Hk = a.kv_heads, max_pos = a.pages_per_row * kPageSize;
-    if (R > (int)blockDim.x || R > 512) return false;
+    if (R > (int)blockDim.x || R > kFirstWaveRows) return false;
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(a.ws + a.L.ctrl);
     int4* row_info = reinterpret_cast<int4*>(a.ws + a.L.row_info);
     ItemDesc* items = reinterpret_cast<ItemDesc*>(a.ws + a.L.items);
     int* merge_cnt = reinterpret_cast<int*>(a.ws + a.L.merge_cnt);
+    const int nf = first_wave(R, Hk, a.grid_attend);
 
     const bool mine = tid < R;
     const int pos = mine ? __ldg(a.positions + table_row<Lay>(a, tid)) : -1;
@@ -288,8 +296,7 @@ __device__ bool build_plan_small(const PrepArgs& a, const Lay& lay) {
     const int lo = ok ? row_lo(pos, row_window(a, lay, tid)) : 0;
     const int first = lo / kPageSize;
     const int n = ok ? pos / kPageSize - first + 1 : 0;
-    for (int i = tid; i <= kChunkMax; i += blockDim.x) s_cnt[i] = 0;
-    if (tid == 0) s_slots = 0;
+    for (int i = tid; i < kChunkMax + 2; i += blockDim.x) s_cnt[i] = 0;
     const int wsum = __reduce_add_sync(0xffffffffu, (unsigned)n);
     const int wmax = __reduce_max_sync(0xffffffffu, (unsigned)n);
     if ((tid & 31) == 0) {
@@ -311,16 +318,20 @@ __device__ bool build_plan_small(const PrepArgs& a, const Lay& lay) {
     const int C = s_chunk;
     const Chunking ch(n, C);
     const int nch = ch.nch;
-    int base = 0;
+    int total_slots = 0;
+    const int base = block_scan_excl<false>(nch * Hk, 0, s_scan, &total_slots);
+    // kv heads of this row whose chunk 0 is in the first wave
+    const int ex = min(max(nf - tid * Hk, 0), Hk);
     if (ok) {
-        if (ch.big) atomicAdd(&s_cnt[ch.q + 1], ch.big * Hk);
-        atomicAdd(&s_cnt[ch.q], (nch - ch.big) * Hk);
-        base = atomicAdd(&s_slots, nch * Hk);
+        const int cnt_big = ch.big * Hk - (ch.big > 0 ? ex : 0);
+        const int cnt_small = (nch - ch.big) * Hk - (ch.big > 0 ? 0 : ex);
+        if (cnt_big) atomicAdd(&s_cnt[ch.q + 1], cnt_big);
+        if (cnt_small) atomicAdd(&s_cnt[ch.q], cnt_small);
     }
     if (mine) row_info[tid] = make_int4(ok ? pos : -1, lo, nch, base);
     __syncthreads();
     if (tid == 0) {
-        int off = 0;
+        int off = nf;
         for (int q = C; q >= 1; --q) { s_cur[q] = off; off += s_cnt[q]; }
         s_cnt[0] = off;
     }
@@ -330,8 +341,10 @@ __device__ bool build_plan_small(const PrepArgs& a, const Lay& lay) {
     if (mine) {
         int at_big = 0, at_small = 0;
         if (ok && fits) {
-            at_big = ch.big ? atomicAdd(&s_cur[ch.q + 1], ch.big * Hk) : 0;
-            at_small = atomicAdd(&s_cur[ch.q], (nch - ch.big) * Hk);
+            const int cnt_big = ch.big * Hk - (ch.big > 0 ? ex : 0);
+            const int cnt_small = (nch - ch.big) * Hk - (ch.big > 0 ? 0 : ex);
+            at_big = cnt_big ? atomicAdd(&s_cur[ch.q + 1], cnt_big) : 0;
+            at_small = cnt_small ? atomicAdd(&s_cur[ch.q], cnt_small) : 0;
         }
         s_row[tid] = make_int4(ok ? pos : -1, lo, nch, base);
         s_at2[tid] = make_int2(at_big, at_small);
@@ -341,13 +354,23 @@ __device__ bool build_plan_small(const PrepArgs& a, const Lay& lay) {
         const int r = pr / Hk, h = pr % Hk;
         merge_cnt[pr] = 0;
         const int4 ri = s_row[r];
-        if (!fits || ri.x < 0) continue;
+        if (!fits) continue;
+        if (ri.x < 0) {
+            // an invalid row keeps its first-wave places, as empty items
+            if (pr < nf) write_item(items, pr, r, h, 0, 0, 0, 0, 0, -1, 0);
+            continue;
+        }
         const int2 at = s_at2[r];
         const int rf = ri.y / kPageSize;
         const Chunking rc(ri.x / kPageSize - rf + 1, C);
-        for (int c = 0; c < ri.z; ++c)
-            write_item(items, c < rc.big ? at.x + c * Hk + h : at.y + (c - rc.big) * Hk + h, r, h, c, ri.z, ri.w,
-                       rf + rc.start(c), rc.size(c), ri.x, ri.y);
+        const int rex = min(max(nf - r * Hk, 0), Hk);
+        for (int c = 0; c < ri.z; ++c) {
+            int idx;
+            if (c == 0 && pr < nf) idx = pr;
+            else if (c < rc.big) idx = at.x + c * Hk + h - rex;
+            else idx = at.y + (c - rc.big) * Hk + h - (rc.big > 0 ? 0 : rex);
+            write_item(items, idx, r, h, c, ri.z, ri.w, rf + rc.start(c), rc.size(c), ri.x, ri.y);
+        }
     }
     __syncthreads();
     if (tid == 0) {
@@ -526,38 +549,6 @@ __global__ void __launch_bounds__(kRopeRowThreads) rope_write_kernel(const __gri
 // ---------------------------------------------------------------------------
 constexpr int kPfBuckets = 1024;     // sort buckets of tile sizes (pages, capped)
 
-// Exclusive block scan (sum, or max with kMax) of one int per thread, with
-// `identity` before the first thread; blockDim.x a multiple of 32.  *total
-// gets the block's sum or max.
-template <bool kMax>
-__device__ int block_scan_excl(int v, int identity, int* s_warp, int* total) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    int x = v;
-    #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, x, d);
-        if (lane >= d) x = kMax ? max(x, o) : x + o;
-    }
-    if (lane == 31) s_warp[w] = x;
-    __syncthreads();
-    if (w == 0) {
-        int t = lane < nw ? s_warp[lane] : identity;
-        #pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, t, d);
-            if (lane >= d) t = kMax ? max(t, o) : t + o;
-        }
-        if (lane < nw) s_warp[lane] = t;
-    }
-    __syncthreads();
-    int up = __shfl_up_sync(0xffffffffu, x, 1);
-    if (lane == 0) up = identity;
-    const int pre = w > 0 ? s_warp[w - 1] : identity;
-    const int ex = kMax ? max(pre, up) : pre + up;
-    *total = s_warp[nw - 1];
-    __syncthreads();
-    return ex;
-}
 
 // The planners run as one block of kPrepThreads threads over chunks of
 // kChunk tokens.  A chunk's row (or segment) ids and positions are staged in
