@@ -22,6 +22,13 @@
  * T is bf16 or f32 (pdattn_dtype).  head_dim is 64 or 128, page_size 64,
  * heads / kv_heads <= 8.  Pointers to T data must be 16-byte aligned.
  *
+ * Pages: a step writes each row's new k and v into that row's last visible
+ * page (table[r, pos / 64]); the attention may read a row's earlier pages
+ * while those writes are still in flight.  So a page that some row writes
+ * in a call must not also be an earlier page of another row in that call:
+ * rows may share only pages that no row of the call writes (full prefix
+ * pages), as a paged cache lays them out.
+ *
  * Ownership: the caller allocates and owns every buffer, including the
  * workspace; the library allocates no device memory, keeps no per-call state
  * and frees nothing.  It caches only per-device properties.

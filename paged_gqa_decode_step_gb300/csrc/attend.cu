@@ -43,7 +43,6 @@ constexpr int kEpilogueWarps = 2;
 constexpr int kThreads = (kConsumerWarps + 2 + kEpilogueWarps) * 32;
 constexpr int kItemSlots = 4;           // items the scheduler may hold ahead of the producer
 constexpr int kBacklogBytes = 256 << 10;  // K/V bytes queued ahead of the TMA issue point
-constexpr int kEpiSlots = 4;            // finished items waiting for the epilogue warp
 constexpr float kNegBig = -1.0e30f;     // running-max start: finite, so exp2(m - m) = 1
 constexpr size_t kTablePrefetchMax = size_t(8) << 20;   // larger page tables are not prefetched
 
@@ -79,22 +78,24 @@ struct Cfg {
     static constexpr int kStages = (kStageBytes <= 16384) ? 10 : (kStageBytes <= 32768 ? 5 : 2);
     static constexpr int kQRow = q_row_bytes<T, D>();
     static constexpr int kQBytes = kMaxGroup * kQRow;
-    static constexpr int kORow = D + 4;                          // padded row of the merge buffer
-    static constexpr int kMergeFloats = 2 * kConsumerWarps * kMaxGroup + kConsumerWarps * kMaxGroup * kORow;
+    static constexpr int kORow = D + 4;                          // padded head row of a stashed output
     static constexpr int kOffQ = kStages * kStageBytes;
-    static constexpr int kOffMerge = kOffQ + kStages * kQBytes;
     static constexpr int kWarpQBytes = (kElem == 4) ? kConsumerWarps * kQBytes : 0;  // f32: private copies
     static constexpr int kWarpPBytes = (kElem == 4) ? kConsumerWarps * kMaxGroup * 16 * 4 : 0;  // f32: p buffers
-    static constexpr int kOffWarpQ = kOffMerge + kMergeFloats * 4;
+    static constexpr int kOffWarpQ = kOffQ + kStages * kQBytes;
     static constexpr int kOffWarpP = kOffWarpQ + kWarpQBytes;
     static constexpr int kOffItems = kOffWarpP + kWarpPBytes;    // kItemSlots x (ItemDesc + 64 page ids)
     static constexpr int kItemBytes = (int)sizeof(ItemDesc) + kChunkMax * 4;
-    // epilogue slots: Meta, (M, L) per head, O[head][D] (fp32, unnormalised)
-    static constexpr int kEpiBytes = (int)sizeof(Meta) + kMaxGroup * 8 + kMaxGroup * D * 4;
+    // Epilogue slots: Meta, then each consumer warp's (m, l) per head and
+    // its O[head][kORow] (fp32, unnormalised); the epilogue warps merge the
+    // four warps.  Two slots per epilogue warp at head dim 64, one at 128.
+    static constexpr int kEpiSlots = D == 128 ? 2 : 4;
+    static constexpr int kEpiOffO = (int)sizeof(Meta) + kConsumerWarps * kMaxGroup * 8;
+    static constexpr int kEpiBytes = kEpiOffO + kConsumerWarps * kMaxGroup * kORow * 4;
     static constexpr int kOffEpi = kOffItems + kItemSlots * kItemBytes;
     static constexpr int kOffMeta = kOffEpi + kEpiSlots * kEpiBytes;
     static constexpr int kOffBar = kOffMeta + kStages * (int)sizeof(Meta);
-    static constexpr int kNumBars = 2 * kStages + 1 + 2 * kItemSlots + 2 * kEpiSlots;
+    static constexpr int kNumBars = 2 * kStages + 2 * kItemSlots + 2 * kEpiSlots;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffMisc + 16 + 1024;           // + alignment slack
     // pages the scheduler keeps queued beyond the producer's issue point
@@ -102,20 +103,9 @@ struct Cfg {
     static constexpr int kBacklogPages = kBacklogBytes / kPageBytes > 2 ? kBacklogBytes / kPageBytes : 2;
     static_assert(kSmem <= 232448, "shared memory per CTA");
     static_assert(kOffBar % 8 == 0, "mbarrier alignment");
+    static_assert(kEpiOffO % 16 == 0 && kEpiBytes % 16 == 0 && kOffEpi % 16 == 0, "16-byte stash rows");
 };
 
-// Reusable barrier among the 128 consumer threads, on an mbarrier so that its
-// wait is bounded.
-struct ConsumerSync {
-    uint32_t bar;
-    uint32_t phase;
-    __device__ bool sync() {
-        mbar_arrive(bar);
-        bool ok = mbar_wait(bar, phase);
-        phase ^= 1;
-        return ok;
-    }
-};
 
 template <typename T>
 __device__ __forceinline__ float load_f32(const void* base, int i);
@@ -268,8 +258,9 @@ struct Consumer<__nv_bfloat16, D, G> {
                            va_[mt][3] & keep_b, b0, b1);
     }
 
-    // Put this warp's (m, l, o) for heads 0..7 into the merge buffer.
-    __device__ void stash(float* sm_m, float* sm_l, float* sm_o, int warp, int lane) {
+    // Put this warp's (m, l) per head (ml[8]) and o for heads 0..7
+    // (ow[8][D + 4]) into an epilogue slot.
+    __device__ void stash(float2* ml, float* ow, int lane) {
         float s0 = l0, s1 = l1;
         #pragma unroll
         for (int sh = 4; sh < 32; sh <<= 1) {
@@ -278,12 +269,9 @@ struct Consumer<__nv_bfloat16, D, G> {
         }
         const int h0 = 2 * (lane & 3);
         if (lane < 4) {
-            sm_m[warp * kMaxGroup + h0] = m0;
-            sm_m[warp * kMaxGroup + h0 + 1] = m1;
-            sm_l[warp * kMaxGroup + h0] = s0;
-            sm_l[warp * kMaxGroup + h0 + 1] = s1;
+            ml[h0] = make_float2(m0, s0);
+            ml[h0 + 1] = make_float2(m1, s1);
         }
-        float* ow = sm_o + warp * kMaxGroup * (D + 4);
         const int d = lane >> 2;
         #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
@@ -439,21 +427,18 @@ struct Consumer<float, D, G> {
         __syncwarp();   // sp is rewritten by the next page
     }
 
-    __device__ void stash(float* sm_m, float* sm_l, float* sm_o, int warp, int lane) {
+    __device__ void stash(float2* ml, float* ow, int lane) {
         #pragma unroll
         for (int j = 0; j < G; ++j) {
             if (j < g) {
                 float lt = l[j];
                 #pragma unroll
                 for (int sh = 1; sh < 32; sh <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, sh);
-                if (lane == 0) {
-                    sm_m[warp * kMaxGroup + j] = m[j];
-                    sm_l[warp * kMaxGroup + j] = lt;
-                }
+                if (lane == 0) ml[j] = make_float2(m[j], lt);
                 #pragma unroll
                 for (int e = 0; e < VD; ++e) {
                     const float tot = o[j][e] + __shfl_xor_sync(0xffffffffu, o[j][e], 16);
-                    if (lane < 16) sm_o[(warp * kMaxGroup + j) * (D + 4) + lane * VD + e] = tot;
+                    if (lane < 16) ow[j * (D + 4) + lane * VD + e] = tot;
                 }
             }
         }
@@ -523,15 +508,11 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar_full = sbase + C::kOffBar;             // S barriers: stage holds data
     const uint32_t bar_empty = bar_full + 8 * S;              // S barriers: stage may be refilled
-    const uint32_t bar_sync = bar_empty + 8 * S;              // consumer barrier
-    const uint32_t bar_ifull = bar_sync + 8;                  // kItemSlots: item queued
+    const uint32_t bar_ifull = bar_empty + 8 * S;             // kItemSlots: item queued
     const uint32_t bar_iempty = bar_ifull + 8 * kItemSlots;   // kItemSlots: item slot free
-    const uint32_t bar_efull = bar_iempty + 8 * kItemSlots;   // kEpiSlots: finished item queued
-    const uint32_t bar_eempty = bar_efull + 8 * kEpiSlots;    // kEpiSlots: epilogue slot free
+    const uint32_t bar_efull = bar_iempty + 8 * kItemSlots;   // C::kEpiSlots: finished item queued
+    const uint32_t bar_eempty = bar_efull + 8 * C::kEpiSlots; // C::kEpiSlots: epilogue slot free
     Meta* meta = reinterpret_cast<Meta*>(smem + C::kOffMeta);
-    float* sm_m = reinterpret_cast<float*>(smem + C::kOffMerge);
-    float* sm_l = sm_m + kConsumerWarps * kMaxGroup;
-    float* sm_o = sm_l + kConsumerWarps * kMaxGroup;
     int* s_flag = reinterpret_cast<int*>(smem + C::kOffMisc);
     volatile int* s_issued = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);  // pages issued so far
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);   // 1: the plan was refused
@@ -545,7 +526,6 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, kConsumerWarps);
         }
-        mbar_init(bar_sync, kConsumerWarps * 32);
         *s_issued = 0;
         *s_abort = 0;
         *s_early = 0;
@@ -553,7 +533,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             mbar_init(bar_ifull + 8 * s, 1);
             mbar_init(bar_iempty + 8 * s, 1);
         }
-        for (int s = 0; s < kEpiSlots; ++s) {
+        for (int s = 0; s < C::kEpiSlots; ++s) {
             mbar_init(bar_efull + 8 * s, kConsumerWarps * 32);
             mbar_init(bar_eempty + 8 * s, 1);
         }
@@ -921,7 +901,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         // head) to arrive merges every partial and writes the output.  Two
         // warps share the slots (warp e takes slots e, e + 2, ...), so one
         // item's atomic and merge reads overlap the next item's work.
-        static_assert(kEpiSlots % kEpilogueWarps == 0, "epilogue slots split evenly over the warps");
+        static_assert(C::kEpiSlots % kEpilogueWarps == 0, "epilogue slots split evenly over the warps");
         const int ew = warp - kEpilogueWarp;
         int eslot = ew;
         uint32_t ephase = 0;
@@ -933,8 +913,28 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             const uint8_t* ep = epi_q + eslot * C::kEpiBytes;
             const Meta mt = *reinterpret_cast<const Meta*>(ep);
             if (mt.flags & kTerm) break;
-            const float2* eml = reinterpret_cast<const float2*>(ep + sizeof(Meta));
-            const float* eo = reinterpret_cast<const float*>(ep + sizeof(Meta) + kMaxGroup * 8);
+            const float2* eml = reinterpret_cast<const float2*>(ep + sizeof(Meta));   // [warp][head]
+            const float* eo = reinterpret_cast<const float*>(ep + C::kEpiOffO);        // [warp][head][kORow]
+            // The four consumer warps' (m, l, o) of head j, dims d0 .. d0 + 7,
+            // merged: M = max m_w, L = sum e^(m_w - M) l_w, O = sum e^(m_w - M) o_w.
+            auto merge4 = [&](int j, int d0, float& M, float& L, float (&O)[8]) {
+                M = kNegBig;
+                #pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, eml[w * kMaxGroup + j].x);
+                L = 0.f;
+                #pragma unroll
+                for (int e = 0; e < 8; ++e) O[e] = 0.f;
+                #pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float2 ml = eml[w * kMaxGroup + j];
+                    const float f = exp2_approx(ml.x - M);
+                    L += f * ml.y;
+                    const float4* src = reinterpret_cast<const float4*>(eo + (w * kMaxGroup + j) * C::kORow + d0);
+                    const float4 p0 = src[0], p1 = src[1];
+                    O[0] += f * p0.x; O[1] += f * p0.y; O[2] += f * p0.z; O[3] += f * p0.w;
+                    O[4] += f * p1.x; O[5] += f * p1.y; O[6] += f * p1.z; O[7] += f * p1.w;
+                }
+            };
             const int row = mt.row, kvh = mt.kvh, nch = mt.nch, slot = mt.slot;
             T* out_base = static_cast<T*>(a.out) + ((size_t)row * a.heads + kvh * g) * D;
             const void* sinks = a.sinks;
@@ -947,21 +947,24 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             if (nch == 1) {
                 for (int u = lane; u < g * D / 8; u += 32) {
                     const int j = u / (D / 8), d0 = (u % (D / 8)) * 8;
+                    float M, L, O[8];
+                    merge4(j, d0, M, L, O);
                     const float sk = has_sink ? load_f32<T>(sinks, kvh * g + j) * 1.4426950408889634f : 0.f;
-                    const float inv = out_scale(eml[j].x, eml[j].y, has_sink, sk);
-                    float O[8];
+                    const float inv = out_scale(M, L, has_sink, sk);
                     #pragma unroll
-                    for (int e = 0; e < 8; ++e) O[e] = eo[j * D + d0 + e] * inv;
+                    for (int e = 0; e < 8; ++e) O[e] *= inv;
                     store8<T>(out_base + j * D + d0, O);
                 }
             } else {
                 for (int u = lane; u < g * D / 8; u += 32) {
                     const int j = u / (D / 8), d0 = (u % (D / 8)) * 8;
+                    float M, L, O[8];
+                    merge4(j, d0, M, L, O);
                     float4* dst = reinterpret_cast<float4*>(part_o + ((size_t)slot * g + j) * D + d0);
-                    dst[0] = *reinterpret_cast<const float4*>(eo + j * D + d0);
-                    dst[1] = *reinterpret_cast<const float4*>(eo + j * D + d0 + 4);
+                    dst[0] = make_float4(O[0], O[1], O[2], O[3]);
+                    dst[1] = make_float4(O[4], O[5], O[6], O[7]);
+                    if (d0 == 0) part_ml[(size_t)slot * g + j] = make_float2(M, L);
                 }
-                if (lane < g) part_ml[(size_t)slot * g + lane] = eml[lane];
                 __syncwarp();
                 int last = 0;
                 if (lane == 0) {
@@ -1008,14 +1011,13 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_eempty + 8 * eslot);
             eslot += kEpilogueWarps;
-            if (eslot >= kEpiSlots) { eslot -= kEpiSlots; ephase ^= 1; }
+            if (eslot >= C::kEpiSlots) { eslot -= C::kEpiSlots; ephase ^= 1; }
         }
         return;
     }
 
     // ================= consumers =================
     Consumer<T, D, G> cs;
-    ConsumerSync csync{bar_sync, 0};
     int stage = 0;
     uint32_t phase = 0;
     int eslot = 0;
@@ -1062,42 +1064,20 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
         if (++stage == S) { stage = 0; phase ^= 1; }
         if (!(mt.flags & kLast)) continue;
 
-        // ---- item done: merge the four warps into an epilogue slot
-        cs.stash(sm_m, sm_l, sm_o, warp, lane);
-        if (!csync.sync() || !mbar_wait(bar_eempty + 8 * eslot, ephase ^ 1)) {
+        // ---- item done: this warp's (m, l, o) into the next epilogue slot,
+        // with no wait on the other consumer warps (the epilogue warps merge
+        // the four); the slot is handed over once all 128 threads arrived.
+        if (!mbar_wait(bar_eempty + 8 * eslot, ephase ^ 1)) {
             if (lane == 0) fail_timeout(ctrl);
             ok = false;
             break;
         }
         uint8_t* ep = epi_q + eslot * C::kEpiBytes;
-        float2* eml = reinterpret_cast<float2*>(ep + sizeof(Meta));
-        float* eo = reinterpret_cast<float*>(ep + sizeof(Meta) + kMaxGroup * 8);
-        const int units = D / 8;
-        const int j = tid / units, d0 = (tid % units) * 8;
-        if (j < g) {
-            float M = kNegBig;
-            #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm_m[w * kMaxGroup + j]);
-            float L = 0.f, O[8];
-            #pragma unroll
-            for (int e = 0; e < 8; ++e) O[e] = 0.f;
-            #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float f = exp2_approx(sm_m[w * kMaxGroup + j] - M);
-                L += f * sm_l[w * kMaxGroup + j];
-                const float* src = sm_o + (w * kMaxGroup + j) * (D + 4) + d0;
-                #pragma unroll
-                for (int e = 0; e < 8; ++e) O[e] += f * src[e];
-            }
-            reinterpret_cast<float4*>(eo + j * D + d0)[0] = make_float4(O[0], O[1], O[2], O[3]);
-            reinterpret_cast<float4*>(eo + j * D + d0)[1] = make_float4(O[4], O[5], O[6], O[7]);
-            if (d0 == 0) eml[j] = make_float2(M, L);
-        }
+        cs.stash(reinterpret_cast<float2*>(ep + sizeof(Meta)) + warp * kMaxGroup,
+                 reinterpret_cast<float*>(ep + C::kEpiOffO) + warp * kMaxGroup * C::kORow, lane);
         if (tid == 0) *reinterpret_cast<Meta*>(ep) = mt;
         mbar_arrive(bar_efull + 8 * eslot);
-        if (++eslot == kEpiSlots) { eslot = 0; ephase ^= 1; }
-        // the stash buffers are rewritten by the next item
-        if (!csync.sync()) { if (lane == 0) fail_timeout(ctrl); ok = false; break; }
+        if (++eslot == C::kEpiSlots) { eslot = 0; ephase ^= 1; }
     }
     // Tell each epilogue warp that no more items follow: the next slot of
     // each warp's share (the next kEpilogueWarps slots) carries the end flag.
@@ -1109,7 +1089,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             if (lane == 0) fail_timeout(ctrl);
             ok = false;
         }
-        if (++eslot == kEpiSlots) { eslot = 0; ephase ^= 1; }
+        if (++eslot == C::kEpiSlots) { eslot = 0; ephase ^= 1; }
     }
 }
 
