@@ -439,19 +439,20 @@ def measure_decode_config(args, b, w, dev, world, rank):
     }
 
 
-def measure_layers(args, b, w, n_layers, dev, world, rank):
-    """gpt-oss-20b decode step over n_layers layers (LayerPairs: a window-128
-    layer, then a full one; shared positions and page table, per-layer
-    caches): one pdattn_decode_layers call against one decode_fused call per
-    layer, back to back on the stream, and against those calls replayed from
-    a CUDA graph.  K/V bytes are all layers' visible pages."""
+def measure_layers(args, b, w, n_layers, dev, world, rank, pairs=True):
+    """Decode step over n_layers layers (shared positions and page table,
+    per-layer caches): one pdattn_decode_layers call against one decode_fused
+    call per layer, back to back on the stream, and against those calls
+    replayed from a CUDA graph.  With `pairs` the layers alternate a window-128
+    layer and a full one (gpt-oss-20b LayerPairs); otherwise all are full.
+    K/V bytes are all layers' visible pages."""
     base = wl.generate(w, dev, seed=rank_seed(w, rank))
     gen = torch.Generator(device=dev)
     gen.manual_seed(rank_seed(w, rank) + 1)
     pos_list = base["positions"].cpu().tolist()
     num_pages = base["k_pool"].shape[0]
     cos, sin = b.rope_tables(w.rope_theta, w.head_dim, w.max_seq, w.torch_dtype)
-    windows = [128 if l % 2 == 0 else 0 for l in range(n_layers)]
+    windows = [128 if (pairs and l % 2 == 0) else 0 for l in range(n_layers)]
     layers = []
     for l in range(n_layers):
         y = {k: torch.randn(base[k].shape, generator=gen, device=dev, dtype=torch.float32).to(w.torch_dtype)
@@ -502,7 +503,8 @@ def measure_layers(args, b, w, n_layers, dev, world, rank):
     except Exception as exc:  # an extra measurement; the two above stand on their own
         print(f"graph capture skipped: {exc}", file=sys.stderr)
     peak, peak_kind = measured_hbm_peak()
-    return {"layers": n_layers, "windows": "128, 0, 128, 0, ...", "rows": w.rows, "heads": w.heads,
+    return {"layers": n_layers, "windows": "128, 0, 128, 0, ..." if pairs else "0 (all full)", "rows": w.rows,
+            "heads": w.heads,
             "kv_heads": w.kv_heads, "head_dim": w.head_dim, "kv_bytes_per_step": kvb,
             "frac_of_hbm_peak": res["one_call"]["kv_gbs"] / peak, "peak": peak, "peak_kind": peak_kind,
             "l2": "inputs larger than L2" if large else "L2 flushed (512 MB write) between timed steps",
@@ -527,6 +529,8 @@ def other_configs(args, world, rank, local):
     for n_layers in (2, 24):
         res[f"gptoss20b_layers{n_layers}"] = measure_layers(args, b, wl.GPTOSS_FULL, n_layers, dev, world, rank)
         torch.cuda.empty_cache()
+    res["llama8b_layer_layers32"] = measure_layers(args, b, wl.LLAMA_LAYER, 32, dev, world, rank, pairs=False)
+    torch.cuda.empty_cache()
     for w in wl.PREFILL_WORKLOADS.values():
         res[w.name] = run_prefill(args, w, world, rank, local, light=True)
         torch.cuda.empty_cache()

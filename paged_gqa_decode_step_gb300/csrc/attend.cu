@@ -35,12 +35,10 @@
 
 namespace pdattn {
 
+// Consumer warps: four, each with 16 of a page's 64 tokens (the rows of the
+// bf16 MMA tile; the f32 consumer uses the same split).
 constexpr int kConsumerWarps = 4;
-constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kSchedulerWarp = kConsumerWarps + 1;
-constexpr int kEpilogueWarp = kConsumerWarps + 2;   // and the next warp: two epilogue warps
 constexpr int kEpilogueWarps = 2;
-constexpr int kThreads = (kConsumerWarps + 2 + kEpilogueWarps) * 32;
 constexpr int kItemSlots = 4;           // items the scheduler may hold ahead of the producer
 constexpr int kBacklogBytes = 256 << 10;  // K/V bytes queued ahead of the TMA issue point
 constexpr float kNegBig = -1.0e30f;     // running-max start: finite, so exp2(m - m) = 1
@@ -64,8 +62,12 @@ constexpr int kValidShift = 16;
 template <typename T, int D>
 __host__ __device__ constexpr int q_row_bytes() { return sizeof(T) == 2 ? D * 2 + 16 : D * (int)sizeof(T); }
 
-template <typename T, int D>
+template <typename T, int D, int G>
 struct Cfg {
+    // warp roles: consumers 0 .. kCW - 1, producer, scheduler, two epilogue warps
+    static constexpr int kCW = kConsumerWarps;
+    static constexpr int kProducer = kCW, kScheduler = kCW + 1, kEpilogue = kCW + 2;
+    static constexpr int kThreads = (kCW + 2 + kEpilogueWarps) * 32;
     static constexpr int kElem = sizeof(T);
     static constexpr int kBoxCols = 128 / kElem;                 // columns per 128-byte box row
     static constexpr int kBoxes = D / kBoxCols;                  // boxes per K (or V) page
@@ -77,11 +79,13 @@ struct Cfg {
     static constexpr int kStageBytes = 2 * kPagesPerStage * kTileBytes;   // K pages, then V pages
     static constexpr int kStages = (kStageBytes <= 16384) ? 10 : (kStageBytes <= 32768 ? 5 : 2);
     static constexpr int kQRow = q_row_bytes<T, D>();
-    static constexpr int kQBytes = kMaxGroup * kQRow;
+    // bf16: eight head rows (the MMA's N; rows past the group stay zero); f32: G
+    static constexpr int kQHeads = kElem == 2 ? kMaxGroup : G;
+    static constexpr int kQBytes = kQHeads * kQRow;
     static constexpr int kORow = D + 4;                          // padded head row of a stashed output
     static constexpr int kOffQ = kStages * kStageBytes;
-    static constexpr int kWarpQBytes = (kElem == 4) ? kConsumerWarps * kQBytes : 0;  // f32: private copies
-    static constexpr int kWarpPBytes = (kElem == 4) ? kConsumerWarps * kMaxGroup * 16 * 4 : 0;  // f32: p buffers
+    static constexpr int kWarpQBytes = (kElem == 4 && G > 1) ? kCW * kQBytes : 0;  // f32: private copies
+    static constexpr int kWarpPBytes = (kElem == 4) ? kCW * G * (64 / kCW) * 4 : 0;   // f32: p buffers
     static constexpr int kOffWarpQ = kOffQ + kStages * kQBytes;
     static constexpr int kOffWarpP = kOffWarpQ + kWarpQBytes;
     static constexpr int kOffItems = kOffWarpP + kWarpPBytes;    // kItemSlots x (ItemDesc + 64 page ids)
@@ -90,8 +94,9 @@ struct Cfg {
     // its O[head][kORow] (fp32, unnormalised); the epilogue warps merge the
     // four warps.  Two slots per epilogue warp at head dim 64, one at 128.
     static constexpr int kEpiSlots = D == 128 ? 2 : 4;
-    static constexpr int kEpiOffO = (int)sizeof(Meta) + kConsumerWarps * kMaxGroup * 8;
-    static constexpr int kEpiBytes = kEpiOffO + kConsumerWarps * kMaxGroup * kORow * 4;
+    static constexpr int kEpiHeads = kElem == 2 ? kMaxGroup : G;   // heads each warp stashes
+    static constexpr int kEpiOffO = (int)sizeof(Meta) + kCW * kEpiHeads * 8;
+    static constexpr int kEpiBytes = kEpiOffO + kCW * kEpiHeads * kORow * 4;
     static constexpr int kOffEpi = kOffItems + kItemSlots * kItemBytes;
     static constexpr int kOffMeta = kOffEpi + kEpiSlots * kEpiBytes;
     static constexpr int kOffBar = kOffMeta + kStages * (int)sizeof(Meta);
@@ -299,23 +304,26 @@ constexpr float kLazyLog2 = 8.f;
 
 template <int D, int G>
 struct Consumer<float, D, G> {
+    static constexpr int TPW = 64 / kConsumerWarps;   // tokens per warp
+    static constexpr int NQ = 32 / TPW;       // lanes sharing one token's score (parts of D)
+    static constexpr int DQ = D / NQ;         // dimensions per part
     static constexpr int VD = D / 16;          // value dimensions per lane
     static constexpr bool kQRegs = (G == 1);
     float o[G][VD];
     float m[G], l[G];
-    float qr[kQRegs ? D / 2 : 1];
+    float qr[kQRegs ? DQ : 1];
     const float* wq;       // this warp's copy of the query group [g][D] (G > 1)
-    float* sp;             // this warp's probabilities [kMaxGroup][16]
+    float* sp;             // this warp's probabilities [G][TPW]
     int g;
 
     __device__ void begin(const float* qbuf, float* warp_q, float* warp_p, int lane, int group) {
         g = group;
         sp = warp_p;
         if constexpr (kQRegs) {
-            const int half = lane >> 4;
+            const int part = lane / TPW;
             #pragma unroll
-            for (int i = 0; i < D / 8; ++i) {
-                const float4 v = reinterpret_cast<const float4*>(qbuf + half * (D / 2))[i];
+            for (int i = 0; i < DQ / 4; ++i) {
+                const float4 v = reinterpret_cast<const float4*>(qbuf + part * DQ)[i];
                 qr[4 * i] = v.x; qr[4 * i + 1] = v.y; qr[4 * i + 2] = v.z; qr[4 * i + 3] = v.w;
             }
             wq = nullptr;
@@ -338,8 +346,8 @@ struct Consumer<float, D, G> {
 
     __device__ void page(const uint8_t* kbase, const uint8_t* vbase, int warp, int lane, int t_lo, int t_hi,
                          bool partial, float sl2) {
-        const int tok0 = warp * 16;
-        const int tl = lane & 15, half = lane >> 4, t = tok0 + tl;
+        const int tok0 = warp * TPW;
+        const int tl = lane % TPW, qp = lane / TPW, t = tok0 + tl;
         // Independent partial sums per head (NA of them) keep the dot
         // product's FMA chain short; they are added once at the end.
         constexpr int NA = G == 1 ? 4 : (G == 2 ? 2 : 1);
@@ -349,9 +357,9 @@ struct Consumer<float, D, G> {
             #pragma unroll
             for (int a = 0; a < NA; ++a) part[j][a] = 0.f;
         // full unroll when the query sits in registers (its index must be static)
-        #pragma unroll (G >= 4 ? 2 : D / 8)
-        for (int c = 0; c < D / 8; ++c) {
-            const int col = half * (D / 2) + c * 4;          // first dimension of the chunk
+        #pragma unroll (G >= 4 ? 2 : DQ / 4)
+        for (int c = 0; c < DQ / 4; ++c) {
+            const int col = qp * DQ + c * 4;                 // first dimension of the chunk
             const float4 kv = *reinterpret_cast<const float4*>(kbase + swz128((col / 32) * 8192, t, (col % 32) / 4));
             #pragma unroll
             for (int j = 0; j < G; ++j) {
@@ -378,12 +386,14 @@ struct Consumer<float, D, G> {
         #pragma unroll
         for (int j = 0; j < G; ++j) {
             if (j < g) {
-                float sc = acc[j] + __shfl_xor_sync(0xffffffffu, acc[j], 16);
+                float sc = acc[j];
+                #pragma unroll
+                for (int sh = TPW; sh < 32; sh <<= 1) sc += __shfl_xor_sync(0xffffffffu, sc, sh);
                 sc = valid ? sc * sl2 : -INFINITY;
                 if (__any_sync(0xffffffffu, sc > m[j] + kLazyLog2)) {
                     float x = sc;
                     #pragma unroll
-                    for (int sh = 1; sh < 16; sh <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, sh));
+                    for (int sh = 1; sh < TPW; sh <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, sh));
                     const float n = fmaxf(m[j], x);
                     const float al = exp2_approx(m[j] - n);
                     m[j] = n;
@@ -392,15 +402,15 @@ struct Consumer<float, D, G> {
                     for (int e = 0; e < VD; ++e) o[j][e] *= al;
                 }
                 const float pj = exp2_approx(sc - m[j]);
-                if (half == 0) l[j] += pj;          // this lane's token; summed over lanes in stash()
-                // token tl goes to slot parity * 8 + index within its parity
-                if (half == 0) sp[j * 16 + (tl & 1) * 8 + (tl >> 1)] = pj;
+                if (qp == 0) l[j] += pj;            // this lane's token; summed over lanes in stash()
+                // token tl goes to slot parity * TPW / 2 + index within its parity
+                if (qp == 0) sp[j * TPW + (tl & 1) * (TPW / 2) + (tl >> 1)] = pj;
             }
         }
         __syncwarp();
-        const int par = half, dg = tl * VD;
+        const int par = lane >> 4, dg = (lane & 15) * VD;
         #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < TPW / 2; ++k) {
             const int row = tok0 + 2 * k + par;
             float v[VD];
             #pragma unroll
@@ -418,7 +428,7 @@ struct Consumer<float, D, G> {
             #pragma unroll
             for (int j = 0; j < G; ++j) {
                 if (j < g) {
-                    const float pk = sp[j * 16 + par * 8 + k];
+                    const float pk = sp[j * TPW + par * (TPW / 2) + k];
                     #pragma unroll
                     for (int e = 0; e < VD; ++e) o[j][e] = fmaf(pk, v[e], o[j][e]);
                 }
@@ -478,7 +488,7 @@ __device__ bool first_wave_item(const AttendArgs& a, const Lay& lay, int b, int 
     #pragma unroll
     for (int sh = 16; sh > 0; sh >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, sh);
     longest = (int)__reduce_max_sync(0xffffffffu, (unsigned)longest);
-    const int C = a.chunk_pages > 0 ? a.chunk_pages : choose_chunk(tot, longest, Hk, grid);
+    const int C = a.chunk_pages > 0 ? a.chunk_pages : choose_chunk(tot, longest, a.rows, Hk, grid);
     const int row = b / Hk, kvh = b % Hk;
     int part = 0;
     for (int v = lane; v < row; v += 32) part += Chunking(pages_of(v, &pos, &lo), C).nch;
@@ -495,10 +505,12 @@ __device__ bool first_wave_item(const AttendArgs& a, const Lay& lay, int b, int 
 // The kernel
 // ---------------------------------------------------------------------------
 template <typename T, int D, int G, typename Lay>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<T, D, G>::kThreads, 1)
 attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
               const __grid_constant__ AttendArgs a, const __grid_constant__ Lay lay) {
-    using C = Cfg<T, D>;
+    using C = Cfg<T, D, G>;
+    constexpr int kThreads = C::kThreads, kCW = C::kCW;
+    constexpr int kProducerWarp = C::kProducer, kSchedulerWarp = C::kScheduler, kEpilogueWarp = C::kEpilogue;
     // Multi-layer launch: item row v is row v % layer_rows of layer
     // v / layer_rows, whose pools, output and sinks come from `lay`.
     constexpr bool kMulti = std::is_same<Lay, AttendLayers>::value;
@@ -524,7 +536,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, kConsumerWarps);
+            mbar_init(bar_empty + 8 * s, kCW);
         }
         *s_issued = 0;
         *s_abort = 0;
@@ -534,7 +546,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             mbar_init(bar_iempty + 8 * s, 1);
         }
         for (int s = 0; s < C::kEpiSlots; ++s) {
-            mbar_init(bar_efull + 8 * s, kConsumerWarps * 32);
+            mbar_init(bar_efull + 8 * s, kCW * 32);
             mbar_init(bar_eempty + 8 * s, 1);
         }
         fence_barrier_init();
@@ -920,16 +932,16 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             auto merge4 = [&](int j, int d0, float& M, float& L, float (&O)[8]) {
                 M = kNegBig;
                 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, eml[w * kMaxGroup + j].x);
+                for (int w = 0; w < kCW; ++w) M = fmaxf(M, eml[w * C::kEpiHeads + j].x);
                 L = 0.f;
                 #pragma unroll
                 for (int e = 0; e < 8; ++e) O[e] = 0.f;
                 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float2 ml = eml[w * kMaxGroup + j];
+                for (int w = 0; w < kCW; ++w) {
+                    const float2 ml = eml[w * C::kEpiHeads + j];
                     const float f = exp2_approx(ml.x - M);
                     L += f * ml.y;
-                    const float4* src = reinterpret_cast<const float4*>(eo + (w * kMaxGroup + j) * C::kORow + d0);
+                    const float4* src = reinterpret_cast<const float4*>(eo + (w * C::kEpiHeads + j) * C::kORow + d0);
                     const float4 p0 = src[0], p1 = src[1];
                     O[0] += f * p0.x; O[1] += f * p0.y; O[2] += f * p0.z; O[3] += f * p0.w;
                     O[4] += f * p1.x; O[5] += f * p1.y; O[6] += f * p1.z; O[7] += f * p1.w;
@@ -1022,7 +1034,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
     uint32_t phase = 0;
     int eslot = 0;
     uint32_t ephase = 0;
-    const int tid = threadIdx.x;     // 0..127
+    const int tid = threadIdx.x;     // 0 .. kCW * 32 - 1
     bool ok = true;
     while (true) {
         if (!mbar_wait(bar_full + 8 * stage, phase)) {
@@ -1039,7 +1051,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             else
                 cs.begin(reinterpret_cast<const float*>(smem + C::kOffQ + stage * C::kQBytes),
                          reinterpret_cast<float*>(smem + C::kOffWarpQ + warp * C::kQBytes),
-                         reinterpret_cast<float*>(smem + C::kOffWarpP + warp * kMaxGroup * 16 * 4), lane, g);
+                         reinterpret_cast<float*>(smem + C::kOffWarpP + warp * G * (64 / kCW) * 4), lane, g);
         }
         {
             constexpr int P = C::kPagesPerStage;
@@ -1073,8 +1085,8 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
             break;
         }
         uint8_t* ep = epi_q + eslot * C::kEpiBytes;
-        cs.stash(reinterpret_cast<float2*>(ep + sizeof(Meta)) + warp * kMaxGroup,
-                 reinterpret_cast<float*>(ep + C::kEpiOffO) + warp * kMaxGroup * C::kORow, lane);
+        cs.stash(reinterpret_cast<float2*>(ep + sizeof(Meta)) + warp * C::kEpiHeads,
+                 reinterpret_cast<float*>(ep + C::kEpiOffO) + warp * C::kEpiHeads * C::kORow, lane);
         if (tid == 0) *reinterpret_cast<Meta*>(ep) = mt;
         mbar_arrive(bar_efull + 8 * eslot);
         if (++eslot == C::kEpiSlots) { eslot = 0; ephase ^= 1; }
@@ -1099,7 +1111,7 @@ attend_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__
 template <typename T, int D, int G, typename Lay = NoLayers>
 static cudaError_t launch_one(const AttendArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
                               int grid, bool programmatic, cudaStream_t stream, const Lay& lay = Lay{}) {
-    using C = Cfg<T, D>;
+    using C = Cfg<T, D, G>;
     auto kern = attend_kernel<T, D, G, Lay>;
     // The shared-memory opt-in is per function and device; setting it again is cheap.
     static int configured_mask = 0;   // bit per device id < 31
@@ -1113,7 +1125,7 @@ static cudaError_t launch_one(const AttendArgs& a, const CUtensorMap& k_map, con
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1165,8 +1177,9 @@ cudaError_t launch_attend_layers(const AttendArgs& a, const AttendLayers& lay, i
 }
 
 size_t attend_smem_bytes(int dtype, int head_dim) {
-    if (dtype == 0) return head_dim == 128 ? Cfg<__nv_bfloat16, 128>::kSmem : Cfg<__nv_bfloat16, 64>::kSmem;
-    return head_dim == 128 ? Cfg<float, 128>::kSmem : Cfg<float, 64>::kSmem;
+    if (dtype == 0)
+        return head_dim == 128 ? Cfg<__nv_bfloat16, 128, kMaxGroup>::kSmem : Cfg<__nv_bfloat16, 64, kMaxGroup>::kSmem;
+    return head_dim == 128 ? Cfg<float, 128, kMaxGroup>::kSmem : Cfg<float, 64, kMaxGroup>::kSmem;
 }
 
 }  // namespace pdattn

@@ -72,14 +72,17 @@ __host__ __device__ __forceinline__ int row_lo(int pos, int window) {
 
 // Pages per split.  A split costs its chunk a partial write and the row a
 // merge, so rows stay whole (up to kChunkMax pages) unless the longest row
-// exceeds twice the average work per CTA; only then do chunks aim at
-// kItemsPerCta items per CTA.  A sweep on GB300 (gpt-oss-20b, Llama layer)
-// found whole rows 4-21% faster wherever the balance allows them.
-__host__ __device__ __forceinline__ int choose_chunk(unsigned long long row_pages, int max_row_pages, int Hk,
-                                                     int grid) {
+// exceeds twice the average work per CTA, or there are fewer than two
+// (row, kv head) pairs per CTA; then chunks aim at kItemsPerCta (long rows)
+// or 2 * kItemsPerCta (few pairs) items per CTA.  Sweeps on GB300: whole
+// rows are 4-21% faster wherever the balance allows them (gpt-oss-20b, the
+// serving batch); 32 Llama rows (256 pairs) run 3% faster in 16-page chunks.
+__host__ __device__ __forceinline__ int choose_chunk(unsigned long long row_pages, int max_row_pages, int rows,
+                                                     int Hk, int grid) {
     const unsigned long long work = row_pages * (unsigned long long)Hk;   // page items
-    if ((unsigned long long)max_row_pages * grid <= 2ull * work) return kChunkMax;
-    const unsigned long long per = (unsigned long long)kItemsPerCta * grid;
+    const bool few_pairs = (long long)rows * Hk < 2ll * grid;
+    if (!few_pairs && (unsigned long long)max_row_pages * grid <= 2ull * work) return kChunkMax;
+    const unsigned long long per = (unsigned long long)(few_pairs ? 2 * kItemsPerCta : kItemsPerCta) * grid;
     const unsigned long long cc = (work + per - 1) / per;
     return (int)(cc < 1 ? 1 : (cc > kChunkMax ? kChunkMax : cc));
 }
@@ -117,7 +120,7 @@ __host__ __device__ inline int plan_max_items(int rows, int kv_heads, int pages_
     if (chunk_pages > 0) {
         n = rh * ((pages_per_row + chunk_pages - 1) / chunk_pages);
     } else {
-        long long a = (long long)kItemsPerCta * grid + rh;
+        long long a = 2ll * kItemsPerCta * grid + rh;   // the few-pairs target of choose_chunk
         long long b = rh * ((pages_per_row + kChunkMax - 1) / kChunkMax);
         n = a > b ? a : b;
     }

@@ -312,7 +312,7 @@ __device__ bool build_plan_small(const PrepArgs& a, const Lay& lay) {
             longest = max(longest, s_warp_max[w]);
         }
         const int c = a.chunk_pages;
-        s_chunk = c > 0 ? c : choose_chunk((unsigned long long)total, longest, Hk, a.grid_attend);
+        s_chunk = c > 0 ? c : choose_chunk((unsigned long long)total, longest, R, Hk, a.grid_attend);
     }
     __syncthreads();
     const int C = s_chunk;
@@ -430,7 +430,7 @@ __device__ void build_plan(const PrepArgs& a, const Lay& lay) {
     __syncthreads();
     if (tid == 0) {
         const int c = a.chunk_pages;
-        s_chunk = c > 0 ? c : choose_chunk(s_work, s_longest, Hk, a.grid_attend);
+        s_chunk = c > 0 ? c : choose_chunk(s_work, s_longest, R, Hk, a.grid_attend);
     }
     __syncthreads();
     const int C = s_chunk;

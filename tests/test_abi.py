@@ -137,14 +137,16 @@ def test_workspace_layout_bound_covers_every_plan():
             lo = max(0, p - window + 1) if window > 0 else 0
             n.append(p // 64 - lo // 64 + 1)
         W = sum(n) * Hk
-        if max(n) * grid <= 2 * W:
+        few_pairs = R * Hk < 2 * grid
+        if not few_pairs and max(n) * grid <= 2 * W:
             C = chunk_max                  # rows kept whole
         else:
-            C = min(max(math.ceil(W / (items_per_cta * grid)), 1), chunk_max)
+            per = (2 * items_per_cta if few_pairs else items_per_cta) * grid
+            C = min(max(math.ceil(W / per), 1), chunk_max)
         items = sum(Hk * math.ceil(x / C) for x in n)
         # at most one empty first-wave item per CTA (a row with a bad position)
         items += min(grid, R * Hk) if R <= 512 else 0
-        bound = max(items_per_cta * grid + R * Hk, R * Hk * math.ceil(Pg / chunk_max)) + grid
+        bound = max(2 * items_per_cta * grid + R * Hk, R * Hk * math.ceil(Pg / chunk_max)) + grid
         assert items <= bound
 
 

@@ -126,3 +126,11 @@ def test_full_size_gptoss_layer_pair():
     # the gpt-oss-20b shape at full size (64 rows, positions up to 4095):
     # both layers of the pair, every row
     run_layers(wl.GPTOSS_FULL, 2, windows=(128, 0), sink_heads=True, seed=6)
+
+
+def test_layers_beyond_the_first_wave_rows():
+    # 6 layers x 100 rows = 600 launch rows: more than the planner's one-row-
+    # per-thread path takes, so the general planner runs and no CTA starts early
+    w = wl.Workload("wide", rows=100, heads=16, kv_heads=4, head_dim=64, pages_per_row=4, dtype="bf16",
+                    rope_theta=10000.0, positions="uniform", pos_lo=0, pos_hi=255, seed=55)
+    run_layers(w, 6, windows=(0, 100, 7), sink_heads=True, seed=7, repeat=2)
