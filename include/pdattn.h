@@ -228,7 +228,7 @@ pdattn_status pdattn_decode_layers(const pdattn_params* p, int32_t n_layers, con
  * which every GPU that loads the library keeps until the process exits.
  * Parameters whose workspace (pdattn_workspace_size) exceeds 16 MiB are
  * rejected with PDATTN_EINVAL before any launch; the Llama-3.1-8B shape at
- * 256 rows needs about 10 MiB.  The first call on each device (with that
+ * 256 rows needs about 10.6 MiB.  The first call on each device (with that
  * device current) looks up the array's device address, which issues no work
  * on any stream; make that first call before capturing any stream.  All calls
  * on a device share the one array: calls whose work overlaps on the GPU

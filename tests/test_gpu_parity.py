@@ -231,3 +231,45 @@ def test_full_size_whole_batch(w):
     assert_close(out, out64, w.dtype, w.name)
     assert np.array_equal(wl.to_numpy(t["k_pool"]).view(np.uint8), kp.view(np.uint8)), "k pool differs"
     assert np.array_equal(wl.to_numpy(t["v_pool"]).view(np.uint8), vp.view(np.uint8)), "v pool differs"
+
+
+@pytest.mark.parametrize("mode", ["fused", "layers"])
+def test_decode_loop_with_advancing_positions(mode):
+    """A serving loop: ten steps on one workspace, each row's position one
+    further every step (crossing page boundaries), new q / k / v each step.
+    Every step's output is checked against the oracle, which runs the same
+    steps on its own copy of the pools; the pools are compared at the end."""
+    b = binding()
+    R, steps = 48, 10
+    rng = np.random.default_rng(21)
+    start = rng.integers(0, 6 * 64 - steps, R)
+    start[:6] = [54, 55, 62, 63, 118, 0]               # rows that cross page boundaries
+    w = W("loop", R=R, Pg=6, Hq=32, Hk=8, D=128, positions=tuple(int(x) for x in start + steps - 1), seed=21)
+    t = wl.generate(w, "cpu")
+    host = {k: wl.to_numpy(v) for k, v in t.items()}
+    kp, vp = host["k_pool"].copy(), host["v_pool"].copy()
+    num_pages = kp.shape[0]
+    shape = oracle_shape(w, num_pages)
+    tables = rope_tables_for(b, w)
+    p = gpu_params(b, w, num_pages, tables)
+    d = {k: v.cuda() for k, v in t.items()}
+    ws = b.new_layers_workspace(p, 1) if mode == "layers" else b.new_workspace(p)
+    gen = torch.Generator().manual_seed(22)
+    for s in range(steps):
+        pos = torch.tensor(start + s, dtype=torch.int32)
+        q = torch.randn(R, w.heads, w.head_dim, generator=gen).to(torch.bfloat16)
+        kn = torch.randn(R, w.kv_heads, w.head_dim, generator=gen).to(torch.bfloat16)
+        vn = torch.randn(R, w.kv_heads, w.head_dim, generator=gen).to(torch.bfloat16)
+        _, _, out64, rc = oracle.step(shape, wl.to_numpy(q), wl.to_numpy(kn), wl.to_numpy(vn), wl.to_numpy(pos),
+                                      host["table"], kp, vp)
+        assert rc == 0
+        out = torch.full((R, w.heads, w.head_dim), float("nan"), dtype=torch.bfloat16, device="cuda")
+        if mode == "fused":
+            b.decode_fused(p, q.cuda(), kn.cuda(), vn.cuda(), pos.cuda(), d["table"], d["k_pool"], d["v_pool"], out, ws)
+        else:
+            b.decode_layers(p, [dict(q=q.cuda(), k_new=kn.cuda(), v_new=vn.cuda(), k_pool=d["k_pool"],
+                                     v_pool=d["v_pool"], out=out)], pos.cuda(), d["table"], ws)
+        b.check_status(ws)
+        assert_close(out, out64, "bf16", f"step {s}")
+    assert np.array_equal(wl.to_numpy(d["k_pool"]).view(np.uint8), kp.view(np.uint8))
+    assert np.array_equal(wl.to_numpy(d["v_pool"]).view(np.uint8), vp.view(np.uint8))

@@ -66,7 +66,7 @@ def test_noalloc_matches_workspace_call_twice_in_a_row(chunk_pages):
 
 
 def test_noalloc_serving_batch_matches_the_oracle_twice_in_a_row():
-    # the Llama-3.1-8B serving batch (256 rows, about 10 MiB of scratch)
+    # the Llama-3.1-8B serving batch (256 rows, about 10.6 MiB of scratch)
     b = binding()
     w = wl.LLAMA_SERVING
     t = wl.generate(w, "cuda")
