@@ -36,8 +36,9 @@
 // is per key (same segment id, position <= the query's, inside the window),
 // from segment ids and positions copied into shared memory with each block.
 //
-// Warpgroups: 0 = warp 0 TMA producer, warp 1 TMEM owner and MMA issuer
-// (warps 2 and 3 idle); 1 and 2 = softmax and epilogue of halves A and B
+// Warpgroups: 0 = warp 0 TMA producer, warp 1 TMEM owner and MMA issuer,
+// warps 2 and 3 the V guard (they zero V rows outside a tile's key range
+// before the block's PV); 1 and 2 = softmax and epilogue of halves A and B
 // (warp w reads TMEM lanes 32 * (w % 4) .. + 31).  The issuing warpgroup
 // hands registers to the softmax warpgroups (setmaxnreg), which hold a
 // whole 128-key row of S.  Every wait is bounded; on a timeout the kernel
@@ -63,6 +64,7 @@ struct PfCfg {
     static constexpr int kStageBytes = 2 * kKBytes;       // K then V of one block
     static constexpr int kStages = D == 128 ? 2 : 5;
     static constexpr int kMaskStages = kPacked ? kStages : 1;
+    static_assert(kStages <= 8, "V ready barriers per stage");
     static constexpr int kOffQ = 0;                       // halves A, B
     static constexpr int kOffStage = 2 * kQBytes;
     static constexpr int kSmem = kOffStage + kStages * kStageBytes + 1024;   // + alignment slack
@@ -275,13 +277,14 @@ __device__ __forceinline__ int uni(int v) { return __shfl_sync(0xffffffffu, v, 0
 // of the descending-cost list (CTA b starts with unit b, later ones come
 // from a global cursor), so a CTA that finishes early takes more work.
 constexpr int kUnitSlots = 4;
-constexpr int kUnitReaders = 9;      // the issuing warp and the eight softmax warps
+constexpr int kUnitReaders = 11;     // the issuing warp, the two V guard warps and the eight softmax warps
 
 struct PfBars {
     uint64_t q_full[2], q_empty[2];   // [half]: Q loaded / every S of the unit reading it done
     uint64_t mma_done;
     uint64_t unit_full[kUnitSlots], unit_empty[kUnitSlots];
     uint64_t s_full[2];      // [half]: S of the block done (its previous PV too)
+    uint64_t v_ready[8];     // [stage]: V of the block landed and its rows outside the tile's range zeroed
     uint64_t p_full[2];      // [half]: P of the block written (one arrival per warp of the half)
     uint64_t o_done[2];      // [half]: the unit's last PV done
 };
@@ -301,7 +304,7 @@ __device__ __forceinline__ int take_unit(PfBars& bars, const int* s_unit, uint32
 // Softmax and epilogue of one half (128 threads, one MMA row each).
 template <int D, bool kPacked>
 __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile* tiles, int n_units, int half,
-                                             int quarter, int lane, uint32_t tmem, uint32_t st_s, PfBars& bars,
+                                             int quarter, int lane, uint32_t tmem, PfBars& bars,
                                              const int (*s_mask)[256], uint64_t* v_full, const int* s_unit,
                                              volatile int* abort, Ctrl* ctrl) {
     using C = PfCfg<D, kPacked>;
@@ -357,12 +360,19 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
             tmem_wait_ld();
             const int key0 = pg0 * kPageSize;
             if (by_index) {
-                // keys c of this block visible to the row: key_lo <= key0 + c <= key_hi
+                // keys c of this block visible to the row: key_lo <= key0 + c <= key_hi;
+                // 32-column chunks visible to every row of the warp skip the test
                 const int c_lo = key_lo - key0, c_hi = min(key_hi - key0, npb * kPageSize - 1);
                 if (!__all_sync(0xffffffffu, c_lo <= 0 && c_hi >= 2 * kPageSize - 1)) {
                     #pragma unroll
-                    for (int c = 0; c < 128; ++c)
-                        if (c < c_lo || c > c_hi) s[c] = __float_as_uint(-INFINITY);
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int b0 = 32 * q4;
+                        if (!__all_sync(0xffffffffu, c_lo <= b0 && c_hi >= b0 + 31)) {
+                            #pragma unroll
+                            for (int c = b0; c < b0 + 32; ++c)
+                                if (c < c_lo || c > c_hi) s[c] = __float_as_uint(-INFINITY);
+                        }
+                    }
                 }
             } else {
                 // key c is visible when it belongs to the row's sequence at a
@@ -441,22 +451,6 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
                 tmem_st32(s_addr + 32 * h64, pk);
             }
             l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-            // V rows outside every row's range hold no cached value of this
-            // tile (possibly stale or non-finite): half A zeroes them so that
-            // 0 * V stays 0 (the issuer runs PV_B after PV_A)
-            const int v_lo = t.lo_min - key0, v_hi = min(t.pos_max - key0, npb * kPageSize - 1);
-            if (half == 0 && (v_lo > 0 || v_hi < 2 * kPageSize - 1)) {
-                mbar_wait(smem_u32(&v_full[(it + b) % C::kStages]), ((it + b) / C::kStages) & 1, kPfTimeoutNs);
-                const uint32_t vb = st_s + ((it + b) % C::kStages) * C::kStageBytes + C::kKBytes;
-                for (int i = m; i < 2 * kPageSize * C::kBoxes * 8; i += 128) {
-                    const int r = i / (C::kBoxes * 8), rest = i % (C::kBoxes * 8);
-                    if (r < v_lo || r > v_hi)
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};"
-                                     ::"r"(vb + (rest >> 3) * 16384 + r * 128 + (rest & 7) * 16), "r"(0)
-                                     : "memory");
-                }
-                fence_proxy_async_shared();
-            }
             // every lane's stores are complete and fenced before its warp's
             // one arrival (128 single arrivals on one word serialise)
             tmem_wait_st();
@@ -537,6 +531,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             mbar_init(smem_u32(&k_empty[s]), 1);
             mbar_init(smem_u32(&v_full[s]), 1);
             mbar_init(smem_u32(&v_empty[s]), 1);
+            mbar_init(smem_u32(&bars.v_ready[s]), 2);
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(smem_u32(&bars.q_full[h]), 1);
@@ -579,8 +574,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (warp >= 4) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
         // ---------------- softmax + epilogue: warps 4..7 half A, 8..11 half B ----------------
-        softmax_half<D, kPacked>(a, tiles, n_units, (warp - 4) >> 2, warp & 3, lane, tmem, st_s, bars, s_mask,
-                                 v_full, s_unit, abort, ctrl);
+        softmax_half<D, kPacked>(a, tiles, n_units, (warp - 4) >> 2, warp & 3, lane, tmem, bars, s_mask, v_full,
+                                 s_unit, abort, ctrl);
     } else {
       // one setmaxnreg site for the whole issuing warpgroup
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
@@ -773,7 +768,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             for (int h = 0; h < 2; ++h) {
                 if ((f & kPend) && (h == 0 || (f & kPendB))) {
                     if (h == 0) {
-                        ok = warp_wait(smem_u32(&v_full[(it - 1) % C::kStages]), ((it - 1) / C::kStages) & 1, abort,
+                        ok = warp_wait(smem_u32(&bars.v_ready[(it - 1) % C::kStages]), ((it - 1) / C::kStages) & 1, abort,
                                        ctrl);
                         if (!ok) break;
                         tc_fence_after();
@@ -817,6 +812,81 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             umma_commit(smem_u32(&bars.mma_done));
             mbar_wait(smem_u32(&bars.mma_done), 0, kPfTimeoutNs);
         }
+      } else {
+        // ---------------- V guard (warps 2 and 3) ----------------
+        // V rows of a block outside the tile's key range [lo_min, pos_max]
+        // hold no key of the tile (stale cache slots, another sequence of
+        // the pack: possibly non-finite), and every row's weight there is 0:
+        // they are zeroed so that 0 * V stays 0 in PV.  The issuer starts a
+        // block's PV only once both warps have passed it.
+        // Tiles of a cache row or of a canonical pack see a key range; in a
+        // pack of any other layout a tile (one run, one segment id) sees the
+        // keys of its segment at positions <= its last query's (and inside
+        // the window of its first), row by row from the block's ids.
+        constexpr int kPieces = C::kBoxes * 8;         // 16-byte pieces of a V row
+        const int gw = warp - 2;
+        const bool by_key = kPacked && ctrl->rows == 0;
+        const int* seg_pad = reinterpret_cast<const int*>(a.ws + a.L.seg_pad);
+        const int W = a.window;
+        uint32_t it = 0;
+        bool ok = true;
+        for (uint32_t k = 0; ok; ++k) {
+            const int u = take_unit(bars, s_unit, k, lane, abort, ctrl);
+            if (u < 0) break;
+            const PfTile t = tiles[u / Hk];
+            const int npg = uni(t.npg), first = uni(t.first_page), lo_min = uni(t.lo_min), pos_max = uni(t.pos_max);
+            int tseg = 0, pmin = INT_MAX, pmax = -1;
+            if (by_key) {
+                const int t0 = uni(t.t0), ntok = uni(t.ntok);
+                tseg = seg_pad[t0];
+                for (int i = lane; i < ntok; i += 32) {
+                    const int p = max(__ldg(a.positions + t0 + i), 0);
+                    pmin = min(pmin, p);
+                    pmax = max(pmax, p);
+                }
+                #pragma unroll
+                for (int d = 16; d > 0; d >>= 1) {
+                    pmin = min(pmin, __shfl_xor_sync(0xffffffffu, pmin, d));
+                    pmax = max(pmax, __shfl_xor_sync(0xffffffffu, pmax, d));
+                }
+            }
+            for (int bk = 0; 2 * bk < npg; ++bk, ++it) {
+                const int st = it % C::kStages;
+                ok = warp_wait(smem_u32(&v_full[st]), (it / C::kStages) & 1, abort, ctrl);
+                if (!ok) break;
+                const int key0 = (first + 2 * bk) * kPageSize, rows = min(2, npg - 2 * bk) * kPageSize;
+                const uint32_t vb = st_s + st * C::kStageBytes + C::kKBytes;
+                auto zero_row = [&](int r) {
+                    #pragma unroll
+                    for (int piece = 0; piece < kPieces; ++piece)
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};"
+                                     ::"r"(vb + (piece >> 3) * 16384 + r * 128 + (piece & 7) * 16), "r"(0)
+                                     : "memory");
+                };
+                if (by_key) {
+                    // the block's segment ids and positions came with V
+                    bool any = false;
+                    for (int r = gw * 32 + lane; r < rows; r += 64) {
+                        const int sg = s_mask[kPacked ? st : 0][r], pp = s_mask[kPacked ? st : 0][128 + r];
+                        if (!(sg == tseg && pp <= pmax && (W <= 0 || pp > pmin - W))) {
+                            zero_row(r);
+                            any = true;
+                        }
+                    }
+                    if (__any_sync(0xffffffffu, any)) fence_proxy_async_shared();
+                } else {
+                    const int v_lo = max(lo_min - key0, 0), v_hi = min(pos_max - key0, rows - 1);   // rows kept
+                    const int n_lo = v_lo, n_hi = rows - 1 - v_hi;                                 // rows zeroed
+                    if (n_lo > 0 || n_hi > 0) {
+                        for (int zr = gw * 32 + lane; zr < n_lo + n_hi; zr += 64)
+                            zero_row(zr < n_lo ? zr : v_hi + 1 + (zr - n_lo));
+                        fence_proxy_async_shared();
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars.v_ready[st]));
+            }
+        }
       }
     }
 
@@ -857,11 +927,6 @@ cudaError_t launch_d(const PrefillArgs& a, const CUtensorMap& q_map, const CUten
     cfg.blockDim = dim3(kPfThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, q_map, k_map, v_map, a);
 }
 
