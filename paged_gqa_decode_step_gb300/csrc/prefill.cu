@@ -319,6 +319,7 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
     const int tq = m / g, jh = m % g;
     const float sl2 = a.scale_log2;
     const __nv_bfloat16* sinks = static_cast<const __nv_bfloat16*>(a.sinks);
+    const bool out_wide = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;   // rows are D * 2 bytes apart
     const uint32_t s_full = smem_u32(&bars.s_full[half]), p_full = smem_u32(&bars.p_full[half]);
     uint32_t it = 0, ch = 0, uh = 0;     // blocks of every unit / of units with this half; units with it
     bool ok = true;
@@ -426,37 +427,47 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
                     tmem_st32(o_addr + c0, o);
                 }
             }
-            // P as bf16 pairs over the first 64 columns of S; the denominator
+            // P as bf16 pairs over the first 64 columns of S.  The denominator
             // sums the same rounded weights, so the normalised weights are an
-            // exact convex combination
+            // exact convex combination.  Packs sum them after the hand-over,
+            // off the path to the next MMA; prefill sums them in line (there
+            // the deferred sum competes for issue with the other half's
+            // softmax and measured slower).
+            uint32_t pk[64];
             float acc[8];
+            auto add_pair = [&](int c) {
+                const float lw = __uint_as_float(pk[c] << 16), hw = __uint_as_float(pk[c] & 0xffff0000u);
+                const int q = c & 3;                      // four pair accumulators
+                if (c < 4) {
+                    acc[2 * q] = lw;
+                    acc[2 * q + 1] = hw;
+                } else {
+                    fadd2(acc[2 * q], acc[2 * q + 1], lw, hw);
+                }
+            };
             #pragma unroll
             for (int h64 = 0; h64 < 2; ++h64) {
-                uint32_t pk[32];
                 #pragma unroll
                 for (int c = 0; c < 64; c += 2) {
                     const int cc = 64 * h64 + c;
                     float x0, x1;
                     ffma2(x0, x1, __uint_as_float(s[cc]), __uint_as_float(s[cc + 1]), sl2, neg_mu);
-                    pk[c >> 1] = pack_bf16x2(exp2_approx(x0), exp2_approx(x1));
-                    const float lw = __uint_as_float(pk[c >> 1] << 16), hw = __uint_as_float(pk[c >> 1] & 0xffff0000u);
-                    const int k = (c >> 1) & 3;               // four pair accumulators
-                    if (h64 == 0 && c < 8) {
-                        acc[2 * k] = lw;
-                        acc[2 * k + 1] = hw;
-                    } else {
-                        fadd2(acc[2 * k], acc[2 * k + 1], lw, hw);
-                    }
+                    pk[cc >> 1] = pack_bf16x2(exp2_approx(x0), exp2_approx(x1));
+                    if constexpr (!kPacked) add_pair(cc >> 1);
                 }
-                tmem_st32(s_addr + 32 * h64, pk);
+                tmem_st32(s_addr + 32 * h64, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32 * h64]));
             }
-            l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
             // every lane's stores are complete and fenced before its warp's
             // one arrival (128 single arrivals on one word serialise)
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
+            if constexpr (kPacked) {
+                #pragma unroll
+                for (int c = 0; c < 64; ++c) add_pair(c);
+            }
+            l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         }
         if (!ok) break;
         // Epilogue: O / l (with the sink's share of the denominator).
@@ -473,20 +484,32 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
             inv = f / (l * f + exp2_approx(sk - Mp));
         }
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + ((size_t)(t.t0 + tok) * a.heads + h) * D;
+        // 64 columns per round trip to TMEM; 32-byte stores (whole sectors)
+        // when the output is 32-byte aligned, else 16-byte ones
         #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld32(o_addr + c0, o);
+        for (int c0 = 0; c0 < D; c0 += 64) {
+            uint32_t o[64];
+            tmem_ld32(o_addr + c0, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+            tmem_ld32(o_addr + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
             tmem_wait_ld();
             if (active) {
                 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
-                    uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-                    w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-                    w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-                    w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-                    *reinterpret_cast<uint4*>(orow + c0 + 8 * v) = w;
+                    uint32_t w[8];
+                    #pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        w[e] = pack_bf16x2(__uint_as_float(o[16 * v + 2 * e]) * inv,
+                                           __uint_as_float(o[16 * v + 2 * e + 1]) * inv);
+                    __nv_bfloat16* dst = orow + c0 + 16 * v;
+                    if (out_wide) {
+                        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                                     ::"l"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+                                       "r"(w[6]), "r"(w[7])
+                                     : "memory");
+                    } else {
+                        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    }
                 }
             }
         }

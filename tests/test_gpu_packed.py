@@ -24,7 +24,7 @@ def to_dev(a):
             for k, v in a.items()}
 
 
-def gpu_packed(w, a, sinks_t=None):
+def gpu_packed(w, a, sinks_t=None, misalign=False):
     b = binding()
     d = to_dev(a)
     cos, sin = b.rope_tables(w.rope_theta, w.head_dim, int(a["positions"].max()) + 1, torch.bfloat16)
@@ -32,14 +32,21 @@ def gpu_packed(w, a, sinks_t=None):
     p = b.make_params(1, w.heads, w.kv_heads, w.head_dim, 1, 1, torch.bfloat16, window=w.window, rope_cos=cos,
                       rope_sin=sin, sinks=sinks_t)
     ws = b.new_packed_workspace(p, len(a["positions"]))
-    out = torch.empty_like(d["q"])
+    if misalign:
+        # an output 16 but not 32 bytes aligned (the epilogue's narrow stores)
+        flat = torch.empty(d["q"].numel() + 16, dtype=d["q"].dtype, device=d["q"].device)
+        off = (8 - flat.data_ptr() % 32 // 2) % 16
+        out = flat[off:off + d["q"].numel()].view(d["q"].shape)
+        assert out.data_ptr() % 32 == 16
+    else:
+        out = torch.empty_like(d["q"])
     b.packed(p, d["q"], d["k"], d["v"], d["positions"], d["segments"], out, ws)
     b.check_status(ws)
     assert b.last_launch_count() == 3
     return out
 
 
-def run(w, sinks=None, q_scale=1.0, transform=None):
+def run(w, sinks=None, q_scale=1.0, transform=None, misalign=False):
     t = wl.generate_packed(w, "cpu")
     if q_scale != 1.0:
         t["q"] = (t["q"].float() * q_scale).to(torch.bfloat16)
@@ -52,7 +59,7 @@ def run(w, sinks=None, q_scale=1.0, transform=None):
     _, _, _, out64, rc = oracle.packed(shape, a["q"], a["k"], a["v"], a["positions"], a["segments"],
                                        None if sink_t is None else wl.to_numpy(sink_t))
     assert rc == 0
-    out = gpu_packed(w, a, None if sink_t is None else sink_t.cuda())
+    out = gpu_packed(w, a, None if sink_t is None else sink_t.cuda(), misalign)
     err = assert_close(out, out64, "bf16", w.name)
     print(f"{w.name}: max |err| {err[0]:.4g}, mean |err| {err[1]:.3g}")
 
@@ -63,6 +70,11 @@ def W(name, lengths, heads, kv_heads, head_dim, **kw):
 
 def test_packed_small_ragged():
     run(W("small", (40, 70, 5, 130), 8, 2, 64, seed=1))
+
+
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_packed_output_aligned_to_16_bytes_only(head_dim):
+    run(W("misaligned", (100, 33, 180), 16, 4, head_dim, rope_theta=500000.0, seed=14), misalign=True)
 
 
 @pytest.mark.parametrize("heads,kv_heads,head_dim", [

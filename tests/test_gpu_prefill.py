@@ -44,7 +44,18 @@ def to_dev(a):
             for k, v in a.items()}
 
 
-def run(w, sinks=None, **kw):
+def out_like(q, misalign):
+    # misalign: an output 16 but not 32 bytes aligned (the epilogue's narrow stores)
+    if not misalign:
+        return torch.empty_like(q)
+    flat = torch.empty(q.numel() + 16, dtype=q.dtype, device=q.device)
+    base = flat.data_ptr() % 32 // 2                 # elements past a 32-byte boundary
+    o = flat[(8 - base) % 16: (8 - base) % 16 + q.numel()].view(q.shape)
+    assert o.data_ptr() % 32 == 16
+    return o
+
+
+def run(w, sinks=None, misalign=False, **kw):
     b = binding()
     a = inputs(w, **kw)
     num_pages = a["k_pool"].shape[0]
@@ -62,7 +73,7 @@ def run(w, sinks=None, **kw):
                       window=w.window, rope_cos=cos, rope_sin=sin,
                       sinks=None if sink_t is None else sink_t.cuda())
     ws = b.new_prefill_workspace(p, w.tokens)
-    out = torch.empty_like(d["q"])
+    out = out_like(d["q"], misalign)
     b.prefill_paged(p, d["q"], d["k_new"], d["v_new"], d["positions"], d["rows"], d["slots"], d["table"],
                     d["k_pool"], d["v_pool"], out, ws)
     b.check_status(ws)
@@ -95,6 +106,11 @@ def test_prefill_groups_and_head_dims(heads, kv_heads, head_dim):
 
 def test_prefill_llama_shape():
     run(W("llama", (0, 1000, 300), (300, 100, 257), 32, 8, 128, rope_theta=500000.0, seed=3))
+
+
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_prefill_output_aligned_to_16_bytes_only(head_dim):
+    run(W("misaligned", (0, 200), (130, 70), 16, 4, head_dim, rope_theta=500000.0, seed=13), misalign=True)
 
 
 @pytest.mark.parametrize("window", [1, 64, 128, 200])
