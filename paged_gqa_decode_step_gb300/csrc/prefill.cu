@@ -226,6 +226,13 @@ __device__ __forceinline__ void fadd2(float& d0, float& d1, float b0, float b1) 
         : "+f"(d0), "+f"(d1) : "f"(b0), "f"(b1));
 }
 
+// a0 += low bf16 of p, a1 += high bf16 of p (exact widening, f32 adds).
+__device__ __forceinline__ void add_bf16x2_f32(float& a0, float& a1, uint32_t p) {
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n add.rn.f32.bf16 %0, lo, %0;\n"
+        " add.rn.f32.bf16 %1, hi, %1;\n}"
+        : "+f"(a0), "+f"(a1) : "r"(p));
+}
+
 // Max of 64 values as eight short independent chains.
 __device__ __forceinline__ float max64(const uint32_t (&s)[64]) {
     float acc[8];
@@ -289,13 +296,26 @@ struct PfBars {
     uint64_t o_done[2];      // [half]: the unit's last PV done
 };
 
-// The next unit from the producer's ring (whole warp): -1 once there is no
-// more work, -2 on abort.
-__device__ __forceinline__ int take_unit(PfBars& bars, const int* s_unit, uint32_t k, int lane, volatile int* abort,
-                                         Ctrl* ctrl) {
+// A slot of the unit ring: the unit and its tile descriptor, so that no
+// reader waits on a global load at a unit boundary.
+struct __align__(32) UnitSlot {
+    PfTile t;
+    int u;
+    int pad[7];
+};
+
+// The next unit from the producer's ring (whole warp) and its tile: -1 once
+// there is no more work, -2 on abort.
+__device__ __forceinline__ int take_unit(PfBars& bars, const UnitSlot* s_unit, uint32_t k, int lane,
+                                         volatile int* abort, Ctrl* ctrl, PfTile& t) {
     const int slot = k % kUnitSlots;
     if (!warp_wait(smem_u32(&bars.unit_full[slot]), (k / kUnitSlots) & 1, abort, ctrl)) return -2;
-    const int u = *reinterpret_cast<const volatile int*>(s_unit + slot);
+    const volatile int4* src = reinterpret_cast<const volatile int4*>(&s_unit[slot]);
+    const int4 t0 = make_int4(src[0].x, src[0].y, src[0].z, src[0].w);
+    const int4 t1 = make_int4(src[1].x, src[1].y, src[1].z, src[1].w);
+    const int u = src[2].x;
+    t.t0 = t0.x; t.ntok = t0.y; t.row = t0.z; t.first_page = t0.w;
+    t.npg = t1.x; t.lo_min = t1.y; t.pos_max = t1.z; t.pad = t1.w;
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&bars.unit_empty[slot]));
     return u;
@@ -305,7 +325,7 @@ __device__ __forceinline__ int take_unit(PfBars& bars, const int* s_unit, uint32
 template <int D, bool kPacked>
 __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile* tiles, int n_units, int half,
                                              int quarter, int lane, uint32_t tmem, PfBars& bars,
-                                             const int (*s_mask)[256], uint64_t* v_full, const int* s_unit,
+                                             const int (*s_mask)[256], uint64_t* v_full, const UnitSlot* s_unit,
                                              volatile int* abort, Ctrl* ctrl) {
     using C = PfCfg<D, kPacked>;
     const int* seg_pad = reinterpret_cast<const int*>(a.ws + a.L.seg_pad);
@@ -321,30 +341,43 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
     const __nv_bfloat16* sinks = static_cast<const __nv_bfloat16*>(a.sinks);
     const bool out_wide = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;   // rows are D * 2 bytes apart
     const uint32_t s_full = smem_u32(&bars.s_full[half]), p_full = smem_u32(&bars.p_full[half]);
+    // A canonical pack (every sequence one run, positions rising) without a
+    // window sees exactly the tokens [run start, own index] of the pack.
+    const bool by_index = !kPacked || canonical_no_window;
+    const int tok = half * Tq + tq;                       // token of this row within a tile
     uint32_t it = 0, ch = 0, uh = 0;     // blocks of every unit / of units with this half; units with it
     bool ok = true;
-    for (uint32_t k = 0; ok; ++k) {
-        const int u = take_unit(bars, s_unit, k, lane, abort, ctrl);
-        if (u < 0) break;
-        const PfTile t = tiles[u / Hk];
+    // The row's position (and segment id) of a unit load while the previous
+    // unit's epilogue runs: the next unit is taken before it.
+    uint32_t k = 0;
+    PfTile t;
+    int u = take_unit(bars, s_unit, k++, lane, abort, ctrl, t);
+    int pos_next = -1, seg_next = 0;
+    auto row_inputs = [&](const PfTile& tt, int& p, int& sg) {
+        p = -1;
+        sg = 0;
+        if (tq < Tq && tok < tt.ntok) {
+            p = __ldg(a.positions + tt.t0 + tok);
+            if (!by_index) sg = seg_pad[tt.t0 + tok];
+        }
+    };
+    if (u >= 0) row_inputs(t, pos_next, seg_next);
+    while (u >= 0) {
         const int kvh = u % Hk, nb = (t.npg + 1) / 2;
         const bool present = half == 0 || t.ntok > Tq;
         if (!present) {
             it += nb;
+            u = take_unit(bars, s_unit, k++, lane, abort, ctrl, t);
+            if (u >= 0) row_inputs(t, pos_next, seg_next);
             continue;
         }
-        const int tok = half * Tq + tq;                   // token of this row within the tile
         const bool active = tq < Tq && tok < t.ntok;
-        int pos = -1, lo = 0, seg = 0;
+        int pos = -1, lo = 0;
+        const int seg = seg_next;
         if (active) {
-            pos = __ldg(a.positions + t.t0 + tok);
-            pos = pos < 0 ? 0 : pos;
+            pos = pos_next < 0 ? 0 : pos_next;
             lo = (W > 0 && pos - W + 1 > 0) ? pos - W + 1 : 0;
-            if (kPacked) seg = seg_pad[t.t0 + tok];
         }
-        // A canonical pack (every sequence one run, positions rising) without
-        // a window sees exactly the tokens [run start, own index] of the pack.
-        const bool by_index = !kPacked || canonical_no_window;
         const int key_lo = kPacked ? t.pad : lo, key_hi = kPacked ? (active ? t.t0 + tok : -1) : pos;
         float m_run = -INFINITY, l = 0.f;
         for (int b = 0; b < nb; ++b) {
@@ -435,14 +468,24 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
             // softmax and measured slower).
             uint32_t pk[64];
             float acc[8];
-            auto add_pair = [&](int c) {
-                const float lw = __uint_as_float(pk[c] << 16), hw = __uint_as_float(pk[c] & 0xffff0000u);
+            // (in line: bf16 + f32 adds; deferred: the pair unpacked, one f32x2
+            // add; each measured faster where it is used)
+            auto add_pair = [&](int c, uint32_t p) {
                 const int q = c & 3;                      // four pair accumulators
-                if (c < 4) {
-                    acc[2 * q] = lw;
-                    acc[2 * q + 1] = hw;
+                if constexpr (!kPacked) {
+                    if (c < 4) {
+                        acc[2 * q] = 0.f;
+                        acc[2 * q + 1] = 0.f;
+                    }
+                    add_bf16x2_f32(acc[2 * q], acc[2 * q + 1], p);
                 } else {
-                    fadd2(acc[2 * q], acc[2 * q + 1], lw, hw);
+                    const float lw = __uint_as_float(p << 16), hw = __uint_as_float(p & 0xffff0000u);
+                    if (c < 4) {
+                        acc[2 * q] = lw;
+                        acc[2 * q + 1] = hw;
+                    } else {
+                        fadd2(acc[2 * q], acc[2 * q + 1], lw, hw);
+                    }
                 }
             };
             #pragma unroll
@@ -453,7 +496,7 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
                     float x0, x1;
                     ffma2(x0, x1, __uint_as_float(s[cc]), __uint_as_float(s[cc + 1]), sl2, neg_mu);
                     pk[cc >> 1] = pack_bf16x2(exp2_approx(x0), exp2_approx(x1));
-                    if constexpr (!kPacked) add_pair(cc >> 1);
+                    if constexpr (!kPacked) add_pair(cc >> 1, pk[cc >> 1]);
                 }
                 tmem_st32(s_addr + 32 * h64, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32 * h64]));
             }
@@ -465,11 +508,15 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
             if (lane == 0) mbar_arrive(p_full);
             if constexpr (kPacked) {
                 #pragma unroll
-                for (int c = 0; c < 64; ++c) add_pair(c);
+                for (int c = 0; c < 64; ++c) add_pair(c, pk[c]);
             }
             l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         }
         if (!ok) break;
+        // The next unit, whose row inputs load under this epilogue.
+        PfTile tn;
+        const int un = take_unit(bars, s_unit, k++, lane, abort, ctrl, tn);
+        if (un >= 0) row_inputs(tn, pos_next, seg_next);
         // Epilogue: O / l (with the sink's share of the denominator).
         ok = warp_wait(smem_u32(&bars.o_done[half]), uh & 1, abort, ctrl);
         if (!ok) break;
@@ -519,6 +566,8 @@ __device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile*
         ch += nb;
         it += nb;
         ++uh;
+        u = un;
+        t = tn;
     }
 }
 
@@ -534,7 +583,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     __shared__ __align__(8) uint64_t v_full[C::kStages], v_empty[C::kStages];
     __shared__ __align__(8) PfBars bars;
     __shared__ __align__(16) int s_mask[C::kMaskStages][256];   // packed: segment ids [0,128), positions [128,256)
-    __shared__ int s_unit[kUnitSlots];
+    __shared__ UnitSlot s_unit[kUnitSlots];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -614,15 +663,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 u = __shfl_sync(0xffffffffu, v, 0);
             }
             const int slot = k % kUnitSlots;
+            PfTile t = {};
+            if (u < n_units) t = tiles[u / Hk];
             ok = warp_wait(smem_u32(&bars.unit_empty[slot]), ((k / kUnitSlots) & 1) ^ 1, abort, ctrl);
             if (!ok) break;
             if (lane == 0) {
-                s_unit[slot] = u < n_units ? u : -1;
+                int4* dst = reinterpret_cast<int4*>(&s_unit[slot]);
+                dst[0] = make_int4(t.t0, t.ntok, t.row, t.first_page);
+                dst[1] = make_int4(t.npg, t.lo_min, t.pos_max, t.pad);
+                dst[2] = make_int4(u < n_units ? u : -1, 0, 0, 0);
                 mbar_arrive(smem_u32(&bars.unit_full[slot]));
             }
             __syncwarp();
             if (u >= n_units) break;
-            const PfTile t = tiles[u / Hk];
             const int kvh = u % Hk, nh = uni(t.ntok > Tq ? 2 : 1), npg = uni(t.npg), t0 = uni(t.t0);
             const int first = uni(t.first_page), row = uni(t.row), nb = (npg + 1) / 2;
             const int* trow = kPacked ? nullptr : a.table + (size_t)row * a.pages_per_row + first;
@@ -769,7 +822,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     ++uq0;
                     if (nh == 2) ++uq1;
                 }
-                const int u = take_unit(bars, s_unit, k++, lane, abort, ctrl);
+                PfTile t;
+                const int u = take_unit(bars, s_unit, k++, lane, abort, ctrl, t);
                 if (u == -2) {
                     ok = false;
                     break;
@@ -780,7 +834,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 if (u < 0) {
                     f |= kEnd;
                 } else {
-                    const PfTile t = tiles[u / Hk];
                     nh = uni(t.ntok > Tq ? 2 : 1);
                     npg = uni(t.npg);
                 }
@@ -854,13 +907,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         uint32_t it = 0;
         bool ok = true;
         for (uint32_t k = 0; ok; ++k) {
-            const int u = take_unit(bars, s_unit, k, lane, abort, ctrl);
+            PfTile t;
+            const int u = take_unit(bars, s_unit, k, lane, abort, ctrl, t);
             if (u < 0) break;
-            const PfTile t = tiles[u / Hk];
-            const int npg = uni(t.npg), first = uni(t.first_page), lo_min = uni(t.lo_min), pos_max = uni(t.pos_max);
+            const int npg = t.npg, first = t.first_page, lo_min = t.lo_min, pos_max = t.pos_max;
             int tseg = 0, pmin = INT_MAX, pmax = -1;
             if (by_key) {
-                const int t0 = uni(t.t0), ntok = uni(t.ntok);
+                const int t0 = t.t0, ntok = t.ntok;
                 tseg = seg_pad[t0];
                 for (int i = lane; i < ntok; i += 32) {
                     const int p = max(__ldg(a.positions + t0 + i), 0);
