@@ -169,12 +169,12 @@ def test_packed_attend_reruns_the_attention_bit_for_bit():
         assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
 
 
-@pytest.mark.parametrize("scatter", [False, True])
-def test_packed_non_finite_keys_and_values_stay_in_their_sequence(scatter):
+@pytest.mark.parametrize("scatter,window", [(False, 0), (True, 0), (False, 100), (True, 100)])
+def test_packed_non_finite_keys_and_values_stay_in_their_sequence(scatter, window):
     # K and V of one sequence hold inf / NaN: that sequence's outputs are
     # undefined, every other sequence's must match the oracle (its keys never
     # see them: masked scores, zeroed V rows in the shared key blocks)
-    w = W("poison", (70, 150, 90, 200), 32, 8, 128, rope_theta=500000.0, seed=11)
+    w = W("poison", (70, 150, 90, 200), 32, 8, 128, rope_theta=500000.0, window=window, seed=11)
     t = wl.generate_packed(w, "cpu")
     a = {k: wl.to_numpy(v) for k, v in t.items()}
     starts = np.concatenate([[0], np.cumsum(w.lengths)])
@@ -187,7 +187,8 @@ def test_packed_non_finite_keys_and_values_stay_in_their_sequence(scatter):
         perm = np.random.default_rng(12).permutation(len(bad))
         a = {k: np.ascontiguousarray(v[perm]) for k, v in a.items()}
         bad = bad[perm]
-    shape = oracle.make_shape(0, w.heads, w.kv_heads, w.head_dim, 1, 1, oracle.BF16, rope_theta=w.rope_theta)
+    shape = oracle.make_shape(0, w.heads, w.kv_heads, w.head_dim, 1, 1, oracle.BF16, window=w.window,
+                              rope_theta=w.rope_theta)
     _, _, _, out64, rc = oracle.packed(shape, a["q"], a["k"], a["v"], a["positions"], a["segments"])
     assert rc == 0
     out = gpu_packed(w, a).cpu()
