@@ -915,9 +915,15 @@ __global__ void __launch_bounds__(kPrepThreads) packed_plan_kernel(const __grid_
     build_packed_plan(a);
 }
 
+// The per-token rope kernels wait on their loads: twelve resident 128-thread
+// blocks (at most 40 registers a thread) keep more loads in flight than the
+// eleven that 44 registers allow; sixteen (32 registers) spill and measured
+// slower.
+constexpr int kRopeBlocksPerSm = 12;
+
 // Block i rotates q and k of packed token i into the workspace.
 template <typename T>
-__global__ void __launch_bounds__(128) packed_rope_kernel(const __grid_constant__ PrefillPrepArgs a) {
+__global__ void __launch_bounds__(128, kRopeBlocksPerSm) packed_rope_kernel(const __grid_constant__ PrefillPrepArgs a) {
     griddep_launch_dependents();
     const int i = blockIdx.x, D = a.head_dim, Hq = a.heads, Hk = a.kv_heads;
     const int pos = __ldg(a.positions + i);
@@ -951,7 +957,7 @@ __global__ void __launch_bounds__(kPrepThreads) prefill_plan_kernel(const __grid
 constexpr int kRopeThreads = 128;
 
 template <typename T>
-__global__ void __launch_bounds__(kRopeThreads) prefill_rope_kernel(const __grid_constant__ PrefillPrepArgs a) {
+__global__ void __launch_bounds__(kRopeThreads, kRopeBlocksPerSm) prefill_rope_kernel(const __grid_constant__ PrefillPrepArgs a) {
     griddep_launch_dependents();
     rope_write_token<T>(a, blockIdx.x);
     if (blockIdx.x == gridDim.x - 1) griddep_wait();
