@@ -27,7 +27,9 @@
 //
 // Units are taken in the planner's descending-cost order: CTA b starts with
 // unit b, later ones come from a global cursor that the last CTA out rewinds.
-// K and V of a stage fill and drain on separate barriers.
+// The producer passes each unit with its tile descriptor to the other roles
+// through a small shared-memory ring.  K and V of a stage fill and drain on
+// separate barriers.
 //
 // Packed sequences (Llama example page, `packed`) run the same kernel: the
 // pack is a contiguous cache of 64-token pages, K and V come by 3-D TMA from
@@ -37,8 +39,8 @@
 // from segment ids and positions copied into shared memory with each block.
 //
 // Warpgroups: 0 = warp 0 TMA producer, warp 1 TMEM owner and MMA issuer,
-// warps 2 and 3 the V guard (they zero V rows outside a tile's key range
-// before the block's PV); 1 and 2 = softmax and epilogue of halves A and B
+// warps 2 and 3 the V guard (before a block's PV they zero the V rows no
+// query of the tile may see); 1 and 2 = softmax and epilogue of halves A and B
 // (warp w reads TMEM lanes 32 * (w % 4) .. + 31).  The issuing warpgroup
 // hands registers to the softmax warpgroups (setmaxnreg), which hold a
 // whole 128-key row of S.  Every wait is bounded; on a timeout the kernel
