@@ -325,10 +325,9 @@ __device__ __forceinline__ int take_unit(PfBars& bars, const UnitSlot* s_unit, u
 
 // Softmax and epilogue of one half (128 threads, one MMA row each).
 template <int D, bool kPacked>
-__device__ __forceinline__ void softmax_half(const PrefillArgs& a, const PfTile* tiles, int n_units, int half,
-                                             int quarter, int lane, uint32_t tmem, PfBars& bars,
-                                             const int (*s_mask)[256], uint64_t* v_full, const UnitSlot* s_unit,
-                                             volatile int* abort, Ctrl* ctrl) {
+__device__ __forceinline__ void softmax_half(const PrefillArgs& a, int half, int quarter, int lane, uint32_t tmem,
+                                             PfBars& bars, const int (*s_mask)[256], uint64_t* v_full,
+                                             const UnitSlot* s_unit, volatile int* abort, Ctrl* ctrl) {
     using C = PfCfg<D, kPacked>;
     const int* seg_pad = reinterpret_cast<const int*>(a.ws + a.L.seg_pad);
     const int4* blk = reinterpret_cast<const int4*>(a.ws + a.L.blk);
@@ -648,8 +647,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (warp >= 4) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
         // ---------------- softmax + epilogue: warps 4..7 half A, 8..11 half B ----------------
-        softmax_half<D, kPacked>(a, tiles, n_units, (warp - 4) >> 2, warp & 3, lane, tmem, bars, s_mask, v_full,
-                                 s_unit, abort, ctrl);
+        softmax_half<D, kPacked>(a, (warp - 4) >> 2, warp & 3, lane, tmem, bars, s_mask, v_full, s_unit, abort,
+                                 ctrl);
     } else {
       // one setmaxnreg site for the whole issuing warpgroup
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
