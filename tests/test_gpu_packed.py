@@ -169,12 +169,13 @@ def test_packed_attend_reruns_the_attention_bit_for_bit():
         assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
 
 
-@pytest.mark.parametrize("scatter,window", [(False, 0), (True, 0), (False, 100), (True, 100)])
-def test_packed_non_finite_keys_and_values_stay_in_their_sequence(scatter, window):
+@pytest.mark.parametrize("scatter,window,head_dim", [(False, 0, 128), (True, 0, 128), (False, 100, 128),
+                                                      (True, 100, 128), (False, 0, 64), (True, 100, 64)])
+def test_packed_non_finite_keys_and_values_stay_in_their_sequence(scatter, window, head_dim):
     # K and V of one sequence hold inf / NaN: that sequence's outputs are
     # undefined, every other sequence's must match the oracle (its keys never
     # see them: masked scores, zeroed V rows in the shared key blocks)
-    w = W("poison", (70, 150, 90, 200), 32, 8, 128, rope_theta=500000.0, window=window, seed=11)
+    w = W("poison", (70, 150, 90, 200), 32, 8, head_dim, rope_theta=500000.0, window=window, seed=11)
     t = wl.generate_packed(w, "cpu")
     a = {k: wl.to_numpy(v) for k, v in t.items()}
     starts = np.concatenate([[0], np.cumsum(w.lengths)])
