@@ -272,6 +272,8 @@ size_t pdattn_prefill_workspace_size(const pdattn_params* p, int32_t n_tokens);
  * list; a row index outside [0, rows) or a bad position is recorded as
  * PDATTN_EBADPOS and the call writes no output; a slot outside the pools
  * is recorded as PDATTN_EBADPAGE and that token's k / v are not written.
+ * Cache slots outside a tile's key range never reach an output, whatever
+ * they hold (non-finite values included).
  */
 pdattn_status pdattn_prefill_paged(const pdattn_params* p, int32_t n_tokens, const void* q,
                                    const void* k_new, const void* v_new, const int32_t* positions,
@@ -314,7 +316,9 @@ size_t pdattn_packed_workspace_size(const pdattn_params* p, int32_t n_tokens);
  * tokens with strictly increasing positions (as packing lays them out);
  * any other layout is handled exactly but visits the whole pack per tile.
  * A negative position or one past the rope table is recorded as
- * PDATTN_EBADPOS and no output is written.
+ * PDATTN_EBADPOS and no output is written.  The keys and values of one
+ * sequence never reach another sequence's outputs, non-finite ones
+ * included.
  */
 pdattn_status pdattn_packed(const pdattn_params* p, int32_t n_tokens, const void* q, const void* k,
                             const void* v, const int32_t* positions, const int32_t* segments,
